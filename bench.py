@@ -1,0 +1,377 @@
+"""Benchmark of the canvas attention block on GB300.
+
+One bench step = one canvas of the 48-step denoising loop (T=512 canvas rows, ctx=8192 cached
+rows, nh=8, nkv=4, hd=256): the cache is prepared once, then 48 forwards run, each on a fresh
+canvas Q/K/V (seed 3 + step) resident in HBM.  The metric is useful attention TFLOP/s
+(4 * T * nh * (ctx + T) * hd per forward).
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle instead, on a bounded
+sample of the same workload.  With torchrun (N > 1) each rank runs an independent replica on its
+own GPU (the block has no cross-GPU exchange); value = work of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "canvas-attention TFLOP/s and us/denoise-step, % of TF32 tensor peak"
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio of the part
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="denoise48_ctx8k")
+    ap.add_argument("--path", default="tc", choices=["tc", "fp32"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, budget_s: float, rows_per_call: int = None):
+    """Time the fp64 oracle on whole denoising steps' canvas rows until ~budget_s of CPU work.
+
+    Returns (useful flops computed, seconds, threads, description)."""
+    import oracle
+    from gqa_canvas_attention_gb300.workloads import EPS, ROPE_THETA, shared_cache, workload_inputs
+
+    threads = oracle.set_threads(0)
+    kc, vc = shared_cache(w)
+    kc, vc = kc.numpy(), vc.numpy()
+    per_row = 4 * w.nh * w.S * w.hd
+    # calibrate on a few rows of step 0
+    d = workload_inputs(w, step=0)
+    t0 = time.perf_counter()
+    oracle.forward(d["q"].numpy(), d["k_canvas"].numpy(), d["v_canvas"].numpy(), kc, vc, w.nh,
+                   w.nkv, w.hd, None if d["q_norm_w"] is None else d["q_norm_w"].numpy(),
+                   None if d["k_norm_w"] is None else d["k_norm_w"].numpy(), eps=EPS,
+                   theta=ROPE_THETA, rows=(0, 16))
+    t_row = (time.perf_counter() - t0) / 16
+    rows_total = max(1, int(budget_s / max(t_row, 1e-9)))
+    rows = min(w.T, rows_total) if rows_per_call is None else rows_per_call
+    flops, secs, step, done = 0, 0.0, 0, 0
+    while done < rows_total and step < w.steps:
+        d = workload_inputs(w, step=step)
+        r = min(rows, rows_total - done)
+        t0 = time.perf_counter()
+        oracle.forward(d["q"].numpy(), d["k_canvas"].numpy(), d["v_canvas"].numpy(), kc, vc,
+                       w.nh, w.nkv, w.hd,
+                       None if d["q_norm_w"] is None else d["q_norm_w"].numpy(),
+                       None if d["k_norm_w"] is None else d["k_norm_w"].numpy(), eps=EPS,
+                       theta=ROPE_THETA, rows=(0, r))
+        secs += time.perf_counter() - t0
+        flops += per_row * r
+        done += r
+        step += 1
+    desc = (f"{done} canvas rows x {w.nh} heads over {step} denoising step(s) of {w.name} "
+            f"(ctx={w.ctx}, T={w.T}, hd={w.hd}), fp64, OpenMP over (row, head)")
+    return flops, secs, threads, desc
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step_budget / 4)
+    flops, secs = 0, 0.0
+    desc = ""
+    threads = 1
+    for _ in range(args.steps):
+        f, s, threads, desc = oracle_sample(w, per_step_budget)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv,
+                   "hd": w.hd, "denoise_steps": w.steps},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def main():
+    args = parse()
+    from gqa_canvas_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from gqa_canvas_attention_gb300 import binding as B
+    from gqa_canvas_attention_gb300.workloads import EPS, ROPE_THETA, shared_cache, workload_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # ---------------------------------------------------------------- inputs (resident)
+    n_fwd = w.forwards()
+    kc, vc = (None, None)
+    if w.ctx > 0:
+        kc, vc = shared_cache(w)
+        kc, vc = kc.to(dev), vc.to(dev)
+    canv = []
+    for i in range(n_fwd):
+        d = workload_inputs(w, step=i) if w.canvases == 1 else workload_inputs(w, canvas=i)
+        canv.append({k: d[k].to(dev) if d[k] is not None else None
+                     for k in ("q", "k_canvas", "v_canvas", "q_norm_w", "k_norm_w")})
+    out = torch.empty((w.T, w.nh * w.hd), dtype=torch.float32, device=dev)
+
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, B.DG_PATH_TC if args.path == "tc" else B.DG_PATH_FP32)
+    if args.splits:
+        plan.set(B.DG_OPT_SPLITS, args.splits)
+    splits = plan.get(B.DG_INFO_SPLITS_USED)
+
+    def one_step():
+        """One canvas: cache conversion once, then every denoising step's forward."""
+        if w.ctx > 0:
+            plan.cache_prepare(kc, vc)
+        for c in canv:
+            plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
+                         c["k_norm_w"], None, out)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    if plan.sync_status() != B.DG_OK:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    # ---------------------------------------------------------------- timed region
+    plan.set(B.DG_OPT_PROFILE, 1)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if plan.sync_status() != B.DG_OK:
+        raise RuntimeError("device wait timed out in the timed region")
+    attn_ms, attn_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_ATTENTION)
+    norm_ms, norm_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_NORM_ROPE)
+    comb_ms, comb_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_COMBINE)
+    cache_ms, cache_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_CACHE)
+    plan.set(B.DG_OPT_PROFILE, 0)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    flops_fwd = w.flops_per_forward()
+    flops_step = flops_fwd * n_fwd
+    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
+    ms_per_step = ms / args.steps
+
+    # ---------------------------------------------------------------- roofline of the kernels
+    peaks, src = measured_peaks()
+    tf32_peak = peaks["bf16_tflops_sustained"] * NOMINAL_TF32_OVER_BF16
+    attn_avg_s = attn_ms / max(1, attn_n) / 1e3
+    attn_tflops = flops_fwd / attn_avg_s / 1e12
+    norm_bytes = 2 * 4 * w.T * (w.nh + 2 * w.nkv) * w.hd     # fp32 in + 4 bytes out per element
+    norm_avg_s = norm_ms / max(1, norm_n) / 1e3
+    norm_gbs = norm_bytes / norm_avg_s / 1e9
+
+    # ---------------------------------------------------------------- end to end from host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda t: None if t is None else t.cpu().pin_memory()
+        h_kc, h_vc = pin(kc), pin(vc)
+        h_canv = [{k: pin(v) for k, v in c.items()} for c in canv]
+        h_out = torch.empty((w.T, w.nh * w.hd), dtype=torch.float32).pin_memory()
+        d_in = {k: torch.empty_like(v) if v is not None else None for k, v in canv[0].items()}
+        h2d = (0 if kc is None else (kc.numel() + vc.numel()) * 4)
+        h2d += sum(v.numel() * 4 for v in canv[0].values() if v is not None) * n_fwd
+        d2h = out.numel() * 4 * n_fwd
+        d_kc = torch.empty_like(kc) if kc is not None else None
+        d_vc = torch.empty_like(vc) if vc is not None else None
+
+        def e2e_step():
+            if kc is not None:
+                d_kc.copy_(h_kc, non_blocking=True)
+                d_vc.copy_(h_vc, non_blocking=True)
+                plan.cache_prepare(d_kc, d_vc)
+            for hc in h_canv:
+                for k, v in hc.items():
+                    if v is not None:
+                        d_in[k].copy_(v, non_blocking=True)
+                plan.forward(d_in["q"], d_in["k_canvas"], d_in["v_canvas"], None, None,
+                             d_in["q_norm_w"], d_in["k_norm_w"], None, out)
+                h_out.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": flops_step * args.e2e_steps * world / (ems / 1e3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ems / args.e2e_steps}
+
+    launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (2 + (1 if splits > 1 else 0))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16x3+tf32" if args.path == "tc" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv,
+                   "hd": w.hd, "denoise_steps": w.steps, "canvases": w.canvases,
+                   "path": args.path, "splits": splits,
+                   "l2": "inputs larger than L2 (fresh canvas per step, 8 MiB x 48 + 64 MiB cache)"},
+        "us_per_denoise_step": ms_per_step * 1e3 / n_fwd,
+        "canvas_steps_per_s": n_fwd * args.steps * world / (ms / 1e3),
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf32_peak,
+                     "unit": "TFLOP/s", "frac": attn_tflops / tf32_peak, "traffic": None,
+                     "kernel": "attn_tc_kernel" if args.path == "tc" else "attn_fp32_kernel",
+                     "peak_source": f"{src}: bf16_tflops_sustained x nominal tf32/bf16 (1.1/2.25)",
+                     "avg_launch_us": attn_avg_s * 1e6, "launches": attn_n},
+        "norm_rope": {"bound": "hbm", "achieved": norm_gbs, "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": norm_gbs / peaks["hbm_gbs"],
+                      "avg_launch_us": norm_avg_s * 1e6, "bytes_per_launch": norm_bytes},
+        "stage_ms_per_step": {"norm_rope": norm_ms / args.steps, "attention": attn_ms / args.steps,
+                              "combine": comb_ms / args.steps, "cache": cache_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        f, s, threads, desc = oracle_sample(w, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    plan.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+"""ctypes binding of libdgattn.so (include/dg_attn.h), names unchanged.
+
+Argument marshalling only: torch tensors become device pointers, the current torch stream becomes
+the ``cudaStream_t``.  Every step of the block runs in the library's CUDA kernels; if the library
+is missing this module raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdgattn.so")
+
+# status codes and option keys (mirrors include/dg_attn.h)
+DG_OK, DG_ERR_ARG, DG_ERR_ALIGN, DG_ERR_CUDA, DG_ERR_TIMEOUT, DG_ERR_UNSUPPORTED, DG_ERR_STATE = range(7)
+DG_PATH_TC, DG_PATH_FP32 = 0, 1
+DG_OPT_PATH, DG_OPT_POS0, DG_OPT_SPLITS, DG_OPT_WAIT_LIMIT_MS, DG_OPT_PROFILE = 1, 2, 3, 4, 5
+DG_INFO_SPLITS_USED, DG_INFO_SCRATCH_BYTES, DG_INFO_CACHE_READY, DG_INFO_LAUNCHES = 16, 17, 18, 19
+DG_STAGE_NORM_ROPE, DG_STAGE_ATTENTION, DG_STAGE_COMBINE, DG_STAGE_CACHE = 0, 1, 2, 3
+
+EXPORTED = [
+    "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare", "dg_attn_norm_rope",
+    "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
+    "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
+]
+
+_lib = None
+
+
+class DgAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)}): {last_error()}")
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with gqa_canvas_attention_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    lib.dg_attn_plan_create.argtypes = [I, I, I, I, I, ctypes.c_float, ctypes.c_float]
+    lib.dg_attn_plan_create.restype = P
+    lib.dg_attn_forward.argtypes = [P] * 11
+    lib.dg_attn_forward.restype = I
+    lib.dg_attn_cache_prepare.argtypes = [P, P, P, P]
+    lib.dg_attn_cache_prepare.restype = I
+    lib.dg_attn_norm_rope.argtypes = [P] * 11
+    lib.dg_attn_norm_rope.restype = I
+    lib.dg_attn_attend.argtypes = [P] * 8
+    lib.dg_attn_attend.restype = I
+    lib.dg_attn_set_option.argtypes = [P, I, LL]
+    lib.dg_attn_set_option.restype = I
+    lib.dg_attn_get_option.argtypes = [P, I, ctypes.POINTER(LL)]
+    lib.dg_attn_get_option.restype = I
+    lib.dg_attn_sync_status.argtypes = [P, P]
+    lib.dg_attn_sync_status.restype = I
+    lib.dg_attn_profile_read.argtypes = [P, I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(LL)]
+    lib.dg_attn_profile_read.restype = I
+    lib.dg_attn_plan_destroy.argtypes = [P]
+    lib.dg_attn_plan_destroy.restype = None
+    lib.dg_attn_status_string.argtypes = [I]
+    lib.dg_attn_status_string.restype = ctypes.c_char_p
+    lib.dg_attn_last_error.argtypes = []
+    lib.dg_attn_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().dg_attn_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return load().dg_attn_last_error().decode()
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != DG_OK:
+        raise DgAttnError(rc, what)
+
+
+def dg_attn_plan_create(nh, nkv, hd, ctx, T, eps, rope_theta):
+    h = load().dg_attn_plan_create(nh, nkv, hd, ctx, T, float(eps), float(rope_theta))
+    if not h:
+        raise RuntimeError(f"dg_attn_plan_create: {last_error()}")
+    return h
+
+
+def dg_attn_plan_destroy(plan):
+    load().dg_attn_plan_destroy(plan)
+
+
+def dg_attn_forward(plan, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                    out, stream=None):
+    rc = load().dg_attn_forward(plan, _ptr(q), _ptr(k_canvas), _ptr(v_canvas), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(cos_sin),
+                                _ptr(out), _stream(stream))
+    _check(rc, "dg_attn_forward")
+
+
+def dg_attn_cache_prepare(plan, k_cache, v_cache, stream=None):
+    _check(load().dg_attn_cache_prepare(plan, _ptr(k_cache), _ptr(v_cache), _stream(stream)),
+           "dg_attn_cache_prepare")
+
+
+def dg_attn_norm_rope(plan, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, q_hat, k_hat,
+                      v_hat, stream=None):
+    rc = load().dg_attn_norm_rope(plan, _ptr(q), _ptr(k_canvas), _ptr(v_canvas), _ptr(q_norm_w),
+                                  _ptr(k_norm_w), _ptr(cos_sin), _ptr(q_hat), _ptr(k_hat),
+                                  _ptr(v_hat), _stream(stream))
+    _check(rc, "dg_attn_norm_rope")
+
+
+def dg_attn_attend(plan, q_hat, k_hat, v_hat, k_cache, v_cache, out, stream=None):
+    rc = load().dg_attn_attend(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(out), _stream(stream))
+    _check(rc, "dg_attn_attend")
+
+
+def dg_attn_set_option(plan, key, value):
+    _check(load().dg_attn_set_option(plan, int(key), int(value)), "dg_attn_set_option")
+
+
+def dg_attn_get_option(plan, key) -> int:
+    v = ctypes.c_longlong(0)
+    _check(load().dg_attn_get_option(plan, int(key), ctypes.byref(v)), "dg_attn_get_option")
+    return v.value
+
+
+def dg_attn_sync_status(plan, stream=None) -> int:
+    """Returns the status (DG_OK or DG_ERR_TIMEOUT) instead of raising on a device timeout."""
+    rc = load().dg_attn_sync_status(plan, _stream(stream))
+    if rc not in (DG_OK, DG_ERR_TIMEOUT):
+        raise DgAttnError(rc, "dg_attn_sync_status")
+    return rc
+
+
+def dg_attn_profile_read(plan, stage):
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_longlong(0)
+    _check(load().dg_attn_profile_read(plan, int(stage), ctypes.byref(ms), ctypes.byref(n)),
+           "dg_attn_profile_read")
+    return ms.value, n.value
+
+
+class Plan:
+    """Owning handle around a dg_attn_plan (created on the current CUDA device)."""
+
+    def __init__(self, nh, nkv, hd, ctx, T, eps=1e-6, rope_theta=10000.0):
+        self.nh, self.nkv, self.hd, self.ctx, self.T = nh, nkv, hd, ctx, T
+        self.handle = dg_attn_plan_create(nh, nkv, hd, ctx, T, eps, rope_theta)
+
+    def close(self):
+        if self.handle:
+            dg_attn_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set(self, key, value):
+        dg_attn_set_option(self.handle, key, value)
+        return self
+
+    def get(self, key):
+        return dg_attn_get_option(self.handle, key)
+
+    def forward(self, q, k_canvas, v_canvas, k_cache=None, v_cache=None, q_norm_w=None,
+                k_norm_w=None, cos_sin=None, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=q.device)
+        dg_attn_forward(self.handle, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w,
+                        cos_sin, out, stream)
+        return out
+
+    def cache_prepare(self, k_cache, v_cache, stream=None):
+        dg_attn_cache_prepare(self.handle, k_cache, v_cache, stream)
+
+    def norm_rope(self, q, k_canvas, v_canvas, q_norm_w=None, k_norm_w=None, cos_sin=None,
+                  stream=None):
+        import torch
+        qh = torch.empty_like(q)
+        kh = torch.empty_like(k_canvas)
+        vh = torch.empty_like(v_canvas)
+        dg_attn_norm_rope(self.handle, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, qh, kh,
+                          vh, stream)
+        return qh, kh, vh
+
+    def attend(self, q_hat, k_hat, v_hat, k_cache=None, v_cache=None, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=q_hat.device)
+        dg_attn_attend(self.handle, q_hat, k_hat, v_hat, k_cache, v_cache, out, stream)
+        return out
+
+    def sync_status(self, stream=None) -> int:
+        return dg_attn_sync_status(self.handle, stream)

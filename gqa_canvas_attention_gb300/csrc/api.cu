@@ -1,0 +1,708 @@
+// api.cu -- the C ABI of libdgattn.so (declared in include/dg_attn.h): plan creation and scratch
+// layout, argument checks, TMA descriptor set-up, the choice of key-range partitions, and the
+// enqueueing of the kernels of one forward on the caller's stream.
+//
+// The plan's scratch, all device-resident and allocated once at creation:
+//   inv_freq  [hd/2] float2        theta^(-2i/hd) as a double-float (hi, lo), made on the host in fp64
+//   fp32 path: q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd]
+//   tensor-core path: Q hi/lo bf16 [nkv, rows_pad, hd] (row R = t*G + h mod G, padded to 128),
+//             K hi/lo bf16 [nkv, ctx + T, hd] and V (TF32-rounded fp32) [nkv, ctx + T, hd] with the
+//             cache in rows 0..ctx-1 and the canvas in rows ctx..ctx+T-1
+//   partials  O [splits, nkv, rows_pad, hd] and (m, l) [splits, nkv, rows_pad]
+//   status    one uint32 that kernels OR their wait failures into
+#include "../../include/dg_attn.h"
+#include "dg_internal.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return DG_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D tiled map over [d2][d1][d0] with a 128-byte swizzle; box {b0, b1, 1}; OOB reads are zero.
+bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, uint64_t d0,
+               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1)
+{
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+struct dg_attn_plan {
+    int nh, nkv, hd, ctx, T, G, S, rows, rows_pad;
+    float eps, theta;
+    long long pos0;
+    int path;
+    int splits_opt;
+    long long wait_limit_ms;
+    int profile;
+    int device, num_sms;
+    bool tc_ok;
+    // scratch
+    float2 *inv_freq;
+    uint32_t *status;
+    float *q32, *k32, *v32;
+    __nv_bfloat16 *qh, *ql, *kh, *kl;
+    float *vt;
+    float *part_o;
+    float2 *part_ml;
+    int part_capacity;           // partitions the partial buffers hold
+    size_t scratch_bytes;
+    // prepared cache
+    bool cache_ready;
+    const float *prep_k, *prep_v;   // fp32 path: the caller's buffers
+    dg::TcMaps maps;
+    // profiling: per stage, pairs of events (start, stop) recorded around launches
+    std::vector<cudaEvent_t> ev[4];
+    size_t ev_used[4];
+};
+
+namespace {
+
+void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
+{
+    if (err != cudaSuccess || bytes == 0) return nullptr;
+    void *ptr = nullptr;
+    err = cudaMalloc(&ptr, bytes);
+    if (err == cudaSuccess) {
+        p->scratch_bytes += bytes;
+        err = cudaMemset(ptr, 0, bytes);
+    }
+    return ptr;
+}
+
+void free_scratch(dg_attn_plan *p)
+{
+    void *ptrs[] = {p->inv_freq, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
+                    p->kh, p->kl, p->vt, p->part_o, p->part_ml};
+    for (void *x : ptrs)
+        if (x) cudaFree(x);
+    for (auto &v : p->ev) {
+        for (cudaEvent_t e : v) cudaEventDestroy(e);
+        v.clear();
+    }
+}
+
+int n_tiles_for(const dg_attn_plan *p)
+{
+    if (p->path == DG_PATH_TC) {
+        const int nk = dg::tc_geometry(p->hd).nk;
+        return (p->S + nk - 1) / nk;
+    }
+    return (p->S + 31) / 32;
+}
+
+int qtiles_for(const dg_attn_plan *p)
+{
+    const int tm = p->path == DG_PATH_TC ? dg::kTileM : dg::kFp32TileM;
+    return ((p->rows + tm - 1) / tm) * p->nkv;
+}
+
+// Key-range partitions: minimise (waves of CTAs) x (tiles per CTA + a fixed start-up cost),
+// with the start-up cost in tile units; ties go to fewer partitions.
+int auto_splits(const dg_attn_plan *p)
+{
+    const int nt = n_tiles_for(p);
+    const int qt = qtiles_for(p);
+    const int per_sm = p->path == DG_PATH_TC ? 1 : 2;
+    const int slots = p->num_sms * per_sm;
+    const double startup = p->path == DG_PATH_TC ? 3.0 : 1.0;
+    int best = 1;
+    double best_cost = 1e300;
+    for (int s = 1; s <= nt && s <= 64; ++s) {
+        const int tps = (nt + s - 1) / s;
+        const int s_eff = (nt + tps - 1) / tps;
+        if (s_eff != s) continue;
+        const int waves = (qt * s + slots - 1) / slots;
+        const double cost = waves * (tps + startup) + (s > 1 ? 0.5 : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// Partitions actually used: the option (clamped so that none is empty) or the automatic choice.
+void split_layout(const dg_attn_plan *p, int &splits, int &tiles_per_split, int &n_tiles)
+{
+    n_tiles = n_tiles_for(p);
+    int s = p->splits_opt > 0 ? p->splits_opt : auto_splits(p);
+    if (s > n_tiles) s = n_tiles;
+    if (s > p->part_capacity) s = p->part_capacity > 0 ? p->part_capacity : 1;
+    if (s < 1) s = 1;
+    tiles_per_split = (n_tiles + s - 1) / s;
+    splits = (n_tiles + tiles_per_split - 1) / tiles_per_split;
+}
+
+int ensure_partials(dg_attn_plan *p, int splits)
+{
+    if (splits <= 1 || splits <= p->part_capacity) return DG_OK;
+    if (p->part_o) cudaFree(p->part_o);
+    if (p->part_ml) cudaFree(p->part_ml);
+    p->part_o = nullptr;
+    p->part_ml = nullptr;
+    p->part_capacity = 0;
+    cudaError_t err = cudaSuccess;
+    const size_t rows = (size_t)splits * p->nkv * p->rows_pad;
+    p->part_o = (float *)dalloc(p, rows * p->hd * sizeof(float), err);
+    p->part_ml = (float2 *)dalloc(p, rows * sizeof(float2), err);
+    if (err != cudaSuccess) return cuda_fail(err, "allocating split-KV partials");
+    p->part_capacity = splits;
+    return DG_OK;
+}
+
+int record_event(dg_attn_plan *p, int stage, cudaStream_t s)
+{
+    if (!p->profile) return DG_OK;
+    auto &v = p->ev[stage];
+    size_t &used = p->ev_used[stage];
+    if (used >= v.size()) {
+        const size_t grow = v.size() ? v.size() : 1024;
+        for (size_t i = 0; i < grow; ++i) {
+            cudaEvent_t e;
+            cudaError_t err = cudaEventCreate(&e);
+            if (err != cudaSuccess) return cuda_fail(err, "cudaEventCreate");
+            v.push_back(e);
+        }
+    }
+    cudaError_t err = cudaEventRecord(v[used++], s);
+    return err == cudaSuccess ? DG_OK : cuda_fail(err, "cudaEventRecord");
+}
+
+int build_maps(dg_attn_plan *p)
+{
+    const int nk = dg::tc_geometry(p->hd).nk;
+    bool ok = true;
+    ok &= encode_3d(&p->maps.ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->ql, p->hd, p->rows_pad,
+                    p->nkv, 64, dg::kTileM);
+    ok &= encode_3d(&p->maps.kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kh, p->hd, p->S, p->nkv,
+                    64, nk);
+    ok &= encode_3d(&p->maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kl, p->hd, p->S, p->nkv,
+                    64, nk);
+    ok &= encode_3d(&p->maps.vt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->vt, p->hd, p->S, p->nkv,
+                    32, nk);
+    if (!ok) {
+        set_error("cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+dg::NormRopeParams norm_params(const dg_attn_plan *p)
+{
+    dg::NormRopeParams n{};
+    n.inv_freq = p->inv_freq;
+    n.T = p->T; n.nh = p->nh; n.nkv = p->nkv; n.ctx = p->ctx; n.S = p->S;
+    n.rows_pad = p->rows_pad;
+    n.pos0 = p->pos0;
+    n.eps = p->eps;
+    n.do_norm = 1; n.do_rope = 1;
+    n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
+    n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vt = p->vt;
+    return n;
+}
+
+// Attention + (when partitioned) combine, reading the operands the first stage left in scratch.
+int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cache, float *out,
+                      cudaStream_t s)
+{
+    int splits, tps, nt;
+    split_layout(p, splits, tps, nt);
+    int rc = record_event(p, DG_STAGE_ATTENTION, s);
+    if (rc) return rc;
+    cudaError_t err;
+    if (p->path == DG_PATH_TC) {
+        dg::AttnTcParams a{};
+        a.qh = p->qh; a.ql = p->ql; a.out = out; a.part_o = p->part_o; a.part_ml = p->part_ml;
+        a.status = p->status;
+        a.wait_limit_ns = (unsigned long long)p->wait_limit_ms * 1000000ull;
+        a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.S = p->S; a.G = p->G;
+        a.rows = p->rows; a.rows_pad = p->rows_pad;
+        a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
+        err = dg::launch_attn_tc(a, p->maps, p->hd, s);
+        if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
+    } else {
+        dg::AttnFp32Params a{};
+        a.q = p->q32; a.k = p->k32; a.v = p->v32;
+        a.k_cache = k_cache; a.v_cache = v_cache;
+        a.out = out; a.part_o = p->part_o; a.part_ml = p->part_ml;
+        a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.ctx = p->ctx; a.S = p->S; a.G = p->G;
+        a.rows = p->rows; a.rows_pad = p->rows_pad;
+        a.splits = splits; a.keys_per_split = tps * 32;
+        err = dg::launch_attn_fp32(a, p->hd, s);
+        if (err != cudaSuccess) return cuda_fail(err, "fp32 attention launch");
+    }
+    rc = record_event(p, DG_STAGE_ATTENTION, s);
+    if (rc) return rc;
+    if (splits > 1) {
+        dg::CombineParams c{};
+        c.part_o = p->part_o; c.part_ml = p->part_ml; c.out = out;
+        c.T = p->T; c.nh = p->nh; c.nkv = p->nkv; c.G = p->G; c.rows = p->rows;
+        c.rows_pad = p->rows_pad; c.splits = splits; c.hd = p->hd;
+        c.log2_domain = p->path == DG_PATH_TC ? 1 : 0;
+        if ((rc = record_event(p, DG_STAGE_COMBINE, s))) return rc;
+        err = dg::launch_combine(c, s);
+        if (err != cudaSuccess) return cuda_fail(err, "combine launch");
+        if ((rc = record_event(p, DG_STAGE_COMBINE, s))) return rc;
+    }
+    return DG_OK;
+}
+
+// Resolve which cache the attention reads; converts a per-call cache on the tensor-core path.
+int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache, cudaStream_t s)
+{
+    if (p->ctx == 0) {
+        if (k_cache || v_cache) {
+            set_error("ctx == 0: k_cache and v_cache must be NULL");
+            return DG_ERR_ARG;
+        }
+        return DG_OK;
+    }
+    if (!k_cache && !v_cache) {
+        if (!p->cache_ready) {
+            set_error("no cache given and none prepared (dg_attn_cache_prepare)");
+            return DG_ERR_STATE;
+        }
+        if (p->path == DG_PATH_FP32) {
+            k_cache = p->prep_k;
+            v_cache = p->prep_v;
+        }
+        return DG_OK;
+    }
+    if (!k_cache || !v_cache) {
+        set_error("k_cache and v_cache must both be given or both be NULL");
+        return DG_ERR_ARG;
+    }
+    if (!aligned16(k_cache) || !aligned16(v_cache)) {
+        set_error("cache pointers must be 16-byte aligned");
+        return DG_ERR_ALIGN;
+    }
+    if (p->path == DG_PATH_TC) {
+        // the per-call conversion overwrites the plan's cache copy
+        p->cache_ready = false;
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->hd};
+        int rc = record_event(p, DG_STAGE_CACHE, s);
+        if (rc) return rc;
+        cudaError_t err = dg::launch_cache_prep(c, s);
+        if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
+        if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
+    }
+    return DG_OK;
+}
+
+int check_plan(const dg_attn_plan *p)
+{
+    if (!p) {
+        set_error("NULL plan");
+        return DG_ERR_ARG;
+    }
+    return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float eps,
+                                  float rope_theta)
+{
+    if (nh < 1 || nkv < 1 || T < 1 || ctx < 0 || nh % nkv != 0) {
+        set_error("bad sizes: nh=%d nkv=%d T=%d ctx=%d (need nh %% nkv == 0, nh, nkv, T >= 1, "
+                  "ctx >= 0)", nh, nkv, T, ctx);
+        return nullptr;
+    }
+    if (hd != 32 && hd != 64 && hd != 128 && hd != 256) {
+        set_error("hd=%d not supported (32, 64, 128 or 256)", hd);
+        return nullptr;
+    }
+    if (!(eps >= 0.f) || !(rope_theta > 0.f)) {
+        set_error("eps must be >= 0 and rope_theta > 0");
+        return nullptr;
+    }
+    if ((long long)ctx + T >= (1ll << 24)) {
+        set_error("positions must stay below 2^24");
+        return nullptr;
+    }
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    cudaDeviceProp prop;
+    if (err == cudaSuccess) err = cudaGetDeviceProperties(&prop, dev);
+    if (err != cudaSuccess) {
+        cuda_fail(err, "querying the current device");
+        return nullptr;
+    }
+    if (!(prop.major == 10 && prop.minor == 3)) {
+        set_error("device %s is sm_%d%d; this library is built for sm_103a only", prop.name,
+                  prop.major, prop.minor);
+        return nullptr;
+    }
+    dg_attn_plan *p = new (std::nothrow) dg_attn_plan();
+    if (!p) {
+        set_error("out of host memory");
+        return nullptr;
+    }
+    p->nh = nh; p->nkv = nkv; p->hd = hd; p->ctx = ctx; p->T = T;
+    p->G = nh / nkv; p->S = ctx + T; p->rows = T * p->G;
+    p->rows_pad = ((p->rows + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
+    p->eps = eps; p->theta = rope_theta; p->pos0 = ctx;
+    p->tc_ok = (hd == 64 || hd == 128 || hd == 256);
+    p->path = p->tc_ok ? DG_PATH_TC : DG_PATH_FP32;
+    p->splits_opt = 0;
+    p->wait_limit_ms = 2000;
+    p->device = dev;
+    p->num_sms = prop.multiProcessorCount;
+
+    const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
+    const size_t nqt = (size_t)nkv * p->rows_pad * hd, nkt = (size_t)nkv * p->S * hd;
+    p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
+    p->status = (uint32_t *)dalloc(p, sizeof(uint32_t) * 4, err);
+    p->q32 = (float *)dalloc(p, nq * sizeof(float), err);
+    p->k32 = (float *)dalloc(p, nk * sizeof(float), err);
+    p->v32 = (float *)dalloc(p, nk * sizeof(float), err);
+    if (p->tc_ok) {
+        p->qh = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
+        p->ql = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
+        p->kh = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
+        p->kl = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
+        p->vt = (float *)dalloc(p, nkt * 4, err);
+    }
+    if (err != cudaSuccess) {
+        cuda_fail(err, "allocating plan scratch");
+        free_scratch(p);
+        delete p;
+        return nullptr;
+    }
+    std::vector<float2> f(hd / 2);
+    for (int i = 0; i < hd / 2; ++i) {
+        const double v = std::pow((double)rope_theta, -2.0 * i / (double)hd);
+        const float hi = (float)v;
+        f[i] = make_float2(hi, (float)(v - (double)hi));
+    }
+    err = cudaMemcpy(p->inv_freq, f.data(), sizeof(float2) * f.size(), cudaMemcpyHostToDevice);
+    if (err == cudaSuccess && p->tc_ok) err = dg::attn_tc_prepare(hd);
+    int rc = (err == cudaSuccess) ? DG_OK : cuda_fail(err, "plan set-up");
+    if (rc == DG_OK && p->tc_ok) rc = build_maps(p);
+    if (rc == DG_OK) {
+        // room for the partitions both paths would pick
+        const int saved = p->path;
+        int need = 1;
+        for (int path : {DG_PATH_TC, DG_PATH_FP32}) {
+            if (path == DG_PATH_TC && !p->tc_ok) continue;
+            p->path = path;
+            const int s = auto_splits(p);
+            if (s > need) need = s;
+        }
+        p->path = saved;
+        rc = ensure_partials(p, need);
+    }
+    if (rc != DG_OK) {
+        free_scratch(p);
+        delete p;
+        return nullptr;
+    }
+    return p;
+}
+
+void dg_attn_plan_destroy(dg_attn_plan *p)
+{
+    if (!p) return;
+    free_scratch(p);
+    delete p;
+}
+
+int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
+{
+    if (int rc = check_plan(p)) return rc;
+    switch (key) {
+    case DG_OPT_PATH:
+        if (value == DG_PATH_TC && !p->tc_ok) {
+            set_error("the tensor-core path needs hd in {64, 128, 256}");
+            return DG_ERR_UNSUPPORTED;
+        }
+        if (value != DG_PATH_TC && value != DG_PATH_FP32) {
+            set_error("unknown path %lld", value);
+            return DG_ERR_ARG;
+        }
+        if (p->path != (int)value) p->cache_ready = false;
+        p->path = (int)value;
+        return DG_OK;
+    case DG_OPT_POS0:
+        if (value < 0 || value + p->T >= (1ll << 24)) {
+            set_error("pos0 out of range");
+            return DG_ERR_ARG;
+        }
+        p->pos0 = value;
+        return DG_OK;
+    case DG_OPT_SPLITS: {
+        if (value < 0 || value > 1024) {
+            set_error("splits must be in [0, 1024]");
+            return DG_ERR_ARG;
+        }
+        p->splits_opt = (int)value;
+        int s, tps, nt;
+        const int cap = p->part_capacity;
+        p->part_capacity = 1 << 30;   // size the request before clamping to the buffers
+        split_layout(p, s, tps, nt);
+        p->part_capacity = cap;
+        return ensure_partials(p, s);
+    }
+    case DG_OPT_WAIT_LIMIT_MS:
+        if (value < 1 || value > 600000) {
+            set_error("wait limit must be in [1, 600000] ms");
+            return DG_ERR_ARG;
+        }
+        p->wait_limit_ms = value;
+        return DG_OK;
+    case DG_OPT_PROFILE:
+        p->profile = value ? 1 : 0;
+        for (size_t &u : p->ev_used) u = 0;
+        return DG_OK;
+    default:
+        set_error("unknown option %d", key);
+        return DG_ERR_ARG;
+    }
+}
+
+int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!value) {
+        set_error("NULL value pointer");
+        return DG_ERR_ARG;
+    }
+    int s, tps, nt;
+    switch (key) {
+    case DG_OPT_PATH: *value = p->path; return DG_OK;
+    case DG_OPT_POS0: *value = p->pos0; return DG_OK;
+    case DG_OPT_SPLITS: *value = p->splits_opt; return DG_OK;
+    case DG_OPT_WAIT_LIMIT_MS: *value = p->wait_limit_ms; return DG_OK;
+    case DG_OPT_PROFILE: *value = p->profile; return DG_OK;
+    case DG_INFO_SPLITS_USED:
+        split_layout(p, s, tps, nt);
+        *value = s;
+        return DG_OK;
+    case DG_INFO_SCRATCH_BYTES: *value = (long long)p->scratch_bytes; return DG_OK;
+    case DG_INFO_CACHE_READY: *value = p->cache_ready ? 1 : 0; return DG_OK;
+    case DG_INFO_LAUNCHES:
+        split_layout(p, s, tps, nt);
+        *value = 2 + (s > 1 ? 1 : 0);
+        return DG_OK;
+    default:
+        set_error("unknown option %d", key);
+        return DG_ERR_ARG;
+    }
+}
+
+int dg_attn_cache_prepare(dg_attn_plan *p, const float *k_cache, const float *v_cache,
+                          cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (p->ctx == 0) {
+        set_error("ctx == 0: there is no cache to prepare");
+        return DG_ERR_ARG;
+    }
+    if (!k_cache || !v_cache) {
+        set_error("k_cache and v_cache are required");
+        return DG_ERR_ARG;
+    }
+    if (!aligned16(k_cache) || !aligned16(v_cache)) {
+        set_error("cache pointers must be 16-byte aligned");
+        return DG_ERR_ALIGN;
+    }
+    if (p->path == DG_PATH_TC) {
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->hd};
+        int rc = record_event(p, DG_STAGE_CACHE, s);
+        if (rc) return rc;
+        cudaError_t err = dg::launch_cache_prep(c, s);
+        if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
+        if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
+    } else {
+        p->prep_k = k_cache;
+        p->prep_v = v_cache;
+    }
+    p->cache_ready = true;
+    return DG_OK;
+}
+
+static int check_canvas_args(const dg_attn_plan *p, const float *a, const float *b, const float *c,
+                             const float *wq, const float *wk, const float *cs, const float *o1,
+                             const float *o2, const float *o3)
+{
+    if (!a || !b || !c || !o1 || (o2 == nullptr) != (o3 == nullptr)) {
+        set_error("a required pointer is NULL");
+        return DG_ERR_ARG;
+    }
+    const void *all[] = {a, b, c, wq, wk, cs, o1, o2, o3};
+    for (const void *x : all)
+        if (x && !aligned16(x)) {
+            set_error("pointers must be 16-byte aligned");
+            return DG_ERR_ALIGN;
+        }
+    (void)p;
+    return DG_OK;
+}
+
+int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, const float *v_canvas,
+                    const float *k_cache, const float *v_cache, const float *q_norm_w,
+                    const float *k_norm_w, const float *cos_sin, float *out, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (int rc = check_canvas_args(p, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, out,
+                                   nullptr, nullptr))
+        return rc;
+    if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+    dg::NormRopeParams n = norm_params(p);
+    n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
+    const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
+    int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
+    if (rc) return rc;
+    cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+    if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
+    if ((rc = record_event(p, DG_STAGE_NORM_ROPE, s))) return rc;
+    return enqueue_attention(p, k_cache, v_cache, out, s);
+}
+
+int dg_attn_norm_rope(dg_attn_plan *p, const float *q, const float *k_canvas,
+                      const float *v_canvas, const float *q_norm_w, const float *k_norm_w,
+                      const float *cos_sin, float *q_hat, float *k_hat, float *v_hat,
+                      cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (int rc = check_canvas_args(p, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, q_hat,
+                                   k_hat, v_hat))
+        return rc;
+    if (!k_hat) {
+        set_error("k_hat and v_hat are required");
+        return DG_ERR_ARG;
+    }
+    dg::NormRopeParams n = norm_params(p);
+    n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
+    n.q_out = q_hat; n.k_out = k_hat; n.v_out = v_hat;
+    cudaError_t err = dg::launch_norm_rope(n, p->hd, dg::kOutFp32, s);
+    if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
+    return DG_OK;
+}
+
+int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, const float *v_hat,
+                   const float *k_cache, const float *v_cache, float *out, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (int rc = check_canvas_args(p, q_hat, k_hat, v_hat, nullptr, nullptr, nullptr, out,
+                                   nullptr, nullptr))
+        return rc;
+    if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+    // the first-stage kernel with norm and rope switched off only re-lays the operands out
+    dg::NormRopeParams n = norm_params(p);
+    n.q = q_hat; n.k = k_hat; n.v = v_hat;
+    n.do_norm = 0; n.do_rope = 0;
+    const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
+    cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+    if (err != cudaSuccess) return cuda_fail(err, "operand layout launch");
+    return enqueue_attention(p, k_cache, v_cache, out, s);
+}
+
+int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    cudaError_t err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
+    uint32_t st = 0;
+    err = cudaMemcpy(&st, p->status, sizeof(st), cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess) err = cudaMemset(p->status, 0, sizeof(uint32_t));
+    if (err != cudaSuccess) return cuda_fail(err, "reading the status word");
+    if (st) {
+        set_error("a device wait ran out (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 drain)",
+                  st);
+        return DG_ERR_TIMEOUT;
+    }
+    return DG_OK;
+}
+
+int dg_attn_profile_read(dg_attn_plan *p, int stage, double *total_ms, long long *launches)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!total_ms || !launches || stage < 0 || stage > 3) {
+        set_error("bad stage or NULL output pointer");
+        return DG_ERR_ARG;
+    }
+    double tot = 0.0;
+    long long n = 0;
+    auto &v = p->ev[stage];
+    for (size_t i = 0; i + 1 < p->ev_used[stage]; i += 2) {
+        cudaError_t err = cudaEventSynchronize(v[i + 1]);
+        float ms = 0.f;
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, v[i], v[i + 1]);
+        if (err != cudaSuccess) return cuda_fail(err, "reading profiling events");
+        tot += ms;
+        ++n;
+    }
+    p->ev_used[stage] = 0;
+    *total_ms = tot;
+    *launches = n;
+    return DG_OK;
+}
+
+const char *dg_attn_status_string(int status)
+{
+    switch (status) {
+    case DG_OK: return "ok";
+    case DG_ERR_ARG: return "invalid argument";
+    case DG_ERR_ALIGN: return "misaligned pointer";
+    case DG_ERR_CUDA: return "CUDA error";
+    case DG_ERR_TIMEOUT: return "device wait timed out";
+    case DG_ERR_UNSUPPORTED: return "unsupported";
+    case DG_ERR_STATE: return "missing plan state";
+    default: return "unknown status";
+    }
+}
+
+const char *dg_attn_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,457 @@
+// attn_tc.cu -- tensor-core attention for the canvas block (page "inferencelayer 0.2.3,
+// src/diffusion_gemma_gpu.rs", item DG_ATTN: GQA bidirectional attention, scaling 1.0, no mask,
+// keys = [cache | canvas] of kv head g = h / (nh/nkv)), written for sm_103a.
+//
+// Work unit: one CTA per (128-row query tile, kv group, key-range partition).  The G query heads
+// of a kv group are packed into the MMA M dimension (row R = t*G + h mod G), so each K/V tile is
+// staged once for all of them.
+//
+// Precision (scores reach |s| ~ 90 because of scaling 1.0, so one TF32 rounding of q or k moves
+// outputs by ~1e-2): Q.K^T is computed as  qh.kh + qh.kl + ql.kh  with bf16 hi/lo splits of both
+// operands (three kind::f16 MMAs, ~16 significant bits per operand); P.V runs in TF32
+// (kind::tf32) with P and V rounded to nearest.
+//
+// Roles (256 threads):
+//   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
+//            lives in shared memory);
+//   warp 1   MMA issuer (one thread) and TMEM owner;
+//   warp 2   V producer: TMA of the V tile into a VST-deep ring;
+//   warp 3   idle;
+//   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
+//            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to TF32, written back over S in
+//            place, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
+//            has grown by more than 2^8 (so P <= 256 in between), and write the output.
+// TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
+// Every mbarrier wait is bounded; a wait that runs out sets a status bit and the CTA unwinds.
+#include "dg_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace dg {
+namespace {
+
+template <int HD> struct Cfg;
+template <> struct Cfg<256> {
+    static constexpr int NK = 32, NSP = 4, KST = 3, VST = 2;
+    static constexpr bool QL_TMEM = false;
+    static constexpr int O_COL = 0, QH_COL = 256, QL_COL = 0, SP_COL = 384;
+};
+template <> struct Cfg<128> {
+    static constexpr int NK = 64, NSP = 4, KST = 3, VST = 3;
+    static constexpr bool QL_TMEM = true;
+    static constexpr int O_COL = 0, QH_COL = 128, QL_COL = 192, SP_COL = 256;
+};
+template <> struct Cfg<64> {
+    static constexpr int NK = 128, NSP = 2, KST = 3, VST = 3;
+    static constexpr bool QL_TMEM = true;
+    static constexpr int O_COL = 0, QH_COL = 64, QL_COL = 96, SP_COL = 128;
+};
+
+template <int HD> struct Layout {
+    using C = Cfg<HD>;
+    static constexpr int KPANELS = HD / 64;                 // 128-byte bf16 panels of a K row
+    static constexpr int VPANELS = HD / 32;                 // 128-byte fp32 panels of a V row
+    static constexpr int QL_BYTES = C::QL_TMEM ? 0 : kTileM * HD * 2;
+    static constexpr int KPANEL_BYTES = C::NK * 128;
+    static constexpr int KSTAGE_BYTES = 2 * KPANELS * KPANEL_BYTES;   // hi + lo
+    static constexpr int VPANEL_BYTES = C::NK * 128;
+    static constexpr int VSTAGE_BYTES = VPANELS * VPANEL_BYTES;
+    static constexpr int K_OFF = QL_BYTES;
+    static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + C::VST * VSTAGE_BYTES;
+    static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 5;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + TMEM slot + alignment
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(C::SP_COL + C::NSP * C::NK <= 512, "TMEM budget");
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 2^8 between rescales
+
+template <int HD>
+__global__ void __launch_bounds__(256, 1)
+attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
+{
+    using C = Cfg<HD>;
+    using Lay = Layout<HD>;
+    constexpr int NK = C::NK, NSP = C::NSP, KST = C::KST, VST = C::VST;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::BAR_OFF);
+    uint64_t *k_full = bars;
+    uint64_t *k_empty = k_full + KST;
+    uint64_t *v_full = k_empty + KST;
+    uint64_t *v_empty = v_full + VST;
+    uint64_t *s_full = v_empty + VST;
+    uint64_t *p_full = s_full + NSP;
+    uint64_t *sp_free = p_full + NSP;
+    uint64_t *o_done = sp_free + NSP;
+    uint64_t *o_final = o_done + 1;
+    uint64_t *q_full = o_final + 1;
+    uint64_t *q_ready = q_full + 1;
+    uint64_t *drain = q_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
+    const int tile0 = split * p.tiles_per_split;
+    const int n_local = min(p.n_tiles, tile0 + p.tiles_per_split) - tile0;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < KST; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+        for (int i = 0; i < VST; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+        for (int i = 0; i < NSP; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&sp_free[i], 1);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(o_final, 1);
+        mbar_init(q_full, 1);
+        mbar_init(q_ready, 128);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        prefetch_tmap(&maps.kh);
+        prefetch_tmap(&maps.kl);
+        prefetch_tmap(&maps.vt);
+        if (!C::QL_TMEM) prefetch_tmap(&maps.ql);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- K producer
+        if (lane == 0) {
+            bool ok = true;
+            int issued[KST] = {};
+            if (!C::QL_TMEM) {
+                uint8_t *qls = smem;
+                mbar_arrive_expect_tx(q_full, Lay::QL_BYTES);
+                for (int pn = 0; pn < Lay::KPANELS; ++pn)
+                    tma_load_3d(qls + pn * (kTileM * 128), &maps.ql, q_full, pn * 64,
+                                qt * kTileM, g);
+            }
+            for (int it = 0; it < n_local; ++it) {
+                const int s = it % KST;
+                if (it >= KST && !mbar_wait_bounded(&k_empty[s], ((it / KST) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *kst = smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES;
+                const int key0 = (tile0 + it) * NK;
+                mbar_arrive_expect_tx(&k_full[s], Lay::KSTAGE_BYTES);
+                for (int pn = 0; pn < Lay::KPANELS; ++pn) {
+                    tma_load_3d(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64, key0, g);
+                    tma_load_3d(kst + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES, &maps.kl, &k_full[s],
+                                pn * 64, key0, g);
+                }
+                ++issued[s];
+            }
+            if (!ok) atomicOr(p.status, kErrWaitProducer);
+            // let every load issued by this thread land before the CTA can exit
+            for (int s = 0; s < KST; ++s)
+                if (issued[s] > 0) mbar_wait_bounded(&k_full[s], (issued[s] - 1) & 1, limit);
+            if (!C::QL_TMEM) mbar_wait_bounded(q_full, 0, limit);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- V producer
+        if (lane == 0) {
+            bool ok = true;
+            int issued[VST] = {};
+            for (int it = 0; it < n_local; ++it) {
+                const int s = it % VST;
+                if (it >= VST && !mbar_wait_bounded(&v_empty[s], ((it / VST) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *vst = smem + Lay::V_OFF + s * Lay::VSTAGE_BYTES;
+                const int key0 = (tile0 + it) * NK;
+                mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
+                for (int pn = 0; pn < Lay::VPANELS; ++pn)
+                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vt, &v_full[s], pn * 32, key0, g);
+                ++issued[s];
+            }
+            if (!ok) atomicOr(p.status, kErrWaitProducer);
+            for (int s = 0; s < VST; ++s)
+                if (issued[s] > 0) mbar_wait_bounded(&v_full[s], (issued[s] - 1) & 1, limit);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
+            constexpr uint32_t idesc_pv = make_idesc(2, 0, 1, kTileM, HD);
+            const uint32_t t_o = tbase + C::O_COL;
+            const uint32_t t_qh = tbase + C::QH_COL;
+            const uint32_t t_ql = tbase + C::QL_COL;
+            const uint32_t t_sp = tbase + C::SP_COL;
+            const uint32_t ql_smem = smem_u32(smem);
+            bool ok = mbar_wait_bounded(q_ready, 0, limit);
+            if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
+            tc_fence_after();
+
+            auto issue_pv = [&](int i) -> bool {
+                const int b = i % NSP, vs = i % VST;
+                if (!mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit)) return false;
+                if (!mbar_wait_bounded(&v_full[vs], (i / VST) & 1, limit)) return false;
+                tc_fence_after();
+                const uint32_t vbase = smem_u32(smem + Lay::V_OFF + vs * Lay::VSTAGE_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < NK / 8; ++ks) {
+                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * 1024, Lay::VPANEL_BYTES, 1024);
+                    mma_tf32_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(&v_empty[vs]);
+                mma_commit(&sp_free[b]);
+                mma_commit(o_done);
+                return true;
+            };
+
+            for (int j = 0; ok && j < n_local; ++j) {
+                const int b = j % NSP, s = j % KST;
+                if (j >= NSP && !mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit)) { ok = false; break; }
+                if (!mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t kbase = smem_u32(smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES);
+                const uint32_t d = t_sp + b * NK;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const int pn = kk >> 2, sub = kk & 3;
+                    const uint32_t khi = kbase + pn * Lay::KPANEL_BYTES + sub * 32;
+                    const uint32_t klo = kbase + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES + sub * 32;
+                    const uint64_t bh = smem_desc_sw128(khi, 16, 1024);
+                    const uint64_t bl = smem_desc_sw128(klo, 16, 1024);
+                    mma_bf16_ts(d, t_qh + kk * 8, bh, idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_bf16_ts(d, t_qh + kk * 8, bl, idesc_qk, 1u);
+                    if constexpr (C::QL_TMEM) {
+                        mma_bf16_ts(d, t_ql + kk * 8, bh, idesc_qk, 1u);
+                    } else {
+                        const uint64_t ad = smem_desc_sw128(ql_smem + pn * (kTileM * 128) + sub * 32, 16, 1024);
+                        mma_bf16_ss(d, ad, bh, idesc_qk, 1u);
+                    }
+                }
+                mma_commit(&k_empty[s]);
+                mma_commit(&s_full[b]);
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok && n_local >= 1 && !issue_pv(n_local - 1)) ok = false;
+            if (ok) mma_commit(o_final);
+            if (!ok) atomicOr(p.status, kErrWaitMma);
+            // no tcgen05 operation of this thread may still run when TMEM is released
+            mma_commit(drain);
+            if (!mbar_wait_bounded(drain, 0, limit)) atomicOr(p.status, kErrWaitDrain);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- softmax / epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;                  // tile row == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int Rg = qt * kTileM + r;                     // packed row in the group
+        bool ok = true;
+
+        // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.
+        {
+            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh + ((size_t)g * p.rows_pad + Rg) * HD);
+#pragma unroll
+            for (int c = 0; c < HD / 64; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 u = src_h[c * 8 + v];
+                    w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+                }
+                tmem_st32(tbase + lane_off + C::QH_COL + 32 * c, w);
+            }
+            if constexpr (C::QL_TMEM) {
+                const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql + ((size_t)g * p.rows_pad + Rg) * HD);
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 u = src_l[c * 8 + v];
+                        w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+                    }
+                    tmem_st32(tbase + lane_off + C::QL_COL + 32 * c, w);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(q_ready);
+        }
+
+        float m_used = -INFINITY;   // log2 units
+        float l_run = 0.f;
+        for (int it = 0; it < n_local; ++it) {
+            const int b = it % NSP;
+            if (!mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
+            uint32_t sr[NK / 32][32];
+#pragma unroll
+            for (int c = 0; c < NK / 32; ++c) tmem_ld32(tsp + 32 * c, sr[c]);
+            tmem_wait_ld();
+            const int valid = p.S - (tile0 + it) * NK;      // keys of this tile below S
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < NK / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(sr[c][i]) * kLog2e;
+                    if (32 * c + i >= valid) x = -INFINITY;
+                    sr[c][i] = __float_as_uint(x);
+                    mx = fmaxf(mx, x);
+                }
+            const bool need = mx > m_used + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = fmaxf(m_used, mx);
+                const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
+                if (it > 0) {
+                    // O is only touched once the previous P.V product has landed
+                    if (!mbar_wait_bounded(o_done, (it - 1) & 1, limit)) ok = false;
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                    }
+                    tmem_wait_st();
+                }
+                l_run *= alpha;
+                m_used = m_new;
+            }
+#pragma unroll
+            for (int c = 0; c < NK / 32; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float pr = ex2_approx(__uint_as_float(sr[c][i]) - m_used);
+                    const uint32_t pt = f32_to_tf32_rna(pr);
+                    l_run += __uint_as_float(pt);
+                    sr[c][i] = pt;
+                }
+                tmem_st32(tsp + 32 * c, sr[c]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[b]);
+        }
+        if (ok && !mbar_wait_bounded(o_final, 0, limit)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kErrWaitSoftmax);
+        } else {
+            tc_fence_after();
+            const bool live = Rg < p.rows;
+            float *dst;
+            float scale;
+            if (p.splits == 1) {
+                const int t = Rg / p.G, h = g * p.G + Rg % p.G;
+                dst = live ? p.out + ((size_t)t * p.nh + h) * HD : nullptr;
+                scale = 1.0f / l_run;
+            } else {
+                const size_t row = ((size_t)split * p.nkv + g) * p.rows_pad + Rg;
+                dst = p.part_o + row * HD;
+                scale = 1.0f;
+                if (live) p.part_ml[row] = make_float2(m_used, l_run);
+            }
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                tmem_wait_ld();
+                if (live) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        d4[v] = make_float4(__uint_as_float(orr[4 * v]) * scale,
+                                            __uint_as_float(orr[4 * v + 1]) * scale,
+                                            __uint_as_float(orr[4 * v + 2]) * scale,
+                                            __uint_as_float(orr[4 * v + 3]) * scale);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+template <int HD>
+cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
+{
+    dim3 grid((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
+    attn_tc_kernel<HD><<<grid, 256, Layout<HD>::SMEM_BYTES, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t prepare_hd()
+{
+    return cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Layout<HD>::SMEM_BYTES);
+}
+
+}  // namespace
+
+TcGeom tc_geometry(int hd)
+{
+    switch (hd) {
+    case 64: return {Cfg<64>::NK, Cfg<64>::QL_TMEM};
+    case 128: return {Cfg<128>::NK, Cfg<128>::QL_TMEM};
+    case 256: return {Cfg<256>::NK, Cfg<256>::QL_TMEM};
+    default: return {0, 0};
+    }
+}
+
+size_t attn_tc_smem_bytes(int hd)
+{
+    switch (hd) {
+    case 64: return Layout<64>::SMEM_BYTES;
+    case 128: return Layout<128>::SMEM_BYTES;
+    case 256: return Layout<256>::SMEM_BYTES;
+    default: return 0;
+    }
+}
+
+cudaError_t attn_tc_prepare(int hd)
+{
+    switch (hd) {
+    case 64: return prepare_hd<64>();
+    case 128: return prepare_hd<128>();
+    case 256: return prepare_hd<256>();
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_attn_tc(const AttnTcParams &p, const TcMaps &maps, int hd, cudaStream_t s)
+{
+    switch (hd) {
+    case 64: return launch_hd<64>(p, maps, s);
+    case 128: return launch_hd<128>(p, maps, s);
+    case 256: return launch_hd<256>(p, maps, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dg

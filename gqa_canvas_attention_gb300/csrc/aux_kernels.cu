@@ -1,0 +1,92 @@
+// aux_kernels.cu -- the two streaming helpers around the attention kernels:
+//  * cache_prep: converts an encoder cache [nkv, ctx, hd] (page "inferencelayer 0.2.3,
+//    src/diffusion_gemma_gpu.rs", DgGpuCache / upload_cache: already normed and roped) into the
+//    tensor-core operand arrays: K as a bf16 hi/lo pair, V rounded to TF32 (round to nearest);
+//  * combine: merges the partial results of the key-range partitions (split-KV) of one query
+//    row with the log-sum-exp rule  out = sum_s w_s O_s / sum_s w_s l_s,  w_s = b^(m_s - max m).
+#include "dg_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace dg {
+namespace {
+
+__global__ void __launch_bounds__(256) cache_prep_kernel(CachePrepParams p)
+{
+    const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
+    const int hd4 = p.hd / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / hd4;              // g * ctx + j
+        const int c4 = (int)(i % hd4);
+        const size_t g = row / p.ctx, j = row % p.ctx;
+        const size_t dst = (g * p.S + j) * p.hd + 4 * (size_t)c4;
+        const float4 k = reinterpret_cast<const float4 *>(p.k_cache)[i];
+        const float4 v = reinterpret_cast<const float4 *>(p.v_cache)[i];
+        const float kx[4] = {k.x, k.y, k.z, k.w};
+        __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hi[e] = __float2bfloat16_rn(kx[e]);
+            lo[e] = __float2bfloat16_rn(kx[e] - __bfloat162float(hi[e]));
+        }
+        __nv_bfloat162 h01, h23, l01, l23;
+        h01.x = hi[0]; h01.y = hi[1]; h23.x = hi[2]; h23.y = hi[3];
+        l01.x = lo[0]; l01.y = lo[1]; l23.x = lo[2]; l23.y = lo[3];
+        uint2 uh, ul;
+        uh.x = *reinterpret_cast<uint32_t *>(&h01); uh.y = *reinterpret_cast<uint32_t *>(&h23);
+        ul.x = *reinterpret_cast<uint32_t *>(&l01); ul.y = *reinterpret_cast<uint32_t *>(&l23);
+        *reinterpret_cast<uint2 *>(p.kh + dst) = uh;
+        *reinterpret_cast<uint2 *>(p.kl + dst) = ul;
+        float4 vt;
+        vt.x = __uint_as_float(f32_to_tf32_rna(v.x));
+        vt.y = __uint_as_float(f32_to_tf32_rna(v.y));
+        vt.z = __uint_as_float(f32_to_tf32_rna(v.z));
+        vt.w = __uint_as_float(f32_to_tf32_rna(v.w));
+        *reinterpret_cast<float4 *>(p.vt + dst) = vt;
+    }
+}
+
+// One CTA per (packed row R, kv group g); one thread per output column.
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p)
+{
+    const int R = blockIdx.x, g = blockIdx.y;
+    if (R >= p.rows) return;
+    const size_t stride = (size_t)p.nkv * p.rows_pad;   // between partitions
+    const size_t row = (size_t)g * p.rows_pad + R;
+    float mmax = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[s * stride + row].x);
+    const int t = R / p.G, h = g * p.G + R % p.G;
+    float *dst = p.out + ((size_t)t * p.nh + h) * p.hd;
+    for (int c = threadIdx.x; c < p.hd; c += blockDim.x) {
+        float num = 0.f, den = 0.f;
+        for (int s = 0; s < p.splits; ++s) {
+            const float2 ml = p.part_ml[s * stride + row];
+            const float w = p.log2_domain ? exp2f(ml.x - mmax) : expf(ml.x - mmax);
+            num = fmaf(w, p.part_o[(s * stride + row) * p.hd + c], num);
+            den = fmaf(w, ml.y, den);
+        }
+        dst[c] = num / den;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
+{
+    const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
+    if (n4 == 0) return cudaSuccess;
+    int blocks = (int)((n4 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    cache_prep_kernel<<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
+{
+    dim3 grid(p.rows, p.nkv);
+    const int threads = p.hd < 256 ? p.hd : 256;
+    combine_kernel<<<grid, threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dg

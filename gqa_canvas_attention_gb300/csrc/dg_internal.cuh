@@ -1,0 +1,111 @@
+// dg_internal.cuh -- shared declarations between the translation units of libdgattn.so:
+// kernel parameter blocks, operand layouts in the plan's scratch, and the host launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace dg {
+
+// Device status word bits (OR-ed in by kernels whose bounded waits ran out).
+enum : uint32_t {
+    kErrWaitProducer = 1u,
+    kErrWaitMma = 2u,
+    kErrWaitSoftmax = 4u,
+    kErrWaitDrain = 8u,
+};
+
+// Rows of the tensor-core query tile: the G = nh/nkv query heads of one kv group are packed
+// into the MMA M dimension, row R = t * G + (h mod G) of group g = h / G.
+constexpr int kTileM = 128;
+// Rows of the fp32 path's query tile.
+constexpr int kFp32TileM = 32;
+
+// What the first-stage kernel writes.
+enum NormOut : int {
+    kOutFp32 = 0,   // q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd] fp32 (input layouts)
+    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, tf32-rounded v_hat (tensor-core layouts)
+};
+
+struct NormRopeParams {
+    const float *q, *k, *v;        // [T, nh*hd], [T, nkv*hd], [T, nkv*hd]
+    const float *wq, *wk;          // [hd] or null
+    const float *cos_sin;          // [T, 2*hd] or null
+    const float2 *inv_freq;        // [hd/2] (hi, lo) double-float of theta^(-2i/hd)
+    int T, nh, nkv, ctx, S, rows_pad;
+    long long pos0;
+    float eps;
+    int do_norm, do_rope;          // 0/1 (the attention-only entry point passes 0, 0)
+    // kOutFp32 destinations
+    float *q_out, *k_out, *v_out;
+    // kOutTc destinations
+    __nv_bfloat16 *qh, *ql;        // [nkv, rows_pad, hd]
+    __nv_bfloat16 *kh, *kl;        // [nkv, S, hd] (canvas rows ctx..ctx+T-1)
+    float *vt;                     // [nkv, S, hd]
+};
+
+// Conversion of a cache [nkv, ctx, hd] into the tensor-core operand arrays (rows 0..ctx-1).
+struct CachePrepParams {
+    const float *k_cache, *v_cache;
+    __nv_bfloat16 *kh, *kl;
+    float *vt;
+    int nkv, ctx, S, hd;
+};
+
+struct AttnFp32Params {
+    const float *q;                // q_hat [T, nh, hd]
+    const float *k_cache, *v_cache;// [nkv, ctx, hd] or null when ctx == 0
+    const float *k, *v;            // canvas k_hat / v_hat [T, nkv, hd]
+    float *out;                    // [T, nh*hd] (splits == 1)
+    float *part_o;                 // [splits, nkv, rows_pad, hd] (splits > 1)
+    float2 *part_ml;               // [splits, nkv, rows_pad] (running max, denominator)
+    int T, nh, nkv, ctx, S, G, rows, rows_pad;
+    int splits, keys_per_split;
+};
+
+struct AttnTcParams {
+    const __nv_bfloat16 *qh;       // [nkv, rows_pad, hd] (q_hat hi, bf16), loaded into TMEM
+    const __nv_bfloat16 *ql;       // [nkv, rows_pad, hd] (q_hat lo), TMEM or TMA
+    float *out;
+    float *part_o;
+    float2 *part_ml;
+    uint32_t *status;
+    unsigned long long wait_limit_ns;
+    int T, nh, nkv, S, G, rows, rows_pad;
+    int splits, tiles_per_split, n_tiles;
+};
+
+struct CombineParams {
+    const float *part_o;
+    const float2 *part_ml;
+    float *out;
+    int T, nh, nkv, G, rows, rows_pad, splits, hd;
+    int log2_domain;               // 1: weights are 2^(s - m) (tensor-core path), 0: e^(s - m)
+};
+
+// Tensor maps handed to the tensor-core kernel (by value, __grid_constant__).
+struct TcMaps {
+    CUtensorMap ql;                // bf16 [nkv][rows_pad][hd], box {64, 128, 1}
+    CUtensorMap kh, kl;            // bf16 [nkv][S][hd], box {64, NK, 1}
+    CUtensorMap vt;                // fp32 [nkv][S][hd], box {32, NK, 1}
+};
+
+// Tile geometry of the tensor-core kernel for a head dimension.
+struct TcGeom {
+    int nk;        // keys per tile
+    int ql_in_tmem;
+};
+TcGeom tc_geometry(int hd);
+
+// Host launchers (return cudaGetLastError()).
+cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);
+cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s);
+cudaError_t launch_attn_fp32(const AttnFp32Params &p, int hd, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnTcParams &p, const TcMaps &maps, int hd, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+cudaError_t attn_tc_prepare(int hd);   // one-time function attributes (smem opt-in)
+size_t attn_tc_smem_bytes(int hd);
+
+}  // namespace dg

@@ -1,0 +1,256 @@
+// norm_rope.cu -- first stage of the canvas attention block (page "inferencelayer 0.2.3,
+// src/diffusion_gemma_gpu.rs", item DG_HEADNORM_ROPE and the three head-norm dispatches of
+// canvas_forward): per (token, head) RMSNorm with optional weight, NeoX rotate-half RoPE on q
+// and k, the weightless un-roped norm on v.
+//
+// One CTA per canvas token; its warps take the token's nh + 2*nkv heads, one warp per head.
+// The token's cos/sin row is computed once per CTA into shared memory: the angle
+// (pos0 + t) * theta^(-2i/hd) is formed in double-float (the frequency arrives as an fp64 value
+// split into two floats, the product is made exact with an FMA), reduced modulo 2*pi with a
+// Cody-Waite split of 2*pi (Cody & Waite, "Software Manual for the Elementary Functions", 1980)
+// and the leftover low part folded in with the second-order angle-addition formula around
+// CUDA's sincosf.  fp32 angles would be off by up to ~1e-3 rad at positions near 8192.
+//
+// Each lane holds hd/32 elements (float, float2, float4 or two float4); the RMS is a warp
+// shuffle reduction and the rotate-half partner of element i (i +- hd/2) is either in the same
+// lane or in lane ^ 16.
+#include "dg_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace dg {
+namespace {
+
+template <int HD>
+struct Lane {
+    static constexpr int EPL = HD / 32;
+    // element index held in slot e of lane l
+    __device__ static __forceinline__ int idx(int l, int e)
+    {
+        if constexpr (HD <= 128) return l * EPL + e;
+        else return (e < 4) ? 4 * l + e : 128 + 4 * l + (e - 4);
+    }
+    // is slot e of lane l in the first half (i < hd/2)?
+    __device__ static __forceinline__ bool first_half(int l, int e)
+    {
+        if constexpr (HD <= 128) return l < 16;
+        else return e < 4;
+    }
+    __device__ static __forceinline__ void load(const float *row, int l, float (&x)[EPL])
+    {
+        if constexpr (HD == 32) {
+            x[0] = row[l];
+        } else if constexpr (HD == 64) {
+            float2 a = reinterpret_cast<const float2 *>(row)[l];
+            x[0] = a.x; x[1] = a.y;
+        } else if constexpr (HD == 128) {
+            float4 a = reinterpret_cast<const float4 *>(row)[l];
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        } else {
+            float4 a = reinterpret_cast<const float4 *>(row)[l];
+            float4 b = reinterpret_cast<const float4 *>(row)[32 + l];
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+    }
+    __device__ static __forceinline__ void store(float *row, int l, const float (&x)[EPL])
+    {
+        if constexpr (HD == 32) {
+            row[l] = x[0];
+        } else if constexpr (HD == 64) {
+            reinterpret_cast<float2 *>(row)[l] = make_float2(x[0], x[1]);
+        } else if constexpr (HD == 128) {
+            reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
+        } else {
+            reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
+            reinterpret_cast<float4 *>(row)[32 + l] = make_float4(x[4], x[5], x[6], x[7]);
+        }
+    }
+    // bf16 stores of EPL elements per lane (HD >= 64 in the tensor-core layouts)
+    __device__ static __forceinline__ void store_bf16(__nv_bfloat16 *row, int l,
+                                                      const __nv_bfloat16 (&x)[EPL])
+    {
+        static_assert(HD >= 64, "tensor-core layouts need hd >= 64");
+        if constexpr (HD == 64) {
+            __nv_bfloat162 v; v.x = x[0]; v.y = x[1];
+            reinterpret_cast<__nv_bfloat162 *>(row)[l] = v;
+        } else if constexpr (HD == 128) {
+            __nv_bfloat162 a, b; a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
+            uint2 u; u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
+            reinterpret_cast<uint2 *>(row)[l] = u;
+        } else {
+            __nv_bfloat162 a, b, c, d;
+            a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
+            c.x = x[4]; c.y = x[5]; d.x = x[6]; d.y = x[7];
+            uint2 u, w;
+            u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
+            w.x = *reinterpret_cast<uint32_t *>(&c); w.y = *reinterpret_cast<uint32_t *>(&d);
+            reinterpret_cast<uint2 *>(row)[l] = u;
+            reinterpret_cast<uint2 *>(row)[32 + l] = w;
+        }
+    }
+};
+
+// cos and sin of p * f with f = f_hi + f_lo (see the file comment for the method).
+__device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c, float &s)
+{
+    const float kTwoPiHi = 6.28318548202514648f;     // 2*pi rounded to fp32
+    const float kTwoPiLo = -1.7484555314695172e-07f; // 2*pi - kTwoPiHi
+    const float kInvTwoPi = 0.15915494309189535f;
+    const float a_hi = pf * f.x;
+    const float a_err = fmaf(pf, f.x, -a_hi);        // p*f_hi = a_hi + a_err exactly
+    const float a_lo = fmaf(pf, f.y, a_err);
+    const float kq = rintf(a_hi * kInvTwoPi);
+    const float P = kq * kTwoPiHi;
+    const float Pe = fmaf(kq, kTwoPiHi, -P);         // kq*2pi_hi = P + Pe exactly
+    const float d = a_hi - P;                         // exact (Sterbenz)
+    const float e = (a_lo - Pe) - kq * kTwoPiLo;      // small remainder of the angle
+    float sd, cd;
+    sincosf(d, &sd, &cd);
+    const float h = 0.5f * e * e;
+    c = cd - sd * e - cd * h;
+    s = sd + cd * e - sd * h;
+}
+
+template <int HD, int MODE>
+__global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
+{
+    using L = Lane<HD>;
+    constexpr int EPL = L::EPL;
+    constexpr int HALF = HD / 2;
+    __shared__ float s_cos[HD];
+    __shared__ float s_sin[HD];
+
+    const int t = blockIdx.x;
+    if (p.do_rope) {
+        if (p.cos_sin) {
+            const float *row = p.cos_sin + (size_t)t * 2 * HD;
+            for (int i = threadIdx.x; i < HD; i += blockDim.x) {
+                s_cos[i] = row[i];
+                s_sin[i] = row[HD + i];
+            }
+        } else {
+            const float pf = (float)(p.pos0 + t);
+            for (int k = threadIdx.x; k < HALF; k += blockDim.x) {
+                float c, s;
+                rope_angle_cos_sin(pf, p.inv_freq[k], c, s);
+                s_cos[k] = c; s_cos[k + HALF] = c;
+                s_sin[k] = s; s_sin[k + HALF] = s;
+            }
+        }
+    }
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int G = p.nh / p.nkv;
+    const int jobs = p.nh + 2 * p.nkv;
+    for (int job = warp; job < jobs; job += nwarps) {
+        int kind, head;
+        if (job < p.nh) { kind = 0; head = job; }
+        else if (job < p.nh + p.nkv) { kind = 1; head = job - p.nh; }
+        else { kind = 2; head = job - p.nh - p.nkv; }
+        const float *src = kind == 0 ? p.q + ((size_t)t * p.nh + head) * HD
+                         : kind == 1 ? p.k + ((size_t)t * p.nkv + head) * HD
+                                     : p.v + ((size_t)t * p.nkv + head) * HD;
+        const float *w = kind == 0 ? p.wq : kind == 1 ? p.wk : nullptr;
+        float x[EPL];
+        L::load(src, lane, x);
+        if (p.do_norm) {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                float y = x[e] * r;
+                if (w) y *= w[L::idx(lane, e)];
+                x[e] = y;
+            }
+        }
+        if (p.do_rope && kind != 2) {
+            float part[EPL];
+            if constexpr (HD <= 128) {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) part[e] = __shfl_xor_sync(0xffffffffu, x[e], 16);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) part[e] = x[e ^ 4];
+            }
+            float z[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const int i = L::idx(lane, e);
+                const float rot = L::first_half(lane, e) ? -part[e] : part[e];
+                z[e] = fmaf(x[e], s_cos[i], rot * s_sin[i]);
+            }
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[e] = z[e];
+        }
+        if constexpr (MODE == kOutFp32) {
+            float *dst = kind == 0 ? p.q_out + ((size_t)t * p.nh + head) * HD
+                       : kind == 1 ? p.k_out + ((size_t)t * p.nkv + head) * HD
+                                   : p.v_out + ((size_t)t * p.nkv + head) * HD;
+            L::store(dst, lane, x);
+        } else {
+            if (kind == 2) {
+                float v[EPL];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) v[e] = __uint_as_float(f32_to_tf32_rna(x[e]));
+                L::store(p.vt + ((size_t)head * p.S + p.ctx + t) * HD, lane, v);
+            } else {
+                __nv_bfloat16 hi[EPL], lo[EPL];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    hi[e] = __float2bfloat16_rn(x[e]);
+                    lo[e] = __float2bfloat16_rn(x[e] - __bfloat162float(hi[e]));
+                }
+                size_t off;
+                __nv_bfloat16 *dh, *dl;
+                if (kind == 0) {
+                    const int g = head / G, R = t * G + head % G;
+                    off = ((size_t)g * p.rows_pad + R) * HD;
+                    dh = p.qh; dl = p.ql;
+                } else {
+                    off = ((size_t)head * p.S + p.ctx + t) * HD;
+                    dh = p.kh; dl = p.kl;
+                }
+                if constexpr (HD >= 64) {
+                    L::store_bf16(dh + off, lane, hi);
+                    L::store_bf16(dl + off, lane, lo);
+                }
+            }
+        }
+    }
+}
+
+template <int HD>
+cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
+{
+    const int jobs = p.nh + 2 * p.nkv;
+    const int warps = jobs < 8 ? jobs : 8;
+    dim3 grid(p.T), block(32 * warps);
+    if (mode == kOutFp32) norm_rope_kernel<HD, kOutFp32><<<grid, block, 0, s>>>(p);
+    else {
+        if constexpr (HD >= 64) norm_rope_kernel<HD, kOutTc><<<grid, block, 0, s>>>(p);
+        else return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s)
+{
+    switch (hd) {
+    case 32: return launch_hd<32>(p, mode, s);
+    case 64: return launch_hd<64>(p, mode, s);
+    case 128: return launch_hd<128>(p, mode, s);
+    case 256: return launch_hd<256>(p, mode, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dg

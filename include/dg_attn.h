@@ -1,0 +1,135 @@
+/*
+ * dg_attn.h -- C ABI of libdgattn.so: DiffusionGemma's canvas-forward attention block on one
+ * GB300 (sm_103a).
+ *
+ * The operation (page "inferencelayer 0.2.3, src/diffusion_gemma_gpu.rs"):
+ *   - items DG_HEADNORM_ROPE and the three head-norm dispatches of canvas_forward:
+ *       q-hat = RoPE(RMSNorm(q) * w_q), k-hat = RoPE(RMSNorm(k_canvas) * w_k),
+ *       v-hat = RMSNorm(v_canvas) (no weight, no RoPE),
+ *       RMSNorm(x) = x * (mean(x^2) + eps)^-1/2 per (token, head); RoPE is NeoX rotate-half at
+ *       position pos0 + t with frequencies rope_theta^(-2i/hd) (both halves equal);
+ *   - item DG_ATTN and its dispatch: GQA bidirectional softmax attention with scaling 1.0 and no
+ *     mask over the split key/value set [cache (ctx rows) | canvas (T rows)], kv head of q head
+ *     h = h / (nh / nkv).
+ *
+ * Layouts (all fp32, dense, row-major, on the current CUDA device):
+ *   q         [T, nh*hd]           k_canvas, v_canvas [T, nkv*hd] (raw, before the norms)
+ *   k_cache   [nkv, ctx, hd]       v_cache [nkv, ctx, hd] (used as given: already normed/roped)
+ *   q_norm_w  [hd] or NULL         k_norm_w [hd] or NULL (NULL = unweighted)
+ *   cos_sin   [T, 2*hd] or NULL    row t = cos(hd) | sin(hd); NULL = computed on the device
+ *   out       [T, nh*hd]
+ *
+ * Ownership: the caller owns every buffer passed in; inputs are only read.  A plan owns its
+ * device scratch (normed operands, split-KV partials), allocated by dg_attn_plan_create on the
+ * current device and released by dg_attn_plan_destroy.
+ *
+ * Execution: every call that takes a stream only enqueues work on it (no host synchronisation,
+ * no allocation), so it can be recorded into a CUDA graph.  One plan must not be used by two
+ * streams at the same time: its scratch is shared between calls.
+ *
+ * Errors: calls return a DG_* status; the text of the last host-side error of the calling thread
+ * is in dg_attn_last_error().  Device-side waits are bounded: a wait that runs out sets a status
+ * word in the plan instead of hanging; dg_attn_sync_status() reads (and clears) it.
+ */
+#ifndef DG_ATTN_H
+#define DG_ATTN_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dg_attn_plan dg_attn_plan;
+
+/* Status codes. */
+#define DG_OK              0
+#define DG_ERR_ARG         1  /* bad size or NULL pointer */
+#define DG_ERR_ALIGN       2  /* a pointer is not 16-byte aligned */
+#define DG_ERR_CUDA        3  /* a CUDA call or launch failed; see dg_attn_last_error() */
+#define DG_ERR_TIMEOUT     4  /* a bounded device wait ran out (the kernel gave up cleanly) */
+#define DG_ERR_UNSUPPORTED 5  /* the request needs something this build or device lacks */
+#define DG_ERR_STATE       6  /* the call needs state the plan does not hold */
+
+/* Arithmetic paths (option DG_OPT_PATH). */
+#define DG_PATH_TC   0  /* tensor cores: Q.K^T as three bf16 MMAs (hi/lo split), P.V in TF32 */
+#define DG_PATH_FP32 1  /* exact fp32 on the CUDA cores */
+
+/* Option keys for dg_attn_set_option / dg_attn_get_option. */
+#define DG_OPT_PATH          1  /* DG_PATH_TC (default when hd is 64, 128 or 256) or DG_PATH_FP32 */
+#define DG_OPT_POS0          2  /* position of canvas row 0 (default ctx, the cache length) */
+#define DG_OPT_SPLITS        3  /* key-range partitions per query tile; 0 = chosen per plan */
+#define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000) */
+#define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage */
+/* Read-only (dg_attn_get_option): */
+#define DG_INFO_SPLITS_USED  16 /* partitions the next forward will use */
+#define DG_INFO_SCRATCH_BYTES 17 /* device bytes the plan holds */
+#define DG_INFO_CACHE_READY  18 /* 1 when dg_attn_cache_prepare has filled the plan's cache copy */
+#define DG_INFO_LAUNCHES     19 /* kernels one dg_attn_forward enqueues with the current options */
+
+/* Create a plan for one geometry on the current device.  Requires nh % nkv == 0, nh, nkv, T >= 1,
+ * ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in {64, 128, 256}),
+ * eps >= 0, rope_theta > 0.  Returns NULL on error (see
+ * dg_attn_last_error()).  Allocates the plan's device scratch with cudaMalloc. */
+dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float eps,
+                                  float rope_theta);
+
+/* The whole block: norms + RoPE, attention, output.  k_cache and v_cache are [nkv, ctx, hd];
+ * with ctx == 0 they must be NULL.  With ctx > 0 and both NULL the plan uses the cache copy made
+ * by the last dg_attn_cache_prepare (DG_ERR_STATE if there is none).  v_canvas may alias
+ * k_canvas (models whose V is the raw K projection).  out must not overlap any input.
+ * Every pointer must be 16-byte aligned (DG_ERR_ALIGN).  Enqueued on `stream`. */
+int dg_attn_forward(dg_attn_plan *plan, const float *q, const float *k_canvas,
+                    const float *v_canvas, const float *k_cache, const float *v_cache,
+                    const float *q_norm_w, const float *k_norm_w, const float *cos_sin, float *out,
+                    cudaStream_t stream);
+
+/* Copy a cache [nkv, ctx, hd] (K and V) into the plan in the tensor-core operand format, once
+ * per cache.  A denoising loop that keeps its cache fixed for many steps calls this once, then
+ * dg_attn_forward with k_cache = v_cache = NULL.  The copy is taken on `stream`; the caller may
+ * reuse its own buffers once that stream has passed this point.  On the fp32 path the plan
+ * keeps the two pointers instead (the caller must keep the buffers alive and unchanged). */
+int dg_attn_cache_prepare(dg_attn_plan *plan, const float *k_cache, const float *v_cache,
+                          cudaStream_t stream);
+
+/* The first stage alone (RMSNorm + weight + RoPE on q and k, RMSNorm on v), in fp32, written in
+ * the input layouts: q_hat [T, nh*hd], k_hat and v_hat [T, nkv*hd]. */
+int dg_attn_norm_rope(dg_attn_plan *plan, const float *q, const float *k_canvas,
+                      const float *v_canvas, const float *q_norm_w, const float *k_norm_w,
+                      const float *cos_sin, float *q_hat, float *k_hat, float *v_hat,
+                      cudaStream_t stream);
+
+/* The attention stage alone, on operands that are already normed and roped (q_hat [T, nh*hd],
+ * k_hat / v_hat [T, nkv*hd], cache as in dg_attn_forward), with the plan's current path. */
+int dg_attn_attend(dg_attn_plan *plan, const float *q_hat, const float *k_hat,
+                   const float *v_hat, const float *k_cache, const float *v_cache, float *out,
+                   cudaStream_t stream);
+
+int dg_attn_set_option(dg_attn_plan *plan, int key, long long value);
+int dg_attn_get_option(const dg_attn_plan *plan, int key, long long *value);
+
+/* Synchronise `stream`, then read and clear the plan's device status word: DG_OK, or
+ * DG_ERR_TIMEOUT when a kernel gave up on a bounded wait since the last call. */
+int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
+
+/* Stages for dg_attn_profile_read. */
+#define DG_STAGE_NORM_ROPE 0  /* the norm + RoPE kernel */
+#define DG_STAGE_ATTENTION 1  /* the attention kernel (tensor-core or fp32) */
+#define DG_STAGE_COMBINE   2  /* the split-KV combine kernel */
+#define DG_STAGE_CACHE     3  /* the cache conversion kernel */
+
+/* With DG_OPT_PROFILE on: synchronise on the recorded events, then return the summed device time
+ * (ms) and the count of the launches of one stage recorded since the last read of that stage
+ * (or since profiling was switched on), and reset that stage's record. */
+int dg_attn_profile_read(dg_attn_plan *plan, int stage, double *total_ms, long long *launches);
+
+void dg_attn_plan_destroy(dg_attn_plan *plan);
+
+const char *dg_attn_status_string(int status);
+const char *dg_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_ATTN_H */

@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on the same seeded
+inputs, element by element.
+
+Tolerances (on outputs of RMS <= 1):
+  tensor-core path: max |gpu - oracle| <= 5e-3 and mean <= 5e-4;
+  fp32 path:        max <= 1e-5.
+Full-size workloads are checked on sampled canvas rows that span several query tiles and the
+ragged tail; small shapes are checked whole.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_canvas_attention_gb300 import binding as B
+from gqa_canvas_attention_gb300.workloads import (EPS, ROPE_THETA, WORKLOADS, make_inputs,
+                                                  workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+TOL = {B.DG_PATH_TC: (5e-3, 5e-4), B.DG_PATH_FP32: (1e-5, 1e-6)}
+PATHS = [B.DG_PATH_TC, B.DG_PATH_FP32]
+PNAME = {B.DG_PATH_TC: "tc", B.DG_PATH_FP32: "fp32"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def to_dev(d):
+    return {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+
+
+def oracle_out(d, nh, nkv, hd, rows=None, pos0=None, cos_sin=None):
+    f = lambda x: None if x is None else x.numpy()
+    return oracle.forward(f(d["q"]), f(d["k_canvas"]), f(d["v_canvas"]), f(d["k_cache"]),
+                          f(d["v_cache"]), nh, nkv, hd, f(d["q_norm_w"]), f(d["k_norm_w"]),
+                          cos_sin=cos_sin, eps=EPS, theta=ROPE_THETA, pos0=pos0, rows=rows)
+
+
+def row_ranges(T):
+    if T <= 64:
+        return [(0, T)]
+    mid = T // 2
+    return [(0, 4), (mid - 3, mid + 3), (T - 5, T)]
+
+
+def check(out, ref, path, ranges, label=""):
+    tmax, tmean = TOL[path]
+    o = out.detach().cpu().double().numpy()
+    errs = np.concatenate([np.abs(o[a:b] - ref[a:b]).ravel() for a, b in ranges])
+    assert np.isfinite(o).all()
+    mx, mn = errs.max(), errs.mean()
+    print(f"{label} {PNAME[path]}: max {mx:.3e} mean {mn:.3e}")
+    assert mx <= tmax, f"{label}: max err {mx:.3e} > {tmax}"
+    assert mn <= tmean, f"{label}: mean err {mn:.3e} > {tmean}"
+
+
+def run_forward(plan, dd, **kw):
+    out = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["k_cache"], dd["v_cache"],
+                       dd["q_norm_w"], dd["k_norm_w"], **kw)
+    assert plan.sync_status() == B.DG_OK
+    return out
+
+
+# ------------------------------------------------------------------ first stage alone
+
+@pytest.mark.parametrize("hd", [32, 64, 128, 256])
+@pytest.mark.parametrize("weighted", [True, False])
+def test_norm_rope_stage(hd, weighted):
+    T, ctx, nh, nkv = 37, 8100, 4, 2
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=5, weighted=weighted, draw_cache=False)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    qh, kh, vh = plan.norm_rope(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["q_norm_w"],
+                                dd["k_norm_w"])
+    torch.cuda.synchronize()
+    w = lambda x: None if x is None else x.numpy()
+    rq = oracle.norm_rope(d["q"].numpy(), nh, hd, w(d["q_norm_w"]), EPS, True, ctx, ROPE_THETA)
+    rk = oracle.norm_rope(d["k_canvas"].numpy(), nkv, hd, w(d["k_norm_w"]), EPS, True, ctx,
+                          ROPE_THETA)
+    rv = oracle.norm_rope(d["v_canvas"].numpy(), nkv, hd, None, EPS, False)
+    for got, ref, name in ((qh, rq, "q"), (kh, rk, "k"), (vh, rv, "v")):
+        e = np.abs(got.cpu().double().numpy().reshape(ref.shape) - ref)
+        print(f"hd={hd} {name}: max {e.max():.2e}")
+        assert e.max() <= 2e-6, f"{name}: {e.max():.3e}"
+
+
+def test_norm_rope_with_table():
+    T, ctx, nh, nkv, hd = 9, 3, 2, 1, 64
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=6, weighted=True, draw_cache=False)
+    g = torch.Generator().manual_seed(7)
+    cs = torch.randn(T, 2 * hd, generator=g)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    qh, kh, _ = plan.norm_rope(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["q_norm_w"],
+                               dd["k_norm_w"], cs.cuda())
+    rq = oracle.norm_rope(d["q"].numpy(), nh, hd, d["q_norm_w"].numpy(), EPS, True, ctx,
+                          ROPE_THETA, cos_sin=cs.numpy())
+    assert np.abs(qh.cpu().double().numpy().reshape(rq.shape) - rq).max() <= 2e-6
+
+
+# ------------------------------------------------------------------ whole block, named workloads
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_parity(name, path):
+    w = WORKLOADS[name]
+    d = workload_inputs(w)
+    dd = to_dev(d)
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path)
+    out = run_forward(plan, dd)
+    ranges = row_ranges(w.T)
+    ref = np.zeros((w.T, w.nh * w.hd))
+    for a, b in ranges:
+        ref[a:b] = oracle_out(d, w.nh, w.nkv, w.hd, rows=(a, b))[a:b]
+    check(out, ref, path, ranges, name)
+
+
+def test_denoise_loop_steps_share_a_prepared_cache():
+    """A few steps of the 48-step loop: cache prepared once, fresh canvas per step."""
+    w = WORKLOADS["denoise48_ctx8k"]
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    d0 = workload_inputs(w, step=0)
+    kc, vc = d0["k_cache"].cuda(), d0["v_cache"].cuda()
+    plan.cache_prepare(kc, vc)
+    assert plan.get(B.DG_INFO_CACHE_READY) == 1
+    for step in (0, 1, 47):
+        d = workload_inputs(w, step=step)
+        d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]
+        dd = to_dev(d)
+        out = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"])
+        assert plan.sync_status() == B.DG_OK
+        ref = oracle_out(d, w.nh, w.nkv, w.hd, rows=(w.T - 4, w.T))
+        check(out, ref, B.DG_PATH_TC, [(w.T - 4, w.T)], f"step{step}")
+
+
+# ------------------------------------------------------------------ shapes and edge cases
+
+SHAPES = [
+    # T, ctx, nh, nkv, hd
+    (1, 0, 1, 1, 64),        # one key
+    (1, 5, 2, 1, 128),       # single canvas row with a cache
+    (3, 0, 4, 4, 64),        # MHA, ctx = 0
+    (70, 33, 6, 2, 64),      # ragged: rows 210 (not a tile multiple), S = 103
+    (129, 200, 2, 2, 128),   # 129 rows: two query tiles, the second with one live row
+    (65, 300, 8, 1, 256),    # G = 8: 520 packed rows
+    (50, 1000, 4, 2, 256),   # S = 1050, not a multiple of the key tile
+    (17, 63, 4, 2, 32),      # fp32-only head size
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d" % s)
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_shapes(shape, path):
+    T, ctx, nh, nkv, hd = shape
+    if path == B.DG_PATH_TC and hd not in (64, 128, 256):
+        pytest.skip("tensor-core path needs hd in {64, 128, 256}")
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=100 + T, weighted=True)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path)
+    out = run_forward(plan, dd)
+    check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], str(shape))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 1000])
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_forced_partitions(splits, path):
+    T, ctx, nh, nkv, hd = 40, 700, 4, 2, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=11, weighted=False)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path).set(B.DG_OPT_SPLITS, splits)
+    assert plan.get(B.DG_INFO_SPLITS_USED) >= 1
+    out = run_forward(plan, dd)
+    check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], f"splits={splits}")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_k_and_v_canvas_may_alias(path):
+    """Models whose V is the raw K projection pass the same buffer twice."""
+    T, ctx, nh, nkv, hd = 24, 40, 4, 2, 64
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=12)
+    d["v_canvas"] = d["k_canvas"]
+    dd = to_dev(d)
+    dd["v_canvas"] = dd["k_canvas"]
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path)
+    out = run_forward(plan, dd)
+    check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], "alias")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_pos0_option_and_table(path):
+    T, ctx, nh, nkv, hd = 20, 16, 2, 1, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=13)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path).set(B.DG_OPT_POS0, 5000)
+    out = run_forward(plan, dd)
+    check(out, oracle_out(d, nh, nkv, hd, pos0=5000), path, [(0, T)], "pos0")
+    g = torch.Generator().manual_seed(3)
+    ang = torch.rand(T, hd // 2, generator=g, dtype=torch.float64) * 6.0
+    cs = torch.cat([ang.cos(), ang.cos(), ang.sin(), ang.sin()], 1).float()
+    out = run_forward(plan, dd, cos_sin=cs.cuda())
+    check(out, oracle_out(d, nh, nkv, hd, cos_sin=cs.numpy()), path, [(0, T)], "table")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_attend_on_oracle_normed_inputs(path):
+    """The attention stage alone, on operands normed by the oracle (rounded to fp32)."""
+    T, ctx, nh, nkv, hd = 48, 80, 4, 2, 256
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=14)
+    qh = oracle.norm_rope(d["q"].numpy(), nh, hd, d["q_norm_w"].numpy(), EPS, True, ctx)
+    kh = oracle.norm_rope(d["k_canvas"].numpy(), nkv, hd, d["k_norm_w"].numpy(), EPS, True, ctx)
+    vh = oracle.norm_rope(d["v_canvas"].numpy(), nkv, hd, None, EPS, False)
+    q32, k32, v32 = (torch.from_numpy(x.astype(np.float32)).reshape(T, -1) for x in (qh, kh, vh))
+    ref = oracle.attention(q32.numpy(), k32.numpy(), v32.numpy(), d["k_cache"].numpy(),
+                           d["v_cache"].numpy(), nh, nkv, hd).reshape(T, nh * hd)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path)
+    out = plan.attend(q32.cuda(), k32.cuda(), v32.cuda(), d["k_cache"].cuda(), d["v_cache"].cuda())
+    assert plan.sync_status() == B.DG_OK
+    check(out, ref, path, [(0, T)], "attend")
+
+
+def test_per_call_cache_and_prepared_cache_agree():
+    T, ctx, nh, nkv, hd = 32, 500, 4, 2, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=15)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    a = run_forward(plan, dd).clone()
+    plan.cache_prepare(dd["k_cache"], dd["v_cache"])
+    b = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                     dd["k_norm_w"])
+    assert plan.sync_status() == B.DG_OK
+    assert torch.equal(a, b)
+
+
+def test_errors_are_reported_not_raised_on_device():
+    T, ctx, nh, nkv, hd = 8, 16, 2, 1, 64
+    d = to_dev(make_inputs(T, ctx, nh, nkv, hd, seed=16))
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    out = torch.empty(T, nh * hd, device="cuda")
+    h = plan.handle
+    # ctx > 0 without a cache and nothing prepared
+    with pytest.raises(B.DgAttnError) as e:
+        B.dg_attn_forward(h, d["q"], d["k_canvas"], d["v_canvas"], None, None, None, None, None, out)
+    assert e.value.status == B.DG_ERR_STATE
+    # misaligned pointer
+    with pytest.raises(B.DgAttnError) as e:
+        B.dg_attn_forward(h, d["q"].data_ptr() + 4, d["k_canvas"], d["v_canvas"], d["k_cache"],
+                          d["v_cache"], None, None, None, out)
+    assert e.value.status == B.DG_ERR_ALIGN
+    # a cache on a ctx == 0 plan
+    p0 = B.Plan(nh, nkv, hd, 0, T, EPS, ROPE_THETA)
+    with pytest.raises(B.DgAttnError) as e:
+        B.dg_attn_forward(p0.handle, d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"],
+                          d["v_cache"], None, None, None, out)
+    assert e.value.status == B.DG_ERR_ARG
+    # the fp32-only head size cannot take the tensor-core path
+    p32 = B.Plan(nh, nkv, 32, ctx, T, EPS, ROPE_THETA)
+    with pytest.raises(B.DgAttnError) as e:
+        p32.set(B.DG_OPT_PATH, B.DG_PATH_TC)
+    assert e.value.status == B.DG_ERR_UNSUPPORTED
+    assert plan.sync_status() == B.DG_OK
