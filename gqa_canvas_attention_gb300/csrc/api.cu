@@ -6,8 +6,9 @@
 //   inv_freq  [hd/2] float2        theta^(-2i/hd) as a double-float (hi, lo), made on the host in fp64
 //   fp32 path: q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd]
 //   tensor-core path: Q hi/lo bf16 [nkv, rows_pad, hd] (row R = t*G + h mod G, padded to 128),
-//             K hi/lo bf16 [nkv, ctx + T, hd] and V (TF32-rounded fp32) [nkv, ctx + T, hd] with the
-//             cache in rows 0..ctx-1 and the canvas in rows ctx..ctx+T-1
+//             K hi/lo bf16 [nkv, S, hd] (S = ctx + T) with the cache in rows 0..ctx-1 and the
+//             canvas in rows ctx..ctx+T-1; V transposed and TF32-rounded [nkv, hd, S_pad], keys
+//             contiguous (the tensor cores take TF32 operands K-major only)
 //   partials  O [splits, nkv, rows_pad, hd] and (m, l) [splits, nkv, rows_pad]
 //   status    one uint32 that kernels OR their wait failures into
 #include "../../include/dg_attn.h"
@@ -56,14 +57,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
     return fn;
 }
 
-// 3-D tiled map over [d2][d1][d0] with a 128-byte swizzle; box {b0, b1, 1}; OOB reads are zero.
+// 3-D tiled map over [d2][d1][d0] (rows of `row` elements, row >= d0) with a 128-byte
+// swizzle; box {b0, b1, 1}; reads outside the dims return zeros.
 bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, uint64_t d0,
-               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1)
+               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t row)
 {
     auto fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+    cuuint64_t strides[2] = {row * esize, row * d1 * esize};
     cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -75,7 +77,7 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, ui
 }  // namespace
 
 struct dg_attn_plan {
-    int nh, nkv, hd, ctx, T, G, S, rows, rows_pad;
+    int nh, nkv, hd, ctx, T, G, S, S_pad, rows, rows_pad;
     float eps, theta;
     long long pos0;
     int path;
@@ -221,13 +223,13 @@ int build_maps(dg_attn_plan *p)
     const int nk = dg::tc_geometry(p->hd).nk;
     bool ok = true;
     ok &= encode_3d(&p->maps.ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->ql, p->hd, p->rows_pad,
-                    p->nkv, 64, dg::kTileM);
+                    p->nkv, 64, dg::kTileM, p->hd);
     ok &= encode_3d(&p->maps.kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kh, p->hd, p->S, p->nkv,
-                    64, nk);
+                    64, nk, p->hd);
     ok &= encode_3d(&p->maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kl, p->hd, p->S, p->nkv,
-                    64, nk);
-    ok &= encode_3d(&p->maps.vt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->vt, p->hd, p->S, p->nkv,
-                    32, nk);
+                    64, nk, p->hd);
+    ok &= encode_3d(&p->maps.vt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->vt, p->S, p->hd, p->nkv,
+                    32, p->hd, p->S_pad);
     if (!ok) {
         set_error("cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
         return DG_ERR_CUDA;
@@ -239,7 +241,7 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
 {
     dg::NormRopeParams n{};
     n.inv_freq = p->inv_freq;
-    n.T = p->T; n.nh = p->nh; n.nkv = p->nkv; n.ctx = p->ctx; n.S = p->S;
+    n.T = p->T; n.nh = p->nh; n.nkv = p->nkv; n.ctx = p->ctx; n.S = p->S; n.S_pad = p->S_pad;
     n.rows_pad = p->rows_pad;
     n.pos0 = p->pos0;
     n.eps = p->eps;
@@ -327,7 +329,8 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
     if (p->path == DG_PATH_TC) {
         // the per-call conversion overwrites the plan's cache copy
         p->cache_ready = false;
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->hd};
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->S_pad,
+                              p->hd};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);
@@ -390,6 +393,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     }
     p->nh = nh; p->nkv = nkv; p->hd = hd; p->ctx = ctx; p->T = T;
     p->G = nh / nkv; p->S = ctx + T; p->rows = T * p->G;
+    p->S_pad = ((p->S + 31) / 32) * 32;
     p->rows_pad = ((p->rows + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
     p->eps = eps; p->theta = rope_theta; p->pos0 = ctx;
     p->tc_ok = (hd == 64 || hd == 128 || hd == 256);
@@ -401,6 +405,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
 
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
     const size_t nqt = (size_t)nkv * p->rows_pad * hd, nkt = (size_t)nkv * p->S * hd;
+    const size_t nvt = (size_t)nkv * hd * p->S_pad;
     p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
     p->status = (uint32_t *)dalloc(p, sizeof(uint32_t) * 4, err);
     p->q32 = (float *)dalloc(p, nq * sizeof(float), err);
@@ -411,7 +416,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
         p->ql = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
         p->kh = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
         p->kl = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
-        p->vt = (float *)dalloc(p, nkt * 4, err);
+        p->vt = (float *)dalloc(p, nvt * 4, err);
     }
     if (err != cudaSuccess) {
         cuda_fail(err, "allocating plan scratch");
@@ -557,7 +562,8 @@ int dg_attn_cache_prepare(dg_attn_plan *p, const float *k_cache, const float *v_
         return DG_ERR_ALIGN;
     }
     if (p->path == DG_PATH_TC) {
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->hd};
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->S_pad,
+                              p->hd};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);

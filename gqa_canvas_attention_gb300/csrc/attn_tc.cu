@@ -15,7 +15,8 @@
 //   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
 //            lives in shared memory);
 //   warp 1   MMA issuer (one thread) and TMEM owner;
-//   warp 2   V producer: TMA of the V tile into a VST-deep ring;
+//   warp 2   V producer: TMA of the V^T tile (keys contiguous: TF32 operands must be K-major)
+//            into a VST-deep ring;
 //   warp 3   idle;
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to TF32, written back over S in
@@ -49,11 +50,11 @@ template <> struct Cfg<64> {
 template <int HD> struct Layout {
     using C = Cfg<HD>;
     static constexpr int KPANELS = HD / 64;                 // 128-byte bf16 panels of a K row
-    static constexpr int VPANELS = HD / 32;                 // 128-byte fp32 panels of a V row
+    static constexpr int VPANELS = Cfg<HD>::NK / 32;        // 32-key (128-byte) panels of V^T
     static constexpr int QL_BYTES = C::QL_TMEM ? 0 : kTileM * HD * 2;
     static constexpr int KPANEL_BYTES = C::NK * 128;
     static constexpr int KSTAGE_BYTES = 2 * KPANELS * KPANEL_BYTES;   // hi + lo
-    static constexpr int VPANEL_BYTES = C::NK * 128;
+    static constexpr int VPANEL_BYTES = HD * 128;          // hd rows of 32 keys
     static constexpr int VSTAGE_BYTES = VPANELS * VPANEL_BYTES;
     static constexpr int K_OFF = QL_BYTES;
     static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
@@ -178,7 +179,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 const int key0 = (tile0 + it) * NK;
                 mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::VPANELS; ++pn)
-                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vt, &v_full[s], pn * 32, key0, g);
+                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vt, &v_full[s], key0 + pn * 32, 0, g);
                 ++issued[s];
             }
             if (!ok) atomicOr(p.status, kErrWaitProducer);
@@ -190,7 +191,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
-            constexpr uint32_t idesc_pv = make_idesc(2, 0, 1, kTileM, HD);
+            constexpr uint32_t idesc_pv = make_idesc(2, 0, 0, kTileM, HD);
             const uint32_t t_o = tbase + C::O_COL;
             const uint32_t t_qh = tbase + C::QH_COL;
             const uint32_t t_ql = tbase + C::QL_COL;
@@ -208,7 +209,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 const uint32_t vbase = smem_u32(smem + Lay::V_OFF + vs * Lay::VSTAGE_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < NK / 8; ++ks) {
-                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * 1024, Lay::VPANEL_BYTES, 1024);
+                    const uint64_t bdesc = smem_desc_sw128(vbase + (ks >> 2) * Lay::VPANEL_BYTES + (ks & 3) * 32, 16, 1024);
                     mma_tf32_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(&v_empty[vs]);

@@ -26,15 +26,18 @@ constexpr int kFp32TileM = 32;
 // What the first-stage kernel writes.
 enum NormOut : int {
     kOutFp32 = 0,   // q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd] fp32 (input layouts)
-    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, tf32-rounded v_hat (tensor-core layouts)
+    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, tf32-rounded v_hat^T (tensor-core layouts)
 };
+
+// Keys per block of the transposed V layout written through shared memory.
+constexpr int kVtKeys = 32;
 
 struct NormRopeParams {
     const float *q, *k, *v;        // [T, nh*hd], [T, nkv*hd], [T, nkv*hd]
     const float *wq, *wk;          // [hd] or null
     const float *cos_sin;          // [T, 2*hd] or null
     const float2 *inv_freq;        // [hd/2] (hi, lo) double-float of theta^(-2i/hd)
-    int T, nh, nkv, ctx, S, rows_pad;
+    int T, nh, nkv, ctx, S, S_pad, rows_pad;
     long long pos0;
     float eps;
     int do_norm, do_rope;          // 0/1 (the attention-only entry point passes 0, 0)
@@ -43,15 +46,15 @@ struct NormRopeParams {
     // kOutTc destinations
     __nv_bfloat16 *qh, *ql;        // [nkv, rows_pad, hd]
     __nv_bfloat16 *kh, *kl;        // [nkv, S, hd] (canvas rows ctx..ctx+T-1)
-    float *vt;                     // [nkv, S, hd]
+    float *vt;                     // [nkv, hd, S_pad]: v_hat transposed, keys contiguous
 };
 
 // Conversion of a cache [nkv, ctx, hd] into the tensor-core operand arrays (rows 0..ctx-1).
 struct CachePrepParams {
     const float *k_cache, *v_cache;
     __nv_bfloat16 *kh, *kl;
-    float *vt;
-    int nkv, ctx, S, hd;
+    float *vt;                     // [nkv, hd, S_pad] (cache keys in columns 0..ctx-1)
+    int nkv, ctx, S, S_pad, hd;
 };
 
 struct AttnFp32Params {
@@ -89,7 +92,7 @@ struct CombineParams {
 struct TcMaps {
     CUtensorMap ql;                // bf16 [nkv][rows_pad][hd], box {64, 128, 1}
     CUtensorMap kh, kl;            // bf16 [nkv][S][hd], box {64, NK, 1}
-    CUtensorMap vt;                // fp32 [nkv][S][hd], box {32, NK, 1}
+    CUtensorMap vt;                // fp32 [nkv][hd][S_pad] (keys innermost), box {32, hd, 1}
 };
 
 // Tile geometry of the tensor-core kernel for a head dimension.

@@ -14,6 +14,11 @@
 // Each lane holds hd/32 elements (float, float2, float4 or two float4); the RMS is a warp
 // shuffle reduction and the rotate-half partner of element i (i +- hd/2) is either in the same
 // lane or in lane ^ 16.
+//
+// For the tensor-core layouts, v-hat is stored transposed ([nkv, hd, keys], keys contiguous) so
+// that it is a K-major operand of the P.V product: extra CTAs after the T token CTAs each take
+// 32 consecutive tokens of one v head, normalise them (one warp per token), round to TF32 and
+// write the transpose through shared memory as 128-byte runs of keys.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -111,15 +116,64 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
+// v-hat of 32 tokens x one kv head, normalised, TF32-rounded and written transposed.
+template <int HD>
+__device__ __forceinline__ void v_transpose_block(const NormRopeParams &p, float *sbuf)
+{
+    using L = Lane<HD>;
+    constexpr int EPL = L::EPL;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int ngroups = (p.T + kVtKeys - 1) / kVtKeys;
+    const int vb = blockIdx.x - p.T;
+    const int g = vb / ngroups, t0 = (vb % ngroups) * kVtKeys;
+    for (int tt = warp; tt < kVtKeys; tt += nwarps) {
+        const int t = t0 + tt;
+        float x[EPL];
+        if (t < p.T) {
+            L::load(p.v + ((size_t)t * p.nkv + g) * HD, lane, x);
+            if (p.do_norm) {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) x[e] *= r;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            sbuf[tt * (HD + 1) + L::idx(lane, e)] = __uint_as_float(f32_to_tf32_rna(x[e]));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < HD * kVtKeys; i += blockDim.x) {
+        const int d = i / kVtKeys, tt = i % kVtKeys;
+        const int t = t0 + tt;
+        if (t < p.T) p.vt[((size_t)g * HD + d) * p.S_pad + p.ctx + t] = sbuf[tt * (HD + 1) + d];
+    }
+}
+
 template <int HD, int MODE>
 __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
 {
     using L = Lane<HD>;
     constexpr int EPL = L::EPL;
     constexpr int HALF = HD / 2;
-    __shared__ float s_cos[HD];
-    __shared__ float s_sin[HD];
+    constexpr int SBUF = (MODE == kOutTc) ? kVtKeys * (HD + 1) : 2 * HD;
+    __shared__ float sbuf[SBUF];
+    float *s_cos = sbuf;
+    float *s_sin = sbuf + HD;
 
+    if constexpr (MODE == kOutTc) {
+        if ((int)blockIdx.x >= p.T) {
+            v_transpose_block<HD>(p, sbuf);
+            return;
+        }
+    }
     const int t = blockIdx.x;
     if (p.do_rope) {
         if (p.cos_sin) {
@@ -144,7 +198,8 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int G = p.nh / p.nkv;
-    const int jobs = p.nh + 2 * p.nkv;
+    // in the tensor-core layouts the v heads are written by the transposing CTAs
+    const int jobs = p.nh + (MODE == kOutTc ? 1 : 2) * p.nkv;
     for (int job = warp; job < jobs; job += nwarps) {
         int kind, head;
         if (job < p.nh) { kind = 0; head = job; }
@@ -195,12 +250,7 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
                                    : p.v_out + ((size_t)t * p.nkv + head) * HD;
             L::store(dst, lane, x);
         } else {
-            if (kind == 2) {
-                float v[EPL];
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) v[e] = __uint_as_float(f32_to_tf32_rna(x[e]));
-                L::store(p.vt + ((size_t)head * p.S + p.ctx + t) * HD, lane, v);
-            } else {
+            {
                 __nv_bfloat16 hi[EPL], lo[EPL];
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
@@ -229,13 +279,17 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
 template <int HD>
 cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
 {
-    const int jobs = p.nh + 2 * p.nkv;
-    const int warps = jobs < 8 ? jobs : 8;
-    dim3 grid(p.T), block(32 * warps);
-    if (mode == kOutFp32) norm_rope_kernel<HD, kOutFp32><<<grid, block, 0, s>>>(p);
-    else {
-        if constexpr (HD >= 64) norm_rope_kernel<HD, kOutTc><<<grid, block, 0, s>>>(p);
-        else return cudaErrorInvalidValue;
+    if (mode == kOutFp32) {
+        const int jobs = p.nh + 2 * p.nkv;
+        const int warps = jobs < 8 ? jobs : 8;
+        norm_rope_kernel<HD, kOutFp32><<<p.T, 32 * warps, 0, s>>>(p);
+    } else {
+        if constexpr (HD >= 64) {
+            const int vblocks = p.nkv * ((p.T + kVtKeys - 1) / kVtKeys);
+            norm_rope_kernel<HD, kOutTc><<<p.T + vblocks, 256, 0, s>>>(p);
+        } else {
+            return cudaErrorInvalidValue;
+        }
     }
     return cudaGetLastError();
 }
