@@ -486,8 +486,8 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
         p->pos0 = value;
         return DG_OK;
     case DG_OPT_SPLITS: {
-        if (value < 0 || value > 1024) {
-            set_error("splits must be in [0, 1024]");
+        if (value < 0 || value > 64) {
+            set_error("splits must be in [0, 64]");
             return DG_ERR_ARG;
         }
         p->splits_opt = (int)value;

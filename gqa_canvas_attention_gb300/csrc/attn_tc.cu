@@ -11,13 +11,17 @@
 // operands (three kind::f16 MMAs, ~16 significant bits per operand); P.V runs in TF32
 // (kind::tf32) with P and V rounded to nearest.
 //
-// Roles (256 threads):
+// Roles (32 * (7 + NQI) threads):
 //   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
 //            lives in shared memory);
-//   warp 1   MMA issuer (one thread) and TMEM owner;
+//   warp 1   P.V issuer (one thread) and TMEM owner;
 //   warp 2   V producer: TMA of the V^T tile (keys contiguous: TF32 operands must be K-major)
 //            into a VST-deep ring;
-//   warp 3   idle;
+//   warp 3, 8.. Q.K^T issuers (one thread each).  A single thread can hand the tensor core only
+//            about one tcgen05.mma per ~60 cycles, far less than the 16-64 cycles of work in each
+//            128 x NK x 16 product, so key tiles are dealt round-robin to NQI issuers; issuer q
+//            owns the score buffers and K ring slots of the tiles j = q (mod NQI), so every
+//            mbarrier keeps a single in-order consumer;
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to TF32, written back over S in
 //            place, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
@@ -32,17 +36,17 @@ namespace {
 
 template <int HD> struct Cfg;
 template <> struct Cfg<256> {
-    static constexpr int NK = 32, NSP = 4, KST = 3, VST = 2;
+    static constexpr int NK = 32, NSP = 3, KST = 3, VST = 2, NQI = 3;
     static constexpr bool QL_TMEM = false;
     static constexpr int O_COL = 0, QH_COL = 256, QL_COL = 0, SP_COL = 384;
 };
 template <> struct Cfg<128> {
-    static constexpr int NK = 64, NSP = 4, KST = 3, VST = 3;
+    static constexpr int NK = 64, NSP = 4, KST = 4, VST = 3, NQI = 2;
     static constexpr bool QL_TMEM = true;
     static constexpr int O_COL = 0, QH_COL = 128, QL_COL = 192, SP_COL = 256;
 };
 template <> struct Cfg<64> {
-    static constexpr int NK = 128, NSP = 2, KST = 3, VST = 3;
+    static constexpr int NK = 128, NSP = 3, KST = 3, VST = 3, NQI = 3;
     static constexpr bool QL_TMEM = true;
     static constexpr int O_COL = 0, QH_COL = 64, QL_COL = 96, SP_COL = 128;
 };
@@ -59,22 +63,24 @@ template <int HD> struct Layout {
     static constexpr int K_OFF = QL_BYTES;
     static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
     static constexpr int BAR_OFF = V_OFF + C::VST * VSTAGE_BYTES;
-    static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 5;
+    static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 3 + (C::NQI + 1);
+    static constexpr int THREADS = 32 * (7 + C::NQI);
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + TMEM slot + alignment
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(C::SP_COL + C::NSP * C::NK <= 512, "TMEM budget");
+    static_assert(C::NSP % C::NQI == 0 && C::KST % C::NQI == 0, "issuer-owned buffers and slots");
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 2^8 between rescales
 
 template <int HD>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
 {
     using C = Cfg<HD>;
     using Lay = Layout<HD>;
-    constexpr int NK = C::NK, NSP = C::NSP, KST = C::KST, VST = C::VST;
+    constexpr int NK = C::NK, NSP = C::NSP, KST = C::KST, VST = C::VST, NQI = C::NQI;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -87,12 +93,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     uint64_t *s_full = v_empty + VST;
     uint64_t *p_full = s_full + NSP;
     uint64_t *sp_free = p_full + NSP;
-    uint64_t *o_done = sp_free + NSP;
-    uint64_t *o_final = o_done + 1;
+    uint64_t *o_final = sp_free + NSP;
     uint64_t *q_full = o_final + 1;
     uint64_t *q_ready = q_full + 1;
-    uint64_t *drain = q_ready + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *drain = q_ready + 1;          // [NQI + 1]: one per MMA-issuing thread
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + NQI + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -109,11 +114,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             mbar_init(&p_full[i], 128);
             mbar_init(&sp_free[i], 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(o_final, 1);
         mbar_init(q_full, 1);
         mbar_init(q_ready, 128);
-        mbar_init(drain, 1);
+        for (int i = 0; i <= NQI; ++i) mbar_init(&drain[i], 1);
         fence_mbar_init();
         prefetch_tmap(&maps.kh);
         prefetch_tmap(&maps.kl);
@@ -187,8 +191,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 if (issued[s] > 0) mbar_wait_bounded(&v_full[s], (issued[s] - 1) & 1, limit);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 3 || warp >= 8) {
+        // ---------------------------------------------------------------- MMA issuers
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
             constexpr uint32_t idesc_pv = make_idesc(2, 0, 0, kTileM, HD);
@@ -196,64 +200,68 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             const uint32_t t_qh = tbase + C::QH_COL;
             const uint32_t t_ql = tbase + C::QL_COL;
             const uint32_t t_sp = tbase + C::SP_COL;
-            const uint32_t ql_smem = smem_u32(smem);
-            bool ok = mbar_wait_bounded(q_ready, 0, limit);
-            if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
-            tc_fence_after();
-
-            auto issue_pv = [&](int i) -> bool {
-                const int b = i % NSP, vs = i % VST;
-                if (!mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit)) return false;
-                if (!mbar_wait_bounded(&v_full[vs], (i / VST) & 1, limit)) return false;
-                tc_fence_after();
-                const uint32_t vbase = smem_u32(smem + Lay::V_OFF + vs * Lay::VSTAGE_BYTES);
+            // Descriptors are built once; per stage / k-step only the start address moves
+            // (the 14-bit address field cannot carry: shared addresses are < 256 KiB).
+            const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + Lay::K_OFF), 16, 1024);
+            const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + Lay::V_OFF), 16, 1024);
+            const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+            const int me = warp == 1 ? 0 : 1 + (warp == 3 ? 0 : warp - 7);   // drain slot
+            bool ok = true;
+            if (warp == 1) {
+                // P.V, in tile order: O += P_i V_i
+                for (int i = 0; ok && i < n_local; ++i) {
+                    const int b = i % NSP, vs = i % VST;
+                    if (!mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit)) { ok = false; break; }
+                    if (!mbar_wait_bounded(&v_full[vs], (i / VST) & 1, limit)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t vd = vdesc0 + (uint64_t)((vs * Lay::VSTAGE_BYTES) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < NK / 8; ++ks) {
-                    const uint64_t bdesc = smem_desc_sw128(vbase + (ks >> 2) * Lay::VPANEL_BYTES + (ks & 3) * 32, 16, 1024);
-                    mma_tf32_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(&v_empty[vs]);
-                mma_commit(&sp_free[b]);
-                mma_commit(o_done);
-                return true;
-            };
-
-            for (int j = 0; ok && j < n_local; ++j) {
-                const int b = j % NSP, s = j % KST;
-                if (j >= NSP && !mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit)) { ok = false; break; }
-                if (!mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t kbase = smem_u32(smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES);
-                const uint32_t d = t_sp + b * NK;
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const int pn = kk >> 2, sub = kk & 3;
-                    const uint32_t khi = kbase + pn * Lay::KPANEL_BYTES + sub * 32;
-                    const uint32_t klo = kbase + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES + sub * 32;
-                    const uint64_t bh = smem_desc_sw128(khi, 16, 1024);
-                    const uint64_t bl = smem_desc_sw128(klo, 16, 1024);
-                    mma_bf16_ts(d, t_qh + kk * 8, bh, idesc_qk, kk > 0 ? 1u : 0u);
-                    mma_bf16_ts(d, t_qh + kk * 8, bl, idesc_qk, 1u);
-                    if constexpr (C::QL_TMEM) {
-                        mma_bf16_ts(d, t_ql + kk * 8, bh, idesc_qk, 1u);
-                    } else {
-                        const uint64_t ad = smem_desc_sw128(ql_smem + pn * (kTileM * 128) + sub * 32, 16, 1024);
-                        mma_bf16_ss(d, ad, bh, idesc_qk, 1u);
+                    for (int ks = 0; ks < NK / 8; ++ks) {
+                        const uint64_t bdesc = vd + (uint64_t)(((ks >> 2) * Lay::VPANEL_BYTES + (ks & 3) * 32) >> 4);
+                        mma_tf32_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
                     }
+                    mma_commit(&v_empty[vs]);
+                    mma_commit(&sp_free[b]);
                 }
-                mma_commit(&k_empty[s]);
-                mma_commit(&s_full[b]);
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                if (ok) mma_commit(o_final);
+            } else {
+                // Q.K^T of the tiles j = q (mod NQI): S_j = qh.kh + qh.kl + ql.kh
+                const int q = warp == 3 ? 0 : warp - 7;
+                ok = mbar_wait_bounded(q_ready, 0, limit);
+                if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
+                tc_fence_after();
+                for (int j = q; ok && j < n_local; j += NQI) {
+                    const int b = j % NSP, s = j % KST;
+                    if (j >= NSP && !mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit)) { ok = false; break; }
+                    if (!mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t kd = kdesc0 + (uint64_t)((s * Lay::KSTAGE_BYTES) >> 4);
+                    const uint32_t d = t_sp + b * NK;
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const int pn = kk >> 2, sub = kk & 3;
+                        const uint64_t bh = kd + (uint64_t)((pn * Lay::KPANEL_BYTES + sub * 32) >> 4);
+                        const uint64_t bl = kd + (uint64_t)(((Lay::KPANELS + pn) * Lay::KPANEL_BYTES + sub * 32) >> 4);
+                        mma_bf16_ts(d, t_qh + kk * 8, bh, idesc_qk, kk > 0 ? 1u : 0u);
+                        mma_bf16_ts(d, t_qh + kk * 8, bl, idesc_qk, 1u);
+                        if constexpr (C::QL_TMEM) {
+                            mma_bf16_ts(d, t_ql + kk * 8, bh, idesc_qk, 1u);
+                        } else {
+                            const uint64_t ad = qdesc0 + (uint64_t)((pn * (kTileM * 128) + sub * 32) >> 4);
+                            mma_bf16_ss(d, ad, bh, idesc_qk, 1u);
+                        }
+                    }
+                    mma_commit(&k_empty[s]);
+                    mma_commit(&s_full[b]);
+                }
             }
-            if (ok && n_local >= 1 && !issue_pv(n_local - 1)) ok = false;
-            if (ok) mma_commit(o_final);
             if (!ok) atomicOr(p.status, kErrWaitMma);
             // no tcgen05 operation of this thread may still run when TMEM is released
-            mma_commit(drain);
-            if (!mbar_wait_bounded(drain, 0, limit)) atomicOr(p.status, kErrWaitDrain);
+            mma_commit(&drain[me]);
+            if (!mbar_wait_bounded(&drain[me], 0, limit)) atomicOr(p.status, kErrWaitDrain);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ---------------------------------------------------------------- softmax / epilogue
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                  // tile row == TMEM lane
@@ -296,31 +304,50 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         float l_run = 0.f;
         for (int it = 0; it < n_local; ++it) {
             const int b = it % NSP;
-            if (!mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit)) { ok = false; break; }
+            ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
             tc_fence_after();
             const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
-            uint32_t sr[NK / 32][32];
-#pragma unroll
-            for (int c = 0; c < NK / 32; ++c) tmem_ld32(tsp + 32 * c, sr[c]);
-            tmem_wait_ld();
+            // NK <= 64: the whole score row stays in registers; NK = 128: the maximum is taken in
+            // a first pass and the scores are read again (register budget of 320 threads)
+            constexpr int RC = NK <= 64 ? NK / 32 : 1;
+            uint32_t sr[RC][32];
             const int valid = p.S - (tile0 + it) * NK;      // keys of this tile below S
             float mx = -INFINITY;
+            if constexpr (NK <= 64) {
 #pragma unroll
-            for (int c = 0; c < NK / 32; ++c)
+                for (int c = 0; c < RC; ++c) tmem_ld32(tsp + 32 * c, sr[c]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x = __uint_as_float(sr[c][i]) * kLog2e;
-                    if (32 * c + i >= valid) x = -INFINITY;
-                    sr[c][i] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
+                for (int c = 0; c < RC; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(sr[c][i]) * kLog2e;
+                        if (32 * c + i >= valid) x = -INFINITY;
+                        sr[c][i] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < NK / 32; ++c) {
+                    tmem_ld32(tsp + 32 * c, sr[0]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = __uint_as_float(sr[0][i]) * kLog2e;
+                        if (32 * c + i < valid) mx = fmaxf(mx, x);
+                    }
                 }
+            }
             const bool need = mx > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float m_new = fmaxf(m_used, mx);
                 const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
                 if (it > 0) {
-                    // O is only touched once the previous P.V product has landed
-                    if (!mbar_wait_bounded(o_done, (it - 1) & 1, limit)) ok = false;
+                    // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
+                    // has landed
+                    const int pb = (it - 1) % NSP;
+                    if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll 1
@@ -338,16 +365,33 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 l_run *= alpha;
                 m_used = m_new;
             }
+            if constexpr (NK <= 64) {
 #pragma unroll
-            for (int c = 0; c < NK / 32; ++c) {
+                for (int c = 0; c < RC; ++c) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float pr = ex2_approx(__uint_as_float(sr[c][i]) - m_used);
-                    const uint32_t pt = f32_to_tf32_rna(pr);
-                    l_run += __uint_as_float(pt);
-                    sr[c][i] = pt;
+                    for (int i = 0; i < 32; ++i) {
+                        const float pr = ex2_approx(__uint_as_float(sr[c][i]) - m_used);
+                        const uint32_t pt = f32_to_tf32_rna(pr);
+                        l_run += __uint_as_float(pt);
+                        sr[c][i] = pt;
+                    }
+                    tmem_st32(tsp + 32 * c, sr[c]);
                 }
-                tmem_st32(tsp + 32 * c, sr[c]);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < NK / 32; ++c) {
+                    tmem_ld32(tsp + 32 * c, sr[0]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(sr[0][i]) * kLog2e;
+                        if (32 * c + i >= valid) x = -INFINITY;
+                        const uint32_t pt = f32_to_tf32_rna(ex2_approx(x - m_used));
+                        l_run += __uint_as_float(pt);
+                        sr[0][i] = pt;
+                    }
+                    tmem_st32(tsp + 32 * c, sr[0]);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -402,7 +446,7 @@ template <int HD>
 cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
 {
     dim3 grid((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
-    attn_tc_kernel<HD><<<grid, 256, Layout<HD>::SMEM_BYTES, s>>>(maps, p);
+    attn_tc_kernel<HD><<<grid, Layout<HD>::THREADS, Layout<HD>::SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
 }
 

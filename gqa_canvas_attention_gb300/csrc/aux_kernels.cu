@@ -59,26 +59,79 @@ __global__ void __launch_bounds__(256) cache_vt_kernel(CachePrepParams p)
     }
 }
 
-// One CTA per (packed row R, kv group g); one thread per output column.
-__global__ void __launch_bounds__(256) combine_kernel(CombineParams p)
+// One CTA per (packed row R, kv group g) and 64-column slab; each thread owns four columns.
+// The partition weights are computed once per CTA into shared memory; the partial rows are then
+// read with independent float4 loads (several partitions in flight per thread).
+constexpr int kMaxCombineSplits = 64;
+
+__global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
 {
+    __shared__ float s_w[kMaxCombineSplits];
+    __shared__ float s_inv_den;
     const int R = blockIdx.x, g = blockIdx.y;
     if (R >= p.rows) return;
     const size_t stride = (size_t)p.nkv * p.rows_pad;   // between partitions
     const size_t row = (size_t)g * p.rows_pad + R;
-    float mmax = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[s * stride + row].x);
-    const int t = R / p.G, h = g * p.G + R % p.G;
-    float *dst = p.out + ((size_t)t * p.nh + h) * p.hd;
-    for (int c = threadIdx.x; c < p.hd; c += blockDim.x) {
-        float num = 0.f, den = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float2 ml = p.part_ml[s * stride + row];
-            const float w = p.log2_domain ? exp2f(ml.x - mmax) : expf(ml.x - mmax);
-            num = fmaf(w, p.part_o[(s * stride + row) * p.hd + c], num);
-            den = fmaf(w, ml.y, den);
+    if (threadIdx.x < 32) {
+        float m[2], l[2];
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int s = threadIdx.x + 32 * k;
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+            if (s < p.splits) {
+                const float2 ml = p.part_ml[s * stride + row];
+                m[k] = ml.x;
+                l[k] = ml.y;
+            }
+            mmax = fmaxf(mmax, m[k]);
         }
-        dst[c] = num / den;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+        float den = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int s = threadIdx.x + 32 * k;
+            if (s < p.splits) {
+                const float w = p.log2_domain ? exp2f(m[k] - mmax) : expf(m[k] - mmax);
+                s_w[s] = w;
+                den = fmaf(w, l[k], den);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (threadIdx.x == 0) s_inv_den = 1.0f / den;
+    }
+    __syncthreads();
+    const int c4 = blockIdx.z * 32 + (threadIdx.x & 31);     // float4 column group
+    const int sgrp = threadIdx.x >> 5;                       // 4 warps split the partitions
+    __shared__ float4 s_acc[4][32];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (4 * c4 < p.hd) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
+        const size_t hd4 = p.hd / 4;
+#pragma unroll 4
+        for (int s = sgrp; s < p.splits; s += 4) {
+            const float4 v = src[(s * stride + row) * hd4 + c4];
+            const float w = s_w[s];
+            acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+        }
+    }
+    s_acc[sgrp][threadIdx.x & 31] = acc;
+    __syncthreads();
+    if (sgrp == 0 && 4 * c4 < p.hd) {
+        float4 r = s_acc[0][threadIdx.x];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+            const float4 a = s_acc[k][threadIdx.x];
+            r.x += a.x; r.y += a.y; r.z += a.z; r.w += a.w;
+        }
+        const float inv = s_inv_den;
+        const int t = R / p.G, h = g * p.G + R % p.G;
+        float4 *dst = reinterpret_cast<float4 *>(p.out + ((size_t)t * p.nh + h) * p.hd);
+        dst[c4] = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
     }
 }
 
@@ -100,9 +153,9 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
-    dim3 grid(p.rows, p.nkv);
-    const int threads = p.hd < 256 ? p.hd : 256;
-    combine_kernel<<<grid, threads, 0, s>>>(p);
+    if (p.splits > kMaxCombineSplits) return cudaErrorInvalidValue;
+    dim3 grid(p.rows, p.nkv, (p.hd / 4 + 31) / 32);
+    combine_kernel<<<grid, 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

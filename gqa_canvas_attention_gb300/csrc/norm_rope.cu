@@ -116,38 +116,46 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
-// v-hat of 32 tokens x one kv head, normalised, TF32-rounded and written transposed.
+// v-hat of 32 tokens x one kv head, normalised, TF32-rounded and written transposed.  Every
+// warp first issues the loads of all its tokens, then reduces and stores them.
 template <int HD>
 __device__ __forceinline__ void v_transpose_block(const NormRopeParams &p, float *sbuf)
 {
     using L = Lane<HD>;
     constexpr int EPL = L::EPL;
+    constexpr int MAXT = kVtKeys / 8;          // tokens per warp with >= 8 warps
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int ngroups = (p.T + kVtKeys - 1) / kVtKeys;
     const int vb = blockIdx.x - p.T;
     const int g = vb / ngroups, t0 = (vb % ngroups) * kVtKeys;
-    for (int tt = warp; tt < kVtKeys; tt += nwarps) {
-        const int t = t0 + tt;
-        float x[EPL];
-        if (t < p.T) {
-            L::load(p.v + ((size_t)t * p.nkv + g) * HD, lane, x);
-            if (p.do_norm) {
-                float ss = 0.f;
+    float x[MAXT][EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) x[e] *= r;
-            }
+    for (int k = 0; k < MAXT; ++k) {
+        const int tt = warp + k * nwarps, t = t0 + tt;
+        if (tt < kVtKeys && t < p.T) {
+            L::load(p.v + ((size_t)t * p.nkv + g) * HD, lane, x[k]);
         } else {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) x[e] = 0.f;
+            for (int e = 0; e < EPL; ++e) x[k][e] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < MAXT; ++k) {
+        const int tt = warp + k * nwarps;
+        if (tt >= kVtKeys) break;
+        if (p.do_norm) {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) ss = fmaf(x[k][e], x[k][e], ss);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[k][e] *= r;
         }
 #pragma unroll
         for (int e = 0; e < EPL; ++e)
-            sbuf[tt * (HD + 1) + L::idx(lane, e)] = __uint_as_float(f32_to_tf32_rna(x[e]));
+            sbuf[tt * (HD + 1) + L::idx(lane, e)] = __uint_as_float(f32_to_tf32_rna(x[k][e]));
     }
     __syncthreads();
     for (int i = threadIdx.x; i < HD * kVtKeys; i += blockDim.x) {
@@ -158,7 +166,7 @@ __device__ __forceinline__ void v_transpose_block(const NormRopeParams &p, float
 }
 
 template <int HD, int MODE>
-__global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
+__global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
 {
     using L = Lane<HD>;
     constexpr int EPL = L::EPL;
@@ -175,6 +183,27 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
         }
     }
     const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int G = p.nh / p.nkv;
+    // in the tensor-core layouts the v heads are written by the transposing CTAs
+    const int jobs = p.nh + (MODE == kOutTc ? 1 : 2) * p.nkv;
+    auto job_src = [&](int job, int &kind, int &head) -> const float * {
+        if (job < p.nh) { kind = 0; head = job; return p.q + ((size_t)t * p.nh + head) * HD; }
+        if (job < p.nh + p.nkv) {
+            kind = 1; head = job - p.nh;
+            return p.k + ((size_t)t * p.nkv + head) * HD;
+        }
+        kind = 2; head = job - p.nh - p.nkv;
+        return p.v + ((size_t)t * p.nkv + head) * HD;
+    };
+    // the first job's row is loaded before the cos/sin work so that its latency overlaps it
+    float xpre[EPL];
+    if (warp < jobs) {
+        int kd, hh;
+        L::load(job_src(warp, kd, hh), lane, xpre);
+    }
     if (p.do_rope) {
         if (p.cos_sin) {
             const float *row = p.cos_sin + (size_t)t * 2 * HD;
@@ -194,23 +223,17 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p)
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int G = p.nh / p.nkv;
-    // in the tensor-core layouts the v heads are written by the transposing CTAs
-    const int jobs = p.nh + (MODE == kOutTc ? 1 : 2) * p.nkv;
     for (int job = warp; job < jobs; job += nwarps) {
         int kind, head;
-        if (job < p.nh) { kind = 0; head = job; }
-        else if (job < p.nh + p.nkv) { kind = 1; head = job - p.nh; }
-        else { kind = 2; head = job - p.nh - p.nkv; }
-        const float *src = kind == 0 ? p.q + ((size_t)t * p.nh + head) * HD
-                         : kind == 1 ? p.k + ((size_t)t * p.nkv + head) * HD
-                                     : p.v + ((size_t)t * p.nkv + head) * HD;
+        const float *src = job_src(job, kind, head);
         const float *w = kind == 0 ? p.wq : kind == 1 ? p.wk : nullptr;
         float x[EPL];
-        L::load(src, lane, x);
+        if (job == warp) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[e] = xpre[e];
+        } else {
+            L::load(src, lane, x);
+        }
         if (p.do_norm) {
             float ss = 0.f;
 #pragma unroll
@@ -281,12 +304,14 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
 {
     if (mode == kOutFp32) {
         const int jobs = p.nh + 2 * p.nkv;
-        const int warps = jobs < 8 ? jobs : 8;
+        const int warps = jobs < 16 ? jobs : 16;
         norm_rope_kernel<HD, kOutFp32><<<p.T, 32 * warps, 0, s>>>(p);
     } else {
         if constexpr (HD >= 64) {
             const int vblocks = p.nkv * ((p.T + kVtKeys - 1) / kVtKeys);
-            norm_rope_kernel<HD, kOutTc><<<p.T + vblocks, 256, 0, s>>>(p);
+            const int jobs = p.nh + p.nkv;
+            const int warps = jobs < 8 ? 8 : (jobs < 16 ? jobs : 16);   // >= 8 for the V blocks
+            norm_rope_kernel<HD, kOutTc><<<p.T + vblocks, 32 * warps, 0, s>>>(p);
         } else {
             return cudaErrorInvalidValue;
         }

@@ -49,28 +49,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes (or the hint,
+// in ns, expires), so a completed phase wakes it at once instead of at the next poll.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
                  : "memory");
     return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed, for at most limit_ns nanoseconds.
-// Returns false when the limit ran out (the caller records the failure and unwinds).
+// Wait until the phase with the given parity has completed, for at most about limit_ns
+// nanoseconds (counted in SM clock cycles at <= 2 GHz, so the bound only grows if the clock
+// drops).  Returns false when the limit ran out (the caller records the failure and unwinds).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    const long long t0 = clock64();
+    const long long lim = (long long)(limit_ns * 2ull);
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > lim) return false;
+    return true;
 }
 
 // ------------------------------------------------------------------ TMA

@@ -58,7 +58,7 @@ typedef struct dg_attn_plan dg_attn_plan;
 /* Option keys for dg_attn_set_option / dg_attn_get_option. */
 #define DG_OPT_PATH          1  /* DG_PATH_TC (default when hd is 64, 128 or 256) or DG_PATH_FP32 */
 #define DG_OPT_POS0          2  /* position of canvas row 0 (default ctx, the cache length) */
-#define DG_OPT_SPLITS        3  /* key-range partitions per query tile; 0 = chosen per plan */
+#define DG_OPT_SPLITS        3  /* key-range partitions per query tile (0..64); 0 = chosen per plan */
 #define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000) */
 #define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage */
 /* Read-only (dg_attn_get_option): */

@@ -168,7 +168,7 @@ def test_shapes(shape, path):
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], str(shape))
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 1000])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
 def test_forced_partitions(splits, path):
     T, ctx, nh, nkv, hd = 40, 700, 4, 2, 128
