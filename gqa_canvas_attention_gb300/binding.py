@@ -23,6 +23,7 @@ EXPORTED = [
     "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare", "dg_attn_norm_rope",
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
+    "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error",
 ]
 
 _lib = None
@@ -67,6 +68,11 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_status_string.restype = ctypes.c_char_p
     lib.dg_attn_last_error.argtypes = []
     lib.dg_attn_last_error.restype = ctypes.c_char_p
+    lib.dg_attn_forward_noalloc.argtypes = ([I] * 5 + [ctypes.c_float, ctypes.c_float, LL] +
+                                            [P] * 10)
+    lib.dg_attn_forward_noalloc.restype = I
+    lib.dg_attn_noalloc_last_error.argtypes = []
+    lib.dg_attn_noalloc_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -138,6 +144,16 @@ def dg_attn_attend(plan, q_hat, k_hat, v_hat, k_cache, v_cache, out, stream=None
     rc = load().dg_attn_attend(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(k_cache),
                                _ptr(v_cache), _ptr(out), _stream(stream))
     _check(rc, "dg_attn_attend")
+
+
+def dg_attn_forward_noalloc(nh, nkv, hd, ctx, T, eps, rope_theta, pos0, q, k_canvas, v_canvas,
+                            k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out, stream=None):
+    """The allocation-free fp32 forward (no plan); returns the status code."""
+    return load().dg_attn_forward_noalloc(nh, nkv, hd, ctx, T, float(eps), float(rope_theta),
+                                          int(pos0), _ptr(q), _ptr(k_canvas), _ptr(v_canvas),
+                                          _ptr(k_cache), _ptr(v_cache), _ptr(q_norm_w),
+                                          _ptr(k_norm_w), _ptr(cos_sin), _ptr(out),
+                                          _stream(stream))
 
 
 def dg_attn_set_option(plan, key, value):

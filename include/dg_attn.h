@@ -125,6 +125,24 @@ int dg_attn_profile_read(dg_attn_plan *plan, int stage, double *total_ms, long l
 
 void dg_attn_plan_destroy(dg_attn_plan *plan);
 
+/* Allocation-free forward.  The pages have no counterpart: this entry point exists for callers
+ * that cannot call cudaMalloc when they run attention (code inside a memory pool or arena it does
+ * not own, or a process whose device memory is reserved up front).  It computes the same block
+ * as dg_attn_forward on the exact-fp32 path with one key-range partition, without a plan: its
+ * working memory is a fixed 16 MiB __device__ array inside the library (held on every GPU that
+ * loads the library until the process exits), so it allocates nothing.  Sizes must satisfy
+ * T*(nh + 2*nkv)*hd*4 + hd*4 <= 16 MiB (checked: DG_ERR_ARG otherwise); other requirements as
+ * for dg_attn_plan_create / dg_attn_forward; pos0 < 0 means pos0 = ctx.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress), so make it before any stream
+ * capture.  Calls share the array: calls that overlap on the GPU race and must be serialised by
+ * the caller.  Host-side errors are described by dg_attn_noalloc_last_error(). */
+int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, float eps,
+                            float rope_theta, long long pos0, const float *q,
+                            const float *k_canvas, const float *v_canvas, const float *k_cache,
+                            const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                            const float *cos_sin, float *out, cudaStream_t stream);
+const char *dg_attn_noalloc_last_error(void);
+
 const char *dg_attn_status_string(int status);
 const char *dg_attn_last_error(void);
 

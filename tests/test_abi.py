@@ -54,3 +54,12 @@ def test_header_option_values_match_binding():
     vals = dict(re.findall(r"#define\s+(DG_\w+)\s+(\d+)", src))
     for name, v in vals.items():
         assert getattr(B, name) == int(v), name
+
+
+def test_noalloc_entry_point_checks_sizes_on_the_host(lib):
+    # rejected before any CUDA call: nh % nkv != 0, and a size beyond the fixed scratch
+    assert B.dg_attn_forward_noalloc(6, 4, 64, 0, 8, 1e-6, 1e4, -1, 16, 16, 16, None, None,
+                                     None, None, None, 16, stream=0) == B.DG_ERR_ARG
+    assert B.dg_attn_forward_noalloc(16, 16, 64, 0, 4096, 1e-6, 1e4, -1, 16, 16, 16, None,
+                                     None, None, None, None, 16, stream=0) == B.DG_ERR_ARG
+    assert "scratch" in lib.dg_attn_noalloc_last_error().decode()
