@@ -84,6 +84,7 @@ struct dg_attn_plan {
     int splits_opt;
     long long wait_limit_ms;
     int profile;
+    int inject_stall;
     int device, num_sms;
     bool tc_ok;
     // scratch
@@ -268,6 +269,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.S = p->S; a.G = p->G;
         a.rows = p->rows; a.rows_pad = p->rows_pad;
         a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
+        a.inject_stall = p->inject_stall;
         err = dg::launch_attn_tc(a, p->maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
     } else {
@@ -505,6 +507,9 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
         }
         p->wait_limit_ms = value;
         return DG_OK;
+    case DG_OPT_INJECT_STALL:
+        p->inject_stall = value ? 1 : 0;
+        return DG_OK;
     case DG_OPT_PROFILE:
         p->profile = value ? 1 : 0;
         for (size_t &u : p->ev_used) u = 0;
@@ -529,6 +534,7 @@ int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
     case DG_OPT_SPLITS: *value = p->splits_opt; return DG_OK;
     case DG_OPT_WAIT_LIMIT_MS: *value = p->wait_limit_ms; return DG_OK;
     case DG_OPT_PROFILE: *value = p->profile; return DG_OK;
+    case DG_OPT_INJECT_STALL: *value = p->inject_stall; return DG_OK;
     case DG_INFO_SPLITS_USED:
         split_layout(p, s, tps, nt);
         *value = s;

@@ -395,7 +395,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
         }
         if (ok && !mbar_wait_bounded(o_final, 0, limit)) ok = false;
         ok = __all_sync(0xffffffffu, ok);

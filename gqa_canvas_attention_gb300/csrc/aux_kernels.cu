@@ -59,80 +59,71 @@ __global__ void __launch_bounds__(256) cache_vt_kernel(CachePrepParams p)
     }
 }
 
-// One CTA per (packed row R, kv group g) and 64-column slab; each thread owns four columns.
-// The partition weights are computed once per CTA into shared memory; the partial rows are then
-// read with independent float4 loads (several partitions in flight per thread).
+// One warp per (packed row R, kv group g): every lane loads the (m, l) pairs and its slice of
+// the partial rows of a group of partitions at once (independent loads in flight), then the
+// weights b^(m_s - max m) are applied.  8 rows per CTA.
 constexpr int kMaxCombineSplits = 64;
+constexpr int kCombineRowsPerCta = 8;
+constexpr int kCombineBatch = 8;      // partitions whose loads are issued together
 
-__global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
+template <int HD>
+__global__ void __launch_bounds__(32 * kCombineRowsPerCta) combine_kernel(CombineParams p)
 {
-    __shared__ float s_w[kMaxCombineSplits];
-    __shared__ float s_inv_den;
-    const int R = blockIdx.x, g = blockIdx.y;
+    constexpr int V4 = HD / 128 > 0 ? HD / 128 : 1;   // float4 per lane (hd 256: 2, 128: 1)
+    constexpr bool PART = HD < 128;                   // hd 64 / 32: lanes beyond hd/4 idle
+    const int lane = threadIdx.x & 31;
+    const int R = blockIdx.x * kCombineRowsPerCta + (threadIdx.x >> 5);
+    const int g = blockIdx.y;
     if (R >= p.rows) return;
-    const size_t stride = (size_t)p.nkv * p.rows_pad;   // between partitions
+    const size_t stride = (size_t)p.nkv * p.rows_pad;   // rows between partitions
     const size_t row = (size_t)g * p.rows_pad + R;
-    if (threadIdx.x < 32) {
-        float m[2], l[2];
-        float mmax = -INFINITY;
+    float mmax = -INFINITY;
+    for (int s = lane; s < p.splits; s += 32) mmax = fmaxf(mmax, p.part_ml[s * stride + row].x);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int s = threadIdx.x + 32 * k;
-            m[k] = -INFINITY;
-            l[k] = 0.f;
+    for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    const bool active = !PART || lane < HD / 4;
+    float4 acc[V4];
+#pragma unroll
+    for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
+    const size_t hd4 = HD / 4;
+    for (int s0 = 0; s0 < p.splits; s0 += kCombineBatch) {
+        float2 ml[kCombineBatch];
+        float4 o[kCombineBatch][V4];
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+            const int s = s0 + k;
+            ml[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int v = 0; v < V4; ++v) o[k][v] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (s < p.splits) {
-                const float2 ml = p.part_ml[s * stride + row];
-                m[k] = ml.x;
-                l[k] = ml.y;
-            }
-            mmax = fmaxf(mmax, m[k]);
-        }
+                ml[k] = p.part_ml[s * stride + row];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
-        float den = 0.f;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int s = threadIdx.x + 32 * k;
-            if (s < p.splits) {
-                const float w = p.log2_domain ? exp2f(m[k] - mmax) : expf(m[k] - mmax);
-                s_w[s] = w;
-                den = fmaf(w, l[k], den);
+                for (int v = 0; v < V4; ++v)
+                    if (active) o[k][v] = src[(s * stride + row) * hd4 + lane + 32 * v];
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (threadIdx.x == 0) s_inv_den = 1.0f / den;
-    }
-    __syncthreads();
-    const int c4 = blockIdx.z * 32 + (threadIdx.x & 31);     // float4 column group
-    const int sgrp = threadIdx.x >> 5;                       // 4 warps split the partitions
-    __shared__ float4 s_acc[4][32];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (4 * c4 < p.hd) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
-        const size_t hd4 = p.hd / 4;
-#pragma unroll 4
-        for (int s = sgrp; s < p.splits; s += 4) {
-            const float4 v = src[(s * stride + row) * hd4 + c4];
-            const float w = s_w[s];
-            acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
-        }
-    }
-    s_acc[sgrp][threadIdx.x & 31] = acc;
-    __syncthreads();
-    if (sgrp == 0 && 4 * c4 < p.hd) {
-        float4 r = s_acc[0][threadIdx.x];
+        for (int k = 0; k < kCombineBatch; ++k) {
+            if (s0 + k >= p.splits) break;
+            const float w = p.log2_domain ? exp2f(ml[k].x - mmax) : expf(ml[k].x - mmax);
+            den = fmaf(w, ml[k].y, den);
 #pragma unroll
-        for (int k = 1; k < 4; ++k) {
-            const float4 a = s_acc[k][threadIdx.x];
-            r.x += a.x; r.y += a.y; r.z += a.z; r.w += a.w;
+            for (int v = 0; v < V4; ++v) {
+                acc[v].x = fmaf(w, o[k][v].x, acc[v].x); acc[v].y = fmaf(w, o[k][v].y, acc[v].y);
+                acc[v].z = fmaf(w, o[k][v].z, acc[v].z); acc[v].w = fmaf(w, o[k][v].w, acc[v].w);
+            }
         }
-        const float inv = s_inv_den;
-        const int t = R / p.G, h = g * p.G + R % p.G;
-        float4 *dst = reinterpret_cast<float4 *>(p.out + ((size_t)t * p.nh + h) * p.hd);
-        dst[c4] = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
     }
+    if (!active) return;
+    const float inv = 1.0f / den;
+    const int t = R / p.G, h = g * p.G + R % p.G;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + ((size_t)t * p.nh + h) * HD);
+#pragma unroll
+    for (int v = 0; v < V4; ++v)
+        dst[lane + 32 * v] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv,
+                                         acc[v].w * inv);
 }
 
 }  // namespace
@@ -154,8 +145,15 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
     if (p.splits > kMaxCombineSplits) return cudaErrorInvalidValue;
-    dim3 grid(p.rows, p.nkv, (p.hd / 4 + 31) / 32);
-    combine_kernel<<<grid, 128, 0, s>>>(p);
+    dim3 grid((p.rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta, p.nkv);
+    const int threads = 32 * kCombineRowsPerCta;
+    switch (p.hd) {
+    case 32: combine_kernel<32><<<grid, threads, 0, s>>>(p); break;
+    case 64: combine_kernel<64><<<grid, threads, 0, s>>>(p); break;
+    case 128: combine_kernel<128><<<grid, threads, 0, s>>>(p); break;
+    case 256: combine_kernel<256><<<grid, threads, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ struct AttnTcParams {
     unsigned long long wait_limit_ns;
     int T, nh, nkv, S, G, rows, rows_pad;
     int splits, tiles_per_split, n_tiles;
+    int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
 };
 
 struct CombineParams {

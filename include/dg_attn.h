@@ -61,6 +61,9 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_OPT_SPLITS        3  /* key-range partitions per query tile (0..64); 0 = chosen per plan */
 #define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000) */
 #define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage */
+#define DG_OPT_INJECT_STALL  6  /* test hook: 1 = the tensor-core kernel's softmax withholds its
+                                   first "P ready" signal, so the bounded waits behind it run out
+                                   and the forward ends with DG_ERR_TIMEOUT (no fault, no hang) */
 /* Read-only (dg_attn_get_option): */
 #define DG_INFO_SPLITS_USED  16 /* partitions the next forward will use */
 #define DG_INFO_SCRATCH_BYTES 17 /* device bytes the plan holds */

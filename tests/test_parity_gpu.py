@@ -269,3 +269,21 @@ def test_errors_are_reported_not_raised_on_device():
         p32.set(B.DG_OPT_PATH, B.DG_PATH_TC)
     assert e.value.status == B.DG_ERR_UNSUPPORTED
     assert plan.sync_status() == B.DG_OK
+
+
+def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable():
+    """Failure detection without a fault: the softmax withholds one P-ready signal (a flag that
+    nothing else sets), every wait behind it runs out after the short limit, the kernel unwinds
+    (TMEM freed, loads drained) and the host reads DG_ERR_TIMEOUT; the next forward is exact."""
+    T, ctx, nh, nkv, hd = 40, 300, 4, 2, 256
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=31)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_WAIT_LIMIT_MS, 100).set(B.DG_OPT_INJECT_STALL, 1)
+    plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["k_cache"], dd["v_cache"],
+                 dd["q_norm_w"], dd["k_norm_w"])
+    assert plan.sync_status() == B.DG_ERR_TIMEOUT
+    assert plan.sync_status() == B.DG_OK          # read-and-clear
+    plan.set(B.DG_OPT_INJECT_STALL, 0)
+    out = run_forward(plan, dd)
+    check(out, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, [(0, T)], "after-timeout")
