@@ -7,8 +7,7 @@
 //   fp32 path: q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd]
 //   tensor-core path: Q hi/lo bf16 [nkv, rows_pad, hd] (row R = t*G + h mod G, padded to 128),
 //             K hi/lo bf16 [nkv, S, hd] (S = ctx + T) with the cache in rows 0..ctx-1 and the
-//             canvas in rows ctx..ctx+T-1; V transposed and TF32-rounded [nkv, hd, S_pad], keys
-//             contiguous (the tensor cores take TF32 operands K-major only)
+//             canvas in rows ctx..ctx+T-1; V in fp16, same layout
 //   partials  O [splits, nkv, rows_pad, hd] and (m, l) [splits, nkv, rows_pad]
 //   status    one uint32 that kernels OR their wait failures into
 #include "../../include/dg_attn.h"
@@ -92,7 +91,7 @@ struct dg_attn_plan {
     uint32_t *status;
     float *q32, *k32, *v32;
     __nv_bfloat16 *qh, *ql, *kh, *kl;
-    float *vt;
+    __half *vh;
     float *part_o;
     float2 *part_ml;
     int part_capacity;           // partitions the partial buffers hold
@@ -123,7 +122,7 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 void free_scratch(dg_attn_plan *p)
 {
     void *ptrs[] = {p->inv_freq, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
-                    p->kh, p->kl, p->vt, p->part_o, p->part_ml};
+                    p->kh, p->kl, p->vh, p->part_o, p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
     for (auto &v : p->ev) {
@@ -229,8 +228,8 @@ int build_maps(dg_attn_plan *p)
                     64, nk, p->hd);
     ok &= encode_3d(&p->maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kl, p->hd, p->S, p->nkv,
                     64, nk, p->hd);
-    ok &= encode_3d(&p->maps.vt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->vt, p->S, p->hd, p->nkv,
-                    32, p->hd, p->S_pad);
+    ok &= encode_3d(&p->maps.vh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->vh, p->hd, p->S, p->nkv,
+                    64, nk, p->hd);
     if (!ok) {
         set_error("cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
         return DG_ERR_CUDA;
@@ -248,7 +247,7 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
     n.eps = p->eps;
     n.do_norm = 1; n.do_rope = 1;
     n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
-    n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vt = p->vt;
+    n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vh = p->vh;
     return n;
 }
 
@@ -331,7 +330,7 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
     if (p->path == DG_PATH_TC) {
         // the per-call conversion overwrites the plan's cache copy
         p->cache_ready = false;
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->S_pad,
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, p->nkv, p->ctx, p->S, p->S_pad,
                               p->hd};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
@@ -407,7 +406,6 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
 
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
     const size_t nqt = (size_t)nkv * p->rows_pad * hd, nkt = (size_t)nkv * p->S * hd;
-    const size_t nvt = (size_t)nkv * hd * p->S_pad;
     p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
     p->status = (uint32_t *)dalloc(p, sizeof(uint32_t) * 4, err);
     p->q32 = (float *)dalloc(p, nq * sizeof(float), err);
@@ -418,7 +416,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
         p->ql = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
         p->kh = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
         p->kl = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
-        p->vt = (float *)dalloc(p, nvt * 4, err);
+        p->vh = (__half *)dalloc(p, nkt * 2, err);
     }
     if (err != cudaSuccess) {
         cuda_fail(err, "allocating plan scratch");
@@ -568,7 +566,7 @@ int dg_attn_cache_prepare(dg_attn_plan *p, const float *k_cache, const float *v_
         return DG_ERR_ALIGN;
     }
     if (p->path == DG_PATH_TC) {
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vt, p->nkv, p->ctx, p->S, p->S_pad,
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, p->nkv, p->ctx, p->S, p->S_pad,
                               p->hd};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;

@@ -8,23 +8,24 @@
 //
 // Precision (scores reach |s| ~ 90 because of scaling 1.0, so one TF32 rounding of q or k moves
 // outputs by ~1e-2): Q.K^T is computed as  qh.kh + qh.kl + ql.kh  with bf16 hi/lo splits of both
-// operands (three kind::f16 MMAs, ~16 significant bits per operand); P.V runs in TF32
-// (kind::tf32) with P and V rounded to nearest.
+// operands (three kind::f16 MMAs, ~16 significant bits per operand).  P.V runs with P and V
+// rounded to fp16: the same 10 explicit mantissa bits as TF32 with round to nearest, P <= 256 and
+// the normed V well inside the fp16 range, at twice the TF32 rate and half the bytes of V.
 //
 // Roles (32 * (7 + NQI) threads):
 //   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
 //            lives in shared memory);
 //   warp 1   P.V issuer (one thread) and TMEM owner;
-//   warp 2   V producer: TMA of the V^T tile (keys contiguous: TF32 operands must be K-major)
-//            into a VST-deep ring;
+//   warp 2   V producer: TMA of the fp16 V tile ([keys, hd], an MN-major operand) into a
+//            VST-deep ring;
 //   warp 3, 8.. Q.K^T issuers (one thread each).  A single thread can hand the tensor core only
 //            about one tcgen05.mma per ~60 cycles, far less than the 16-64 cycles of work in each
 //            128 x NK x 16 product, so key tiles are dealt round-robin to NQI issuers; issuer q
 //            owns the score buffers and K ring slots of the tiles j = q (mod NQI), so every
 //            mbarrier keeps a single in-order consumer;
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
-//            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to TF32, written back over S in
-//            place, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
+//            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to fp16, packed two per column
+//            over the start of S, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
 //            has grown by more than 2^8 (so P <= 256 in between), and write the output.
 // TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit and the CTA unwinds.
@@ -36,12 +37,12 @@ namespace {
 
 template <int HD> struct Cfg;
 template <> struct Cfg<256> {
-    static constexpr int NK = 32, NSP = 3, KST = 3, VST = 2, NQI = 3;
+    static constexpr int NK = 32, NSP = 4, KST = 4, VST = 2, NQI = 4;
     static constexpr bool QL_TMEM = false;
     static constexpr int O_COL = 0, QH_COL = 256, QL_COL = 0, SP_COL = 384;
 };
 template <> struct Cfg<128> {
-    static constexpr int NK = 64, NSP = 4, KST = 4, VST = 3, NQI = 2;
+    static constexpr int NK = 64, NSP = 4, KST = 4, VST = 4, NQI = 4;
     static constexpr bool QL_TMEM = true;
     static constexpr int O_COL = 0, QH_COL = 128, QL_COL = 192, SP_COL = 256;
 };
@@ -54,11 +55,11 @@ template <> struct Cfg<64> {
 template <int HD> struct Layout {
     using C = Cfg<HD>;
     static constexpr int KPANELS = HD / 64;                 // 128-byte bf16 panels of a K row
-    static constexpr int VPANELS = Cfg<HD>::NK / 32;        // 32-key (128-byte) panels of V^T
+    static constexpr int VPANELS = HD / 64;                 // 128-byte fp16 panels of a V row
     static constexpr int QL_BYTES = C::QL_TMEM ? 0 : kTileM * HD * 2;
     static constexpr int KPANEL_BYTES = C::NK * 128;
     static constexpr int KSTAGE_BYTES = 2 * KPANELS * KPANEL_BYTES;   // hi + lo
-    static constexpr int VPANEL_BYTES = HD * 128;          // hd rows of 32 keys
+    static constexpr int VPANEL_BYTES = C::NK * 128;       // NK key rows of 64 hd values
     static constexpr int VSTAGE_BYTES = VPANELS * VPANEL_BYTES;
     static constexpr int K_OFF = QL_BYTES;
     static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
@@ -121,7 +122,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         fence_mbar_init();
         prefetch_tmap(&maps.kh);
         prefetch_tmap(&maps.kl);
-        prefetch_tmap(&maps.vt);
+        prefetch_tmap(&maps.vh);
         if (!C::QL_TMEM) prefetch_tmap(&maps.ql);
     }
     if (warp == 1) {
@@ -183,7 +184,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 const int key0 = (tile0 + it) * NK;
                 mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::VPANELS; ++pn)
-                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vt, &v_full[s], key0 + pn * 32, 0, g);
+                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64, key0, g);
                 ++issued[s];
             }
             if (!ok) atomicOr(p.status, kErrWaitProducer);
@@ -195,7 +196,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         // ---------------------------------------------------------------- MMA issuers
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
-            constexpr uint32_t idesc_pv = make_idesc(2, 0, 0, kTileM, HD);
+            constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, kTileM, HD);   // fp16, B MN-major
             const uint32_t t_o = tbase + C::O_COL;
             const uint32_t t_qh = tbase + C::QH_COL;
             const uint32_t t_ql = tbase + C::QL_COL;
@@ -203,7 +204,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             // Descriptors are built once; per stage / k-step only the start address moves
             // (the 14-bit address field cannot carry: shared addresses are < 256 KiB).
             const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + Lay::K_OFF), 16, 1024);
-            const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + Lay::V_OFF), 16, 1024);
+            // V is MN-major: 64-wide hd panels NK rows apart (leading offset), 8-key groups 1 KiB
+            // apart (stride offset)
+            const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + Lay::V_OFF), Lay::VPANEL_BYTES, 1024);
             const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
             const int me = warp == 1 ? 0 : 1 + (warp == 3 ? 0 : warp - 7);   // drain slot
             bool ok = true;
@@ -216,9 +219,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     tc_fence_after();
                     const uint64_t vd = vdesc0 + (uint64_t)((vs * Lay::VSTAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < NK / 8; ++ks) {
-                        const uint64_t bdesc = vd + (uint64_t)(((ks >> 2) * Lay::VPANEL_BYTES + (ks & 3) * 32) >> 4);
-                        mma_tf32_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < NK / 16; ++ks) {
+                        // keys 16ks..16ks+15: two 8-row groups, 2 KiB into every hd panel
+                        const uint64_t bdesc = vd + (uint64_t)((ks * 16 * 128) >> 4);
+                        mma_bf16_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&v_empty[vs]);
                     mma_commit(&sp_free[b]);
@@ -365,32 +369,41 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 l_run *= alpha;
                 m_used = m_new;
             }
+            // P in fp16, two keys per 32-bit column, written over the start of the score buffer
+            // (chunk c of 32 scores lands in columns 16c..16c+15, already read)
             if constexpr (NK <= 64) {
 #pragma unroll
                 for (int c = 0; c < RC; ++c) {
+                    uint32_t pw[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float pr = ex2_approx(__uint_as_float(sr[c][i]) - m_used);
-                        const uint32_t pt = f32_to_tf32_rna(pr);
-                        l_run += __uint_as_float(pt);
-                        sr[c][i] = pt;
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2_approx(__uint_as_float(sr[c][2 * i]) - m_used);
+                        const float p1 = ex2_approx(__uint_as_float(sr[c][2 * i + 1]) - m_used);
+                        const __half2 h = __floats2half2_rn(p0, p1);
+                        const float2 hf = __half22float2(h);
+                        l_run += hf.x + hf.y;
+                        pw[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
-                    tmem_st32(tsp + 32 * c, sr[c]);
+                    tmem_st16(tsp + 16 * c, pw);
                 }
             } else {
 #pragma unroll 1
                 for (int c = 0; c < NK / 32; ++c) {
                     tmem_ld32(tsp + 32 * c, sr[0]);
                     tmem_wait_ld();
+                    uint32_t pw[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(sr[0][i]) * kLog2e;
-                        if (32 * c + i >= valid) x = -INFINITY;
-                        const uint32_t pt = f32_to_tf32_rna(ex2_approx(x - m_used));
-                        l_run += __uint_as_float(pt);
-                        sr[0][i] = pt;
+                    for (int i = 0; i < 16; ++i) {
+                        float x0 = __uint_as_float(sr[0][2 * i]) * kLog2e;
+                        float x1 = __uint_as_float(sr[0][2 * i + 1]) * kLog2e;
+                        if (32 * c + 2 * i >= valid) x0 = -INFINITY;
+                        if (32 * c + 2 * i + 1 >= valid) x1 = -INFINITY;
+                        const __half2 h = __floats2half2_rn(ex2_approx(x0 - m_used), ex2_approx(x1 - m_used));
+                        const float2 hf = __half22float2(h);
+                        l_run += hf.x + hf.y;
+                        pw[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
-                    tmem_st32(tsp + 32 * c, sr[0]);
+                    tmem_st16(tsp + 16 * c, pw);
                 }
             }
             tmem_wait_st();

@@ -1,8 +1,7 @@
 // aux_kernels.cu -- the two streaming helpers around the attention kernels:
 //  * cache_prep: converts an encoder cache [nkv, ctx, hd] (page "inferencelayer 0.2.3,
 //    src/diffusion_gemma_gpu.rs", DgGpuCache / upload_cache: already normed and roped) into the
-//    tensor-core operand arrays: K as a bf16 hi/lo pair [nkv, S, hd]; V rounded to TF32 (round
-//    to nearest) and transposed to [nkv, hd, S_pad] through 32 x 32 shared-memory tiles;
+//    tensor-core operand arrays [nkv, S, hd]: K as a bf16 hi/lo pair, V rounded to fp16;
 //  * combine: merges the partial results of the key-range partitions (split-KV) of one query
 //    row with the log-sum-exp rule  out = sum_s w_s O_s / sum_s w_s l_s,  w_s = b^(m_s - max m).
 #include "dg_internal.cuh"
@@ -11,7 +10,7 @@
 namespace dg {
 namespace {
 
-__global__ void __launch_bounds__(256) cache_k_kernel(CachePrepParams p)
+__global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
 {
     const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
     const int hd4 = p.hd / 4;
@@ -22,6 +21,7 @@ __global__ void __launch_bounds__(256) cache_k_kernel(CachePrepParams p)
         const size_t g = row / p.ctx, j = row % p.ctx;
         const size_t dst = (g * p.S + j) * p.hd + 4 * (size_t)c4;
         const float4 k = reinterpret_cast<const float4 *>(p.k_cache)[i];
+        const float4 v = reinterpret_cast<const float4 *>(p.v_cache)[i];
         const float kx[4] = {k.x, k.y, k.z, k.w};
         __nv_bfloat16 hi[4], lo[4];
 #pragma unroll
@@ -37,25 +37,10 @@ __global__ void __launch_bounds__(256) cache_k_kernel(CachePrepParams p)
         ul.x = *reinterpret_cast<uint32_t *>(&l01); ul.y = *reinterpret_cast<uint32_t *>(&l23);
         *reinterpret_cast<uint2 *>(p.kh + dst) = uh;
         *reinterpret_cast<uint2 *>(p.kl + dst) = ul;
-    }
-}
-
-// One 32-key x 32-dim tile per CTA (32 x 8 threads): read rows of v_cache, write rows of V^T.
-__global__ void __launch_bounds__(256) cache_vt_kernel(CachePrepParams p)
-{
-    __shared__ float tile[32][33];
-    const int j0 = blockIdx.x * 32, d0 = blockIdx.y * 32, g = blockIdx.z;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int jj = ty; jj < 32; jj += 8) {
-        const int j = j0 + jj;
-        float v = 0.f;
-        if (j < p.ctx) v = p.v_cache[((size_t)g * p.ctx + j) * p.hd + d0 + tx];
-        tile[jj][tx] = __uint_as_float(f32_to_tf32_rna(v));
-    }
-    __syncthreads();
-    for (int dd = ty; dd < 32; dd += 8) {
-        const int j = j0 + tx;
-        if (j < p.ctx) p.vt[((size_t)g * p.hd + d0 + dd) * p.S_pad + j] = tile[tx][dd];
+        __half2 v01 = __floats2half2_rn(v.x, v.y), v23 = __floats2half2_rn(v.z, v.w);
+        uint2 uv;
+        uv.x = *reinterpret_cast<uint32_t *>(&v01); uv.y = *reinterpret_cast<uint32_t *>(&v23);
+        *reinterpret_cast<uint2 *>(p.vh + dst) = uv;
     }
 }
 
@@ -134,11 +119,7 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
     if (n4 == 0) return cudaSuccess;
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    cache_k_kernel<<<blocks, 256, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dim3 grid((p.ctx + 31) / 32, p.hd / 32, p.nkv);
-    cache_vt_kernel<<<grid, 256, 0, s>>>(p);
+    cache_kv_kernel<<<blocks, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -26,11 +27,8 @@ constexpr int kFp32TileM = 32;
 // What the first-stage kernel writes.
 enum NormOut : int {
     kOutFp32 = 0,   // q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd] fp32 (input layouts)
-    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, tf32-rounded v_hat^T (tensor-core layouts)
+    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, fp16 v_hat (tensor-core layouts)
 };
-
-// Keys per block of the transposed V layout written through shared memory.
-constexpr int kVtKeys = 32;
 
 struct NormRopeParams {
     const float *q, *k, *v;        // [T, nh*hd], [T, nkv*hd], [T, nkv*hd]
@@ -46,14 +44,14 @@ struct NormRopeParams {
     // kOutTc destinations
     __nv_bfloat16 *qh, *ql;        // [nkv, rows_pad, hd]
     __nv_bfloat16 *kh, *kl;        // [nkv, S, hd] (canvas rows ctx..ctx+T-1)
-    float *vt;                     // [nkv, hd, S_pad]: v_hat transposed, keys contiguous
+    __half *vh;                    // [nkv, S, hd] fp16 (canvas rows ctx..ctx+T-1)
 };
 
 // Conversion of a cache [nkv, ctx, hd] into the tensor-core operand arrays (rows 0..ctx-1).
 struct CachePrepParams {
     const float *k_cache, *v_cache;
     __nv_bfloat16 *kh, *kl;
-    float *vt;                     // [nkv, hd, S_pad] (cache keys in columns 0..ctx-1)
+    __half *vh;                    // [nkv, S, hd] fp16 (cache rows 0..ctx-1)
     int nkv, ctx, S, S_pad, hd;
 };
 
@@ -93,7 +91,7 @@ struct CombineParams {
 struct TcMaps {
     CUtensorMap ql;                // bf16 [nkv][rows_pad][hd], box {64, 128, 1}
     CUtensorMap kh, kl;            // bf16 [nkv][S][hd], box {64, NK, 1}
-    CUtensorMap vt;                // fp32 [nkv][hd][S_pad] (keys innermost), box {32, hd, 1}
+    CUtensorMap vh;                // fp16 [nkv][S][hd], box {64, NK, 1}
 };
 
 // Tile geometry of the tensor-core kernel for a head dimension.

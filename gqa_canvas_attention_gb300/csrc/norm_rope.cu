@@ -15,10 +15,8 @@
 // shuffle reduction and the rotate-half partner of element i (i +- hd/2) is either in the same
 // lane or in lane ^ 16.
 //
-// For the tensor-core layouts, v-hat is stored transposed ([nkv, hd, keys], keys contiguous) so
-// that it is a K-major operand of the P.V product: extra CTAs after the T token CTAs each take
-// 32 consecutive tokens of one v head, normalise them (one warp per token), round to TF32 and
-// write the transpose through shared memory as 128-byte runs of keys.
+// For the tensor-core layouts q-hat and k-hat are written as bf16 hi/lo pairs and v-hat as fp16,
+// next to the cache rows of the same kv head.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -70,20 +68,20 @@ struct Lane {
             reinterpret_cast<float4 *>(row)[32 + l] = make_float4(x[4], x[5], x[6], x[7]);
         }
     }
-    // bf16 stores of EPL elements per lane (HD >= 64 in the tensor-core layouts)
-    __device__ static __forceinline__ void store_bf16(__nv_bfloat16 *row, int l,
-                                                      const __nv_bfloat16 (&x)[EPL])
+    // 16-bit stores of EPL elements per lane (HD >= 64 in the tensor-core layouts)
+    template <typename H, typename H2>
+    __device__ static __forceinline__ void store_16(H *row, int l, const H (&x)[EPL])
     {
         static_assert(HD >= 64, "tensor-core layouts need hd >= 64");
         if constexpr (HD == 64) {
-            __nv_bfloat162 v; v.x = x[0]; v.y = x[1];
-            reinterpret_cast<__nv_bfloat162 *>(row)[l] = v;
+            H2 v; v.x = x[0]; v.y = x[1];
+            reinterpret_cast<H2 *>(row)[l] = v;
         } else if constexpr (HD == 128) {
-            __nv_bfloat162 a, b; a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
+            H2 a, b; a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
             uint2 u; u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
             reinterpret_cast<uint2 *>(row)[l] = u;
         } else {
-            __nv_bfloat162 a, b, c, d;
+            H2 a, b, c, d;
             a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
             c.x = x[4]; c.y = x[5]; d.x = x[6]; d.y = x[7];
             uint2 u, w;
@@ -116,79 +114,20 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
-// v-hat of 32 tokens x one kv head, normalised, TF32-rounded and written transposed.  Every
-// warp first issues the loads of all its tokens, then reduces and stores them.
-template <int HD>
-__device__ __forceinline__ void v_transpose_block(const NormRopeParams &p, float *sbuf)
-{
-    using L = Lane<HD>;
-    constexpr int EPL = L::EPL;
-    constexpr int MAXT = kVtKeys / 8;          // tokens per warp with >= 8 warps
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int ngroups = (p.T + kVtKeys - 1) / kVtKeys;
-    const int vb = blockIdx.x - p.T;
-    const int g = vb / ngroups, t0 = (vb % ngroups) * kVtKeys;
-    float x[MAXT][EPL];
-#pragma unroll
-    for (int k = 0; k < MAXT; ++k) {
-        const int tt = warp + k * nwarps, t = t0 + tt;
-        if (tt < kVtKeys && t < p.T) {
-            L::load(p.v + ((size_t)t * p.nkv + g) * HD, lane, x[k]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) x[k][e] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < MAXT; ++k) {
-        const int tt = warp + k * nwarps;
-        if (tt >= kVtKeys) break;
-        if (p.do_norm) {
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) ss = fmaf(x[k][e], x[k][e], ss);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) x[k][e] *= r;
-        }
-#pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            sbuf[tt * (HD + 1) + L::idx(lane, e)] = __uint_as_float(f32_to_tf32_rna(x[k][e]));
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < HD * kVtKeys; i += blockDim.x) {
-        const int d = i / kVtKeys, tt = i % kVtKeys;
-        const int t = t0 + tt;
-        if (t < p.T) p.vt[((size_t)g * HD + d) * p.S_pad + p.ctx + t] = sbuf[tt * (HD + 1) + d];
-    }
-}
-
 template <int HD, int MODE>
 __global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
 {
     using L = Lane<HD>;
     constexpr int EPL = L::EPL;
     constexpr int HALF = HD / 2;
-    constexpr int SBUF = (MODE == kOutTc) ? kVtKeys * (HD + 1) : 2 * HD;
-    __shared__ float sbuf[SBUF];
-    float *s_cos = sbuf;
-    float *s_sin = sbuf + HD;
-
-    if constexpr (MODE == kOutTc) {
-        if ((int)blockIdx.x >= p.T) {
-            v_transpose_block<HD>(p, sbuf);
-            return;
-        }
-    }
+    __shared__ float s_cos[HD];
+    __shared__ float s_sin[HD];
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int G = p.nh / p.nkv;
-    // in the tensor-core layouts the v heads are written by the transposing CTAs
-    const int jobs = p.nh + (MODE == kOutTc ? 1 : 2) * p.nkv;
+    const int jobs = p.nh + 2 * p.nkv;
     auto job_src = [&](int job, int &kind, int &head) -> const float * {
         if (job < p.nh) { kind = 0; head = job; return p.q + ((size_t)t * p.nh + head) * HD; }
         if (job < p.nh + p.nkv) {
@@ -273,7 +212,14 @@ __global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
                                    : p.v_out + ((size_t)t * p.nkv + head) * HD;
             L::store(dst, lane, x);
         } else {
-            {
+            if (kind == 2) {
+                __half v[EPL];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) v[e] = __float2half_rn(x[e]);
+                if constexpr (HD >= 64)
+                    L::template store_16<__half, __half2>(p.vh + ((size_t)head * p.S + p.ctx + t) * HD,
+                                                          lane, v);
+            } else {
                 __nv_bfloat16 hi[EPL], lo[EPL];
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
@@ -291,8 +237,8 @@ __global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
                     dh = p.kh; dl = p.kl;
                 }
                 if constexpr (HD >= 64) {
-                    L::store_bf16(dh + off, lane, hi);
-                    L::store_bf16(dl + off, lane, lo);
+                    L::template store_16<__nv_bfloat16, __nv_bfloat162>(dh + off, lane, hi);
+                    L::template store_16<__nv_bfloat16, __nv_bfloat162>(dl + off, lane, lo);
                 }
             }
         }
@@ -308,10 +254,9 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
         norm_rope_kernel<HD, kOutFp32><<<p.T, 32 * warps, 0, s>>>(p);
     } else {
         if constexpr (HD >= 64) {
-            const int vblocks = p.nkv * ((p.T + kVtKeys - 1) / kVtKeys);
-            const int jobs = p.nh + p.nkv;
-            const int warps = jobs < 8 ? 8 : (jobs < 16 ? jobs : 16);   // >= 8 for the V blocks
-            norm_rope_kernel<HD, kOutTc><<<p.T + vblocks, 32 * warps, 0, s>>>(p);
+            const int jobs = p.nh + 2 * p.nkv;
+            const int warps = jobs < 16 ? jobs : 16;
+            norm_rope_kernel<HD, kOutTc><<<p.T, 32 * warps, 0, s>>>(p);
         } else {
             return cudaErrorInvalidValue;
         }

@@ -139,7 +139,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32 dense MMAs with an fp32 accumulator.
-//   ab_fmt: 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32)
+//   ab_fmt: 0 = fp16, 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32)
 //   a_mn / b_mn: 1 when that operand is MN-major in shared memory
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, uint32_t a_mn, uint32_t b_mn,
                                                   uint32_t M, uint32_t N)
@@ -222,6 +222,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                  "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
                  "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
                  "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit words.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+                 "r"(r[14]), "r"(r[15])
                  : "memory");
 }
 

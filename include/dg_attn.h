@@ -52,7 +52,8 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_ERR_STATE       6  /* the call needs state the plan does not hold */
 
 /* Arithmetic paths (option DG_OPT_PATH). */
-#define DG_PATH_TC   0  /* tensor cores: Q.K^T as three bf16 MMAs (hi/lo split), P.V in TF32 */
+#define DG_PATH_TC   0  /* tensor cores: Q.K^T as three bf16 MMAs (hi/lo split), P.V in fp16 (10-bit
+                           mantissa, the TF32 rounding); cache V must lie within fp16 range */
 #define DG_PATH_FP32 1  /* exact fp32 on the CUDA cores */
 
 /* Option keys for dg_attn_set_option / dg_attn_get_option. */
