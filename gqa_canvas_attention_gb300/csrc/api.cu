@@ -146,15 +146,20 @@ int qtiles_for(const dg_attn_plan *p)
     return ((p->rows + tm - 1) / tm) * p->nkv;
 }
 
-// Key-range partitions: minimise (waves of CTAs) x (tiles per CTA + a fixed start-up cost),
-// with the start-up cost in tile units; ties go to fewer partitions.
+// Key-range partitions: minimise (waves of CTAs) x (tiles per CTA + the fixed start-up and drain
+// cost of a CTA) + the combine kernel's cost, all in units of one key tile's time.  The
+// tensor-core figures were measured on the GB300 at hd = 256: ~0.9 us per 32-key tile and
+// ~8 us of start-up plus epilogue per CTA; the combine reads the partitions' rows once.
 int auto_splits(const dg_attn_plan *p)
 {
     const int nt = n_tiles_for(p);
     const int qt = qtiles_for(p);
-    const int per_sm = p->path == DG_PATH_TC ? 1 : 2;
+    const bool tc = p->path == DG_PATH_TC;
+    const int per_sm = tc ? 1 : 2;
     const int slots = p->num_sms * per_sm;
-    const double startup = p->path == DG_PATH_TC ? 3.0 : 1.0;
+    const double tile_us = tc ? 0.9 : 2.0;
+    const double startup = tc ? 8.0 / tile_us : 1.0;
+    const double rows = (double)qt * (tc ? dg::kTileM : dg::kFp32TileM);
     int best = 1;
     double best_cost = 1e300;
     for (int s = 1; s <= nt && s <= 64; ++s) {
@@ -162,7 +167,11 @@ int auto_splits(const dg_attn_plan *p)
         const int s_eff = (nt + tps - 1) / tps;
         if (s_eff != s) continue;
         const int waves = (qt * s + slots - 1) / slots;
-        const double cost = waves * (tps + startup) + (s > 1 ? 0.5 : 0.0);
+        double cost = waves * (tps + startup);
+        if (s > 1) {
+            const double bytes = rows * p->hd * 4.0 * (s + 1);
+            cost += (3.0 + bytes / 3.0e6) / tile_us;   // launch + traffic at ~3 TB/s (bytes/us)
+        }
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best = s;

@@ -416,33 +416,51 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             if (lane == 0) atomicOr(p.status, kErrWaitSoftmax);
         } else {
             tc_fence_after();
-            const bool live = Rg < p.rows;
-            float *dst;
+            // Every MMA has completed, so the K ring is free: each warp stages its 32 rows x 32
+            // columns of O in a shared-memory tile (row pitch 36 floats, conflict-free for float4)
+            // and writes it back row-contiguous: a store instruction covers 128 bytes of each of
+            // 4 output rows.  Each lane computes its own row's destination once.
+            float *stage = reinterpret_cast<float *>(smem + Lay::K_OFF) + quarter * (32 * 36);
             float scale;
+            float *mydst = nullptr;
             if (p.splits == 1) {
-                const int t = Rg / p.G, h = g * p.G + Rg % p.G;
-                dst = live ? p.out + ((size_t)t * p.nh + h) * HD : nullptr;
                 scale = 1.0f / l_run;
+                if (Rg < p.rows) {
+                    const int t = Rg / p.G, h = g * p.G + Rg % p.G;
+                    mydst = p.out + ((size_t)t * p.nh + h) * HD;
+                }
             } else {
-                const size_t row = ((size_t)split * p.nkv + g) * p.rows_pad + Rg;
-                dst = p.part_o + row * HD;
                 scale = 1.0f;
-                if (live) p.part_ml[row] = make_float2(m_used, l_run);
+                const size_t row = ((size_t)split * p.nkv + g) * p.rows_pad + Rg;
+                if (Rg < p.rows) {
+                    p.part_ml[row] = make_float2(m_used, l_run);
+                    mydst = p.part_o + row * HD;
+                }
             }
+            const int sub = lane & 7, rsub = lane >> 3;
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t orr[32];
                 tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
                 tmem_wait_ld();
-                if (live) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        d4[v] = make_float4(__uint_as_float(orr[4 * v]) * scale,
-                                            __uint_as_float(orr[4 * v + 1]) * scale,
-                                            __uint_as_float(orr[4 * v + 2]) * scale,
-                                            __uint_as_float(orr[4 * v + 3]) * scale);
+                for (int v = 0; v < 8; ++v)
+                    *reinterpret_cast<float4 *>(stage + lane * 36 + 4 * v) =
+                        make_float4(__uint_as_float(orr[4 * v]) * scale,
+                                    __uint_as_float(orr[4 * v + 1]) * scale,
+                                    __uint_as_float(orr[4 * v + 2]) * scale,
+                                    __uint_as_float(orr[4 * v + 3]) * scale);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int j = 4 * k + rsub;
+                    float *d = reinterpret_cast<float *>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mydst), j));
+                    if (d)
+                        *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) =
+                            *reinterpret_cast<const float4 *>(stage + j * 36 + 4 * sub);
                 }
+                __syncwarp();
             }
         }
     }
