@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the 48 forwards one by one instead of replaying a CUDA graph")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     return ap.parse_args()
 
@@ -258,8 +260,23 @@ def main():
     if plan.sync_status() != B.DG_OK:
         raise RuntimeError("device wait timed out during warm-up")
 
-    # ---------------------------------------------------------------- timed region
+    # The library's calls only enqueue work (no allocation, no host synchronisation), so the
+    # whole canvas -- cache conversion and 48 forwards, with the profiling events around each
+    # launch -- is captured once into a CUDA graph and replayed; the kernels are the same.
     plan.set(B.DG_OPT_PROFILE, 1)
+    run_step = one_step
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+        run_step = graph.replay
+        for _ in range(max(3, args.warmup)):
+            run_step()
+        torch.cuda.synchronize()
+        if plan.sync_status() != B.DG_OK:
+            raise RuntimeError("device wait timed out during graph warm-up")
+
+    # ---------------------------------------------------------------- timed region
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -267,7 +284,7 @@ def main():
     with ClockSampler(dev.index) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
-            one_step()
+            run_step()
         ev1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -338,15 +355,15 @@ def main():
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ems / args.e2e_steps}
 
-    launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (2 + (1 if splits > 1 else 0))
+    launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * plan.get(B.DG_INFO_LAUNCHES)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16x3+tf32" if args.path == "tc" else "f32", "data": "synthetic",
+        "dtype": "bf16x3+f16" if args.path == "tc" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv,
                    "hd": w.hd, "denoise_steps": w.steps, "canvases": w.canvases,
-                   "path": args.path, "splits": splits,
+                   "path": args.path, "splits": splits, "cuda_graph": not args.no_graph,
                    "l2": "inputs larger than L2 (fresh canvas per step, 8 MiB x 48 + 64 MiB cache)"},
         "us_per_denoise_step": ms_per_step * 1e3 / n_fwd,
         "canvas_steps_per_s": n_fwd * args.steps * world / (ms / 1e3),

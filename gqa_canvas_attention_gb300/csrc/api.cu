@@ -15,6 +15,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -86,8 +87,12 @@ struct dg_attn_plan {
     int inject_stall;
     int device, num_sms;
     bool tc_ok;
+    // clusters of s CTAs (s = 2..8) the tensor-core kernel can hold at once (0: not launchable)
+    int max_clusters[dg::kMaxClusterSplits + 1];
     // scratch
     float2 *inv_freq;
+    float *rope_cs;              // [T, 2*hd] cos|sin of the positions pos0 .. pos0 + T - 1
+    bool rope_dirty;             // rope_cs does not hold the current pos0 yet
     uint32_t *status;
     float *q32, *k32, *v32;
     __nv_bfloat16 *qh, *ql, *kh, *kl;
@@ -121,7 +126,7 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 
 void free_scratch(dg_attn_plan *p)
 {
-    void *ptrs[] = {p->inv_freq, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
+    void *ptrs[] = {p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
                     p->kh, p->kl, p->vh, p->part_o, p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
@@ -150,6 +155,14 @@ int qtiles_for(const dg_attn_plan *p)
 // cost of a CTA) + the combine kernel's cost, all in units of one key tile's time.  The
 // tensor-core figures were measured on the GB300 at hd = 256: ~0.9 us per 32-key tile and
 // ~8 us of start-up plus epilogue per CTA; the combine reads the partitions' rows once.
+// The tensor-core path merges 2..8 partitions inside the kernel (one cluster per query tile)
+// when such clusters fit on the GPU; other partition counts go through the combine kernel.
+bool cluster_combine(const dg_attn_plan *p, int splits)
+{
+    return p->path == DG_PATH_TC && splits >= 2 && splits <= dg::kMaxClusterSplits &&
+           p->max_clusters[splits] > 0;
+}
+
 int auto_splits(const dg_attn_plan *p)
 {
     const int nt = n_tiles_for(p);
@@ -166,9 +179,14 @@ int auto_splits(const dg_attn_plan *p)
         const int tps = (nt + s - 1) / s;
         const int s_eff = (nt + tps - 1) / tps;
         if (s_eff != s) continue;
-        const int waves = (qt * s + slots - 1) / slots;
+        const bool cl = cluster_combine(p, s);
+        // co-resident CTAs: whole clusters only (they are placed within one GPC each)
+        const int slots_s = cl ? std::min(slots, p->max_clusters[s] * s) : slots;
+        const int waves = (qt * s + slots_s - 1) / slots_s;
         double cost = waves * (tps + startup);
-        if (s > 1) {
+        if (s > 1 && cl) {
+            cost += 1.5 / tile_us;                     // in-kernel merge through shared memory
+        } else if (s > 1) {
             const double bytes = rows * p->hd * 4.0 * (s + 1);
             cost += (3.0 + bytes / 3.0e6) / tile_us;   // launch + traffic at ~3 TB/s (bytes/us)
         }
@@ -223,7 +241,14 @@ int record_event(dg_attn_plan *p, int stage, cudaStream_t s)
             v.push_back(e);
         }
     }
-    cudaError_t err = cudaEventRecord(v[used++], s);
+    // Inside a stream capture a plain record only orders the graph's nodes; the external flag
+    // makes each replay of the graph record the event, so the timings stay readable.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cap);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaStreamIsCapturing");
+    err = cap == cudaStreamCaptureStatusActive
+              ? cudaEventRecordWithFlags(v[used++], s, cudaEventRecordExternal)
+              : cudaEventRecord(v[used++], s);
     return err == cudaSuccess ? DG_OK : cuda_fail(err, "cudaEventRecord");
 }
 
@@ -277,6 +302,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.S = p->S; a.G = p->G;
         a.rows = p->rows; a.rows_pad = p->rows_pad;
         a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
+        a.cluster_combine = cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
         err = dg::launch_attn_tc(a, p->maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
@@ -293,7 +319,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
     }
     rc = record_event(p, DG_STAGE_ATTENTION, s);
     if (rc) return rc;
-    if (splits > 1) {
+    if (splits > 1 && !cluster_combine(p, splits)) {
         dg::CombineParams c{};
         c.part_o = p->part_o; c.part_ml = p->part_ml; c.out = out;
         c.T = p->T; c.nh = p->nh; c.nkv = p->nkv; c.G = p->G; c.rows = p->rows;
@@ -347,6 +373,20 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
         if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
         if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
     }
+    return DG_OK;
+}
+
+// Without a caller's table the first stage reads the plan's cos|sin table, rebuilt on the stream
+// (ahead of the work that reads it) after a change of position.
+int rope_table(dg_attn_plan *p, const float *&cos_sin, cudaStream_t s)
+{
+    if (cos_sin) return DG_OK;
+    if (p->rope_dirty) {
+        cudaError_t err = dg::launch_rope_table(p->rope_cs, p->inv_freq, p->T, p->hd, p->pos0, s);
+        if (err != cudaSuccess) return cuda_fail(err, "cos/sin table launch");
+        p->rope_dirty = false;
+    }
+    cos_sin = p->rope_cs;
     return DG_OK;
 }
 
@@ -416,6 +456,8 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
     const size_t nqt = (size_t)nkv * p->rows_pad * hd, nkt = (size_t)nkv * p->S * hd;
     p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
+    p->rope_cs = (float *)dalloc(p, sizeof(float) * 2 * (size_t)T * hd, err);
+    p->rope_dirty = true;
     p->status = (uint32_t *)dalloc(p, sizeof(uint32_t) * 4, err);
     p->q32 = (float *)dalloc(p, nq * sizeof(float), err);
     p->k32 = (float *)dalloc(p, nk * sizeof(float), err);
@@ -441,6 +483,10 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     }
     err = cudaMemcpy(p->inv_freq, f.data(), sizeof(float2) * f.size(), cudaMemcpyHostToDevice);
     if (err == cudaSuccess && p->tc_ok) err = dg::attn_tc_prepare(hd);
+    for (int sp = 0; sp <= dg::kMaxClusterSplits; ++sp)
+        p->max_clusters[sp] = (err == cudaSuccess && p->tc_ok)
+                                  ? dg::attn_tc_max_clusters(hd, sp, p->rows_pad / dg::kTileM, nkv)
+                                  : 0;
     int rc = (err == cudaSuccess) ? DG_OK : cuda_fail(err, "plan set-up");
     if (rc == DG_OK && p->tc_ok) rc = build_maps(p);
     if (rc == DG_OK) {
@@ -492,6 +538,7 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
             set_error("pos0 out of range");
             return DG_ERR_ARG;
         }
+        if (p->pos0 != value) p->rope_dirty = true;
         p->pos0 = value;
         return DG_OK;
     case DG_OPT_SPLITS: {
@@ -550,7 +597,7 @@ int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
     case DG_INFO_CACHE_READY: *value = p->cache_ready ? 1 : 0; return DG_OK;
     case DG_INFO_LAUNCHES:
         split_layout(p, s, tps, nt);
-        *value = 2 + (s > 1 ? 1 : 0);
+        *value = 2 + (s > 1 && !cluster_combine(p, s) ? 1 : 0) + (p->rope_dirty ? 1 : 0);
         return DG_OK;
     default:
         set_error("unknown option %d", key);
@@ -617,6 +664,7 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
                                    nullptr, nullptr))
         return rc;
     if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+    if (int rc = rope_table(p, cos_sin, s)) return rc;
     dg::NormRopeParams n = norm_params(p);
     n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
     const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
@@ -641,6 +689,7 @@ int dg_attn_norm_rope(dg_attn_plan *p, const float *q, const float *k_canvas,
         set_error("k_hat and v_hat are required");
         return DG_ERR_ARG;
     }
+    if (int rc = rope_table(p, cos_sin, s)) return rc;
     dg::NormRopeParams n = norm_params(p);
     n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
     n.q_out = q_hat; n.k_out = k_hat; n.v_out = v_hat;

@@ -9,8 +9,10 @@
 // Precision (scores reach |s| ~ 90 because of scaling 1.0, so one TF32 rounding of q or k moves
 // outputs by ~1e-2): Q.K^T is computed as  qh.kh + qh.kl + ql.kh  with bf16 hi/lo splits of both
 // operands (three kind::f16 MMAs, ~16 significant bits per operand).  P.V runs with P and V
-// rounded to fp16: the same 10 explicit mantissa bits as TF32 with round to nearest, P <= 256 and
+// rounded to fp16: the same 10 explicit mantissa bits as TF32 with round to nearest, P <= 2^15 and
 // the normed V well inside the fp16 range, at twice the TF32 rate and half the bytes of V.
+// K and V tiles are read by every query tile of their kv group, and the cache part by every
+// forward of a denoising loop: their loads carry an L2 evict-last policy.
 //
 // Roles (32 * (7 + NQI) threads):
 //   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
@@ -26,7 +28,7 @@
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to fp16, packed two per column
 //            over the start of S, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
-//            has grown by more than 2^8 (so P <= 256 in between), and write the output.
+//            has grown by more than 2^15 (so P <= 2^15 in between), and write the output.
 // TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit and the CTA unwinds.
 #include "dg_internal.cuh"
@@ -67,13 +69,23 @@ template <int HD> struct Layout {
     static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 3 + (C::NQI + 1);
     static constexpr int THREADS = 32 * (7 + C::NQI);
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + TMEM slot + alignment
+    // In-cluster combine, once every MMA has completed (operand rings free): O of the tile
+    // (row pitch HD + 4 floats: a float4 store per lane is conflict-free), the (m, l) of each
+    // row, the merge weights and output row pointers of the rows this CTA writes.
+    static constexpr int STG_PITCH = HD + 4;
+    static constexpr int ML_OFF = kTileM * STG_PITCH * 4;
+    static constexpr int WGT_OFF = ML_OFF + kTileM * 8;
+    static constexpr int DST_OFF = WGT_OFF + kTileM * kMaxClusterSplits * 4;
+    static constexpr int CMB_END = DST_OFF + kTileM * 8;
+    static_assert(CMB_END <= BAR_OFF, "combine staging fits below the barriers");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(C::SP_COL + C::NSP * C::NK <= 512, "TMEM budget");
     static_assert(C::NSP % C::NQI == 0 && C::KST % C::NQI == 0, "issuer-owned buffers and slots");
 };
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 2^8 between rescales
+// log2 units: P stays <= 2^15 between rescales, inside the fp16 range (65504), and a rescale of O
+// (which every row of a warp takes when any one row needs it) is rare
+constexpr float kRescaleThreshold = 15.0f;
 
 template <int HD>
 __global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
@@ -137,6 +149,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     if (warp == 0) {
         // ---------------------------------------------------------------- K producer
         if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             int issued[KST] = {};
             if (!C::QL_TMEM) {
@@ -156,9 +169,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 const int key0 = (tile0 + it) * NK;
                 mbar_arrive_expect_tx(&k_full[s], Lay::KSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::KPANELS; ++pn) {
-                    tma_load_3d(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64, key0, g);
-                    tma_load_3d(kst + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES, &maps.kl, &k_full[s],
-                                pn * 64, key0, g);
+                    tma_load_3d_hint(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64,
+                                     key0, g, pol);
+                    tma_load_3d_hint(kst + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES, &maps.kl,
+                                     &k_full[s], pn * 64, key0, g, pol);
                 }
                 ++issued[s];
             }
@@ -172,6 +186,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     } else if (warp == 2) {
         // ---------------------------------------------------------------- V producer
         if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             int issued[VST] = {};
             for (int it = 0; it < n_local; ++it) {
@@ -184,7 +199,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 const int key0 = (tile0 + it) * NK;
                 mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::VPANELS; ++pn)
-                    tma_load_3d(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64, key0, g);
+                    tma_load_3d_hint(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64,
+                                     key0, g, pol);
                 ++issued[s];
             }
             if (!ok) atomicOr(p.status, kErrWaitProducer);
@@ -304,8 +320,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             mbar_arrive(q_ready);
         }
 
-        float m_used = -INFINITY;   // log2 units
-        float l_run = 0.f;
+        // Scores arrive in log2 units: the first stage scaled q-hat by log2(e) before its
+        // hi/lo split, so P = 2^(s - m) needs no multiply here.
+        float m_used = -INFINITY;
+        float2 l2 = make_float2(0.f, 0.f);   // running denominator, two partial sums
         for (int it = 0; it < n_local; ++it) {
             const int b = it % NSP;
             ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
@@ -316,32 +334,46 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             // a first pass and the scores are read again (register budget of 320 threads)
             constexpr int RC = NK <= 64 ? NK / 32 : 1;
             uint32_t sr[RC][32];
-            const int valid = p.S - (tile0 + it) * NK;      // keys of this tile below S
-            float mx = -INFINITY;
+            // keys of this tile below S; only the last tile of the key range is partial, so the
+            // masking branch is warp-uniform and almost never taken
+            const int valid = p.S - (tile0 + it) * NK;
+            float mx;
             if constexpr (NK <= 64) {
 #pragma unroll
                 for (int c = 0; c < RC; ++c) tmem_ld32(tsp + 32 * c, sr[c]);
                 tmem_wait_ld();
+                if (valid < NK) {
+#pragma unroll
+                    for (int c = 0; c < RC; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < RC; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(sr[c][i]) * kLog2e;
-                        if (32 * c + i >= valid) x = -INFINITY;
-                        sr[c][i] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
+                    for (int i = 0; i < 32; i += 2)
+                        m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[c][i]),
+                                                 __uint_as_float(sr[c][i + 1]));
+                mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             } else {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
                 for (int c = 0; c < NK / 32; ++c) {
                     tmem_ld32(tsp + 32 * c, sr[0]);
                     tmem_wait_ld();
+                    if (32 * c + 32 > valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float x = __uint_as_float(sr[0][i]) * kLog2e;
-                        if (32 * c + i < valid) mx = fmaxf(mx, x);
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
                     }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[0][i]),
+                                                 __uint_as_float(sr[0][i + 1]));
                 }
+                mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             }
             const bool need = mx > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
@@ -354,34 +386,41 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t orr[32];
                         tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 o = mul_f32x2(make_float2(__uint_as_float(orr[i]),
+                                                                   __uint_as_float(orr[i + 1])), a2);
+                            orr[i] = __float_as_uint(o.x);
+                            orr[i + 1] = __float_as_uint(o.y);
+                        }
                         tmem_st32(tbase + lane_off + C::O_COL + 32 * c, orr);
                     }
                     tmem_wait_st();
                 }
-                l_run *= alpha;
+                l2 = mul_f32x2(l2, make_float2(alpha, alpha));
                 m_used = m_new;
             }
             // P in fp16, two keys per 32-bit column, written over the start of the score buffer
-            // (chunk c of 32 scores lands in columns 16c..16c+15, already read)
+            // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
+            // sums the fp32 values; their fp16 roundings differ by at most 2^-11 relative each.
+            const float2 mm = make_float2(m_used, m_used);
             if constexpr (NK <= 64) {
 #pragma unroll
                 for (int c = 0; c < RC; ++c) {
                     uint32_t pw[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2_approx(__uint_as_float(sr[c][2 * i]) - m_used);
-                        const float p1 = ex2_approx(__uint_as_float(sr[c][2 * i + 1]) - m_used);
-                        const __half2 h = __floats2half2_rn(p0, p1);
-                        const float2 hf = __half22float2(h);
-                        l_run += hf.x + hf.y;
+                        const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[c][2 * i]),
+                                                               __uint_as_float(sr[c][2 * i + 1])), mm);
+                        const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+                        l2 = add_f32x2(l2, pp);
+                        const __half2 h = __floats2half2_rn(pp.x, pp.y);
                         pw[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
                     tmem_st16(tsp + 16 * c, pw);
@@ -391,16 +430,19 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 for (int c = 0; c < NK / 32; ++c) {
                     tmem_ld32(tsp + 32 * c, sr[0]);
                     tmem_wait_ld();
+                    if (32 * c + 32 > valid) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
+                    }
                     uint32_t pw[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        float x0 = __uint_as_float(sr[0][2 * i]) * kLog2e;
-                        float x1 = __uint_as_float(sr[0][2 * i + 1]) * kLog2e;
-                        if (32 * c + 2 * i >= valid) x0 = -INFINITY;
-                        if (32 * c + 2 * i + 1 >= valid) x1 = -INFINITY;
-                        const __half2 h = __floats2half2_rn(ex2_approx(x0 - m_used), ex2_approx(x1 - m_used));
-                        const float2 hf = __half22float2(h);
-                        l_run += hf.x + hf.y;
+                        const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[0][2 * i]),
+                                                               __uint_as_float(sr[0][2 * i + 1])), mm);
+                        const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+                        l2 = add_f32x2(l2, pp);
+                        const __half2 h = __floats2half2_rn(pp.x, pp.y);
                         pw[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
                     tmem_st16(tsp + 16 * c, pw);
@@ -410,6 +452,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             tc_fence_before();
             if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
         }
+        const float l_run = l2.x + l2.y;
         if (ok && !mbar_wait_bounded(o_final, 0, limit)) ok = false;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -420,6 +463,22 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             // columns of O in a shared-memory tile (row pitch 36 floats, conflict-free for float4)
             // and writes it back row-contiguous: a store instruction covers 128 bytes of each of
             // 4 output rows.  Each lane computes its own row's destination once.
+            if (p.cluster_combine) {
+                // unnormalised O row and its (m, l), for the merge across the cluster
+                float *stg = reinterpret_cast<float *>(smem) + r * Lay::STG_PITCH;
+                reinterpret_cast<float2 *>(smem + Lay::ML_OFF)[r] = make_float2(m_used, l_run);
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<float4 *>(stg + 32 * c + 4 * v) =
+                            make_float4(__uint_as_float(orr[4 * v]), __uint_as_float(orr[4 * v + 1]),
+                                        __uint_as_float(orr[4 * v + 2]), __uint_as_float(orr[4 * v + 3]));
+                }
+            } else {
             float *stage = reinterpret_cast<float *>(smem + Lay::K_OFF) + quarter * (32 * 36);
             float scale;
             float *mydst = nullptr;
@@ -462,7 +521,78 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 }
                 __syncwarp();
             }
+            }
         }
+    }
+
+    if (p.cluster_combine) {
+        // The splits CTAs of this query tile are one cluster.  After the barrier every CTA's
+        // staged O and (m, l) are visible cluster-wide; CTA k merges rows [k*128/P, (k+1)*128/P):
+        //   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
+        // reading the P partial rows through distributed shared memory, in partition order.
+        __syncwarp();
+        cluster_sync_all();
+        const int P = p.splits;
+        const int rank = (int)cluster_ctarank();
+        const int r0 = rank * kTileM / P, r1 = (rank + 1) * kTileM / P, nr = r1 - r0;
+        float *wgt = reinterpret_cast<float *>(smem + Lay::WGT_OFF);
+        float **dst = reinterpret_cast<float **>(smem + Lay::DST_OFF);
+        const uint32_t ml_base = smem_u32(smem + Lay::ML_OFF);
+        if ((int)threadIdx.x < nr) {
+            const int i = threadIdx.x, r = r0 + i;
+            float m[kMaxClusterSplits], l[kMaxClusterSplits];
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) {
+                if (q < P) {
+                    const float2 v = dsmem_ld_f2(dsmem_map(ml_base + r * 8, q));
+                    m[q] = v.x;
+                    l[q] = v.y;
+                    M = fmaxf(M, v.x);
+                }
+            }
+            float L = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) {
+                if (q < P) {
+                    m[q] = exp2f(m[q] - M);
+                    L += l[q] * m[q];
+                }
+            }
+            const float inv = 1.0f / L;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q)
+                if (q < P) wgt[i * kMaxClusterSplits + q] = m[q] * inv;
+            const int Rg = qt * kTileM + r;
+            dst[i] = Rg < p.rows ? p.out + ((size_t)(Rg / p.G) * p.nh + g * p.G + Rg % p.G) * HD
+                                 : nullptr;
+        }
+        __syncthreads();
+        uint32_t peer[kMaxClusterSplits];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterSplits; ++q) peer[q] = q < P ? dsmem_map(smem_u32(smem), q) : 0u;
+        constexpr int V4 = HD / 4;
+        for (int item = threadIdx.x; item < nr * V4; item += Lay::THREADS) {
+            const int i = item / V4, c4 = item % V4;
+            float *d = dst[i];
+            if (!d) continue;
+            const uint32_t off = (uint32_t)(((r0 + i) * Lay::STG_PITCH + 4 * c4) * 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) {
+                if (q < P) {
+                    const float4 v = dsmem_ld_f4(peer[q] + off);
+                    const float w = wgt[i * kMaxClusterSplits + q];
+                    acc.x = fmaf(w, v.x, acc.x);
+                    acc.y = fmaf(w, v.y, acc.y);
+                    acc.z = fmaf(w, v.z, acc.z);
+                    acc.w = fmaf(w, v.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(d + 4 * c4) = acc;
+        }
+        // no CTA leaves (or frees its shared memory) while a peer may still read it
+        cluster_sync_all();
     }
 
     tc_fence_before();
@@ -476,9 +606,41 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
 template <int HD>
 cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
 {
-    dim3 grid((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
-    attn_tc_kernel<HD><<<grid, Layout<HD>::THREADS, Layout<HD>::SMEM_BYTES, s>>>(maps, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
+    cfg.blockDim = dim3(Layout<HD>::THREADS);
+    cfg.dynamicSmemBytes = Layout<HD>::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = p.splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.cluster_combine ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, p);
+}
+
+template <int HD>
+int max_clusters_hd(int splits, int qtiles, int nkv)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(qtiles, nkv, splits);
+    cfg.blockDim = dim3(Layout<HD>::THREADS);
+    cfg.dynamicSmemBytes = Layout<HD>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 template <int HD>
@@ -517,6 +679,17 @@ cudaError_t attn_tc_prepare(int hd)
     case 128: return prepare_hd<128>();
     case 256: return prepare_hd<256>();
     default: return cudaErrorInvalidValue;
+    }
+}
+
+int attn_tc_max_clusters(int hd, int splits, int qtiles, int nkv)
+{
+    if (splits < 2 || splits > kMaxClusterSplits) return 0;
+    switch (hd) {
+    case 64: return max_clusters_hd<64>(splits, qtiles, nkv);
+    case 128: return max_clusters_hd<128>(splits, qtiles, nkv);
+    case 256: return max_clusters_hd<256>(splits, qtiles, nkv);
+    default: return 0;
     }
 }
 

@@ -27,13 +27,14 @@ constexpr int kFp32TileM = 32;
 // What the first-stage kernel writes.
 enum NormOut : int {
     kOutFp32 = 0,   // q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd] fp32 (input layouts)
-    kOutTc = 1,     // bf16 hi/lo planes of q_hat and k_hat, fp16 v_hat (tensor-core layouts)
+    kOutTc = 1,     // bf16 hi/lo planes of q_hat * log2(e) and k_hat, fp16 v_hat (tensor-core
+                    // layouts)
 };
 
 struct NormRopeParams {
     const float *q, *k, *v;        // [T, nh*hd], [T, nkv*hd], [T, nkv*hd]
     const float *wq, *wk;          // [hd] or null
-    const float *cos_sin;          // [T, 2*hd] or null
+    const float *cos_sin;          // [T, 2*hd] or null (then computed per lane from inv_freq)
     const float2 *inv_freq;        // [hd/2] (hi, lo) double-float of theta^(-2i/hd)
     int T, nh, nkv, ctx, S, S_pad, rows_pad;
     long long pos0;
@@ -76,6 +77,8 @@ struct AttnTcParams {
     unsigned long long wait_limit_ns;
     int T, nh, nkv, S, G, rows, rows_pad;
     int splits, tiles_per_split, n_tiles;
+    int cluster_combine;           // 1: the splits CTAs of a query tile form a cluster and merge
+                                   // their partial results through distributed shared memory
     int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
 };
 
@@ -103,11 +106,17 @@ TcGeom tc_geometry(int hd);
 
 // Host launchers (return cudaGetLastError()).
 cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);
+// cos|sin table [T, 2*hd] of the positions pos0 .. pos0 + T - 1 (layout of a caller's table).
+cudaError_t launch_rope_table(float *cs, const float2 *inv_freq, int T, int hd, long long pos0,
+                              cudaStream_t s);
 cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s);
 cudaError_t launch_attn_fp32(const AttnFp32Params &p, int hd, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnTcParams &p, const TcMaps &maps, int hd, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t attn_tc_prepare(int hd);   // one-time function attributes (smem opt-in)
+// Clusters of `splits` CTAs the GPU can hold at once (0: that cluster launch cannot run).
+int attn_tc_max_clusters(int hd, int splits, int qtiles, int nkv);
+constexpr int kMaxClusterSplits = 8;   // portable cluster size
 size_t attn_tc_smem_bytes(int hd);
 
 }  // namespace dg

@@ -3,8 +3,11 @@
 // canvas_forward): per (token, head) RMSNorm with optional weight, NeoX rotate-half RoPE on q
 // and k, the weightless un-roped norm on v.
 //
-// One CTA per canvas token; its warps take the token's nh + 2*nkv heads, one warp per head.
-// The token's cos/sin row is computed once per CTA into shared memory: the angle
+// One warp per (canvas token, chunk of up to 1024/hd of its nh + 2*nkv heads): the warp requests
+// every row of its chunk, its norm weights and its cos/sin row before any arithmetic, then
+// normalises, rotates and stores the rows one by one.  The cos/sin rows come from a table (the
+// caller's, or the plan's, built once per set of positions by rope_table_kernel); without one each
+// lane computes those of its own elements.  Either way the angle
 // (pos0 + t) * theta^(-2i/hd) is formed in double-float (the frequency arrives as an fp64 value
 // split into two floats, the product is made exact with an FMA), reduced modulo 2*pi with a
 // Cody-Waite split of 2*pi (Cody & Waite, "Software Manual for the Elementary Functions", 1980)
@@ -15,8 +18,8 @@
 // shuffle reduction and the rotate-half partner of element i (i +- hd/2) is either in the same
 // lane or in lane ^ 16.
 //
-// For the tensor-core layouts q-hat and k-hat are written as bf16 hi/lo pairs and v-hat as fp16,
-// next to the cache rows of the same kv head.
+// For the tensor-core layouts q-hat (times log2 e) and k-hat are written as bf16 hi/lo pairs and
+// v-hat as fp16, next to the cache rows of the same kv head.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -114,117 +117,126 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
+// Rows (heads) of one token that one warp takes: 32 elements per lane in registers.
+template <int HD> constexpr int kChunkRows = 1024 / HD;
+
 template <int HD, int MODE>
-__global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
+__global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int chunks)
 {
     using L = Lane<HD>;
     constexpr int EPL = L::EPL;
     constexpr int HALF = HD / 2;
-    __shared__ float s_cos[HD];
-    __shared__ float s_sin[HD];
-    const int t = blockIdx.x;
+    constexpr int CH = kChunkRows<HD>;
+    // distinct frequencies per lane: with hd = 256 slots e and e + 4 share one
+    constexpr int NU = HD == 256 ? 4 : EPL;
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int G = p.nh / p.nkv;
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int t = gw / chunks;
+    if (t >= p.T) return;
     const int jobs = p.nh + 2 * p.nkv;
-    auto job_src = [&](int job, int &kind, int &head) -> const float * {
-        if (job < p.nh) { kind = 0; head = job; return p.q + ((size_t)t * p.nh + head) * HD; }
-        if (job < p.nh + p.nkv) {
-            kind = 1; head = job - p.nh;
-            return p.k + ((size_t)t * p.nkv + head) * HD;
-        }
-        kind = 2; head = job - p.nh - p.nkv;
-        return p.v + ((size_t)t * p.nkv + head) * HD;
+    const int j0 = (gw % chunks) * CH;
+    const int nj = min(CH, jobs - j0);
+    const int G = p.nh / p.nkv;
+    auto src_row = [&](int job) -> const float * {
+        if (job < p.nh) return p.q + ((size_t)t * p.nh + job) * HD;
+        if (job < p.nh + p.nkv) return p.k + ((size_t)t * p.nkv + (job - p.nh)) * HD;
+        return p.v + ((size_t)t * p.nkv + (job - p.nh - p.nkv)) * HD;
     };
-    // the first job's row is loaded before the cos/sin work so that its latency overlaps it
-    float xpre[EPL];
-    if (warp < jobs) {
-        int kd, hh;
-        L::load(job_src(warp, kd, hh), lane, xpre);
-    }
-    if (p.do_rope) {
+
+    // every row of the chunk is requested before any arithmetic
+    float x[CH][EPL];
+#pragma unroll
+    for (int r = 0; r < CH; ++r)
+        if (r < nj) L::load(src_row(j0 + r), lane, x[r]);
+
+    // the norm weights of the kinds present in the chunk (vector loads, once per warp)
+    float wq[EPL], wk[EPL];
+    const bool has_q = j0 < p.nh, has_k = j0 < p.nh + p.nkv && j0 + nj > p.nh;
+    if (p.do_norm && p.wq && has_q) L::load(p.wq, lane, wq);
+    if (p.do_norm && p.wk && has_k) L::load(p.wk, lane, wk);
+
+    // cos and sin of this lane's elements at position pos0 + t; the sine carries the sign of the
+    // rotate-half partner (-x[i + hd/2] in the first half), so the rotation is two FMAs
+    float cs[EPL], sn[EPL];
+    if (p.do_rope && (has_q || has_k)) {
         if (p.cos_sin) {
             const float *row = p.cos_sin + (size_t)t * 2 * HD;
-            for (int i = threadIdx.x; i < HD; i += blockDim.x) {
-                s_cos[i] = row[i];
-                s_sin[i] = row[HD + i];
-            }
+            L::load(row, lane, cs);
+            L::load(row + HD, lane, sn);
         } else {
             const float pf = (float)(p.pos0 + t);
-            for (int k = threadIdx.x; k < HALF; k += blockDim.x) {
-                float c, s;
-                rope_angle_cos_sin(pf, p.inv_freq[k], c, s);
-                s_cos[k] = c; s_cos[k + HALF] = c;
-                s_sin[k] = s; s_sin[k + HALF] = s;
+#pragma unroll
+            for (int e = 0; e < NU; ++e)
+                rope_angle_cos_sin(pf, p.inv_freq[L::idx(lane, e) % HALF], cs[e], sn[e]);
+#pragma unroll
+            for (int e = NU; e < EPL; ++e) {
+                cs[e] = cs[e - NU];
+                sn[e] = sn[e - NU];
             }
         }
-    }
-    __syncthreads();
-
-    for (int job = warp; job < jobs; job += nwarps) {
-        int kind, head;
-        const float *src = job_src(job, kind, head);
-        const float *w = kind == 0 ? p.wq : kind == 1 ? p.wk : nullptr;
-        float x[EPL];
-        if (job == warp) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) x[e] = xpre[e];
-        } else {
-            L::load(src, lane, x);
-        }
+        for (int e = 0; e < EPL; ++e)
+            if (L::first_half(lane, e)) sn[e] = -sn[e];
+    }
+
+#pragma unroll
+    for (int r = 0; r < CH; ++r) {
+        if (r >= nj) break;
+        const int job = j0 + r;
+        const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
+        const int head = kind == 0 ? job : kind == 1 ? job - p.nh : job - p.nh - p.nkv;
+        float *xr = x[r];
         if (p.do_norm) {
             float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
+            for (int e = 0; e < EPL; ++e) ss = fmaf(xr[e], xr[e], ss);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
+            const float rn = rsqrtf(ss * (1.0f / (float)HD) + p.eps);
+            const float *w = (kind == 0 && p.wq) ? wq : (kind == 1 && p.wk) ? wk : nullptr;
+            if (w) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                float y = x[e] * r;
-                if (w) y *= w[L::idx(lane, e)];
-                x[e] = y;
+                for (int e = 0; e < EPL; ++e) xr[e] = (xr[e] * rn) * w[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) xr[e] *= rn;
             }
         }
         if (p.do_rope && kind != 2) {
             float part[EPL];
             if constexpr (HD <= 128) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[e] = __shfl_xor_sync(0xffffffffu, x[e], 16);
+                for (int e = 0; e < EPL; ++e) part[e] = __shfl_xor_sync(0xffffffffu, xr[e], 16);
             } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[e] = x[e ^ 4];
-            }
-            float z[EPL];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                const int i = L::idx(lane, e);
-                const float rot = L::first_half(lane, e) ? -part[e] : part[e];
-                z[e] = fmaf(x[e], s_cos[i], rot * s_sin[i]);
+                for (int e = 0; e < EPL; ++e) part[e] = xr[e ^ 4];
             }
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) x[e] = z[e];
+            for (int e = 0; e < EPL; ++e) xr[e] = fmaf(xr[e], cs[e], part[e] * sn[e]);
         }
         if constexpr (MODE == kOutFp32) {
             float *dst = kind == 0 ? p.q_out + ((size_t)t * p.nh + head) * HD
                        : kind == 1 ? p.k_out + ((size_t)t * p.nkv + head) * HD
                                    : p.v_out + ((size_t)t * p.nkv + head) * HD;
-            L::store(dst, lane, x);
+            L::store(dst, lane, x[r]);
         } else {
             if (kind == 2) {
                 __half v[EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) v[e] = __float2half_rn(x[e]);
+                for (int e = 0; e < EPL; ++e) v[e] = __float2half_rn(xr[e]);
                 if constexpr (HD >= 64)
                     L::template store_16<__half, __half2>(p.vh + ((size_t)head * p.S + p.ctx + t) * HD,
                                                           lane, v);
             } else {
+                // q-hat is scaled by log2(e) (one fp32 rounding) so that the tensor-core kernel
+                // gets its scores in the log2 units of its exponentials
+                const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;
                 __nv_bfloat16 hi[EPL], lo[EPL];
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
-                    hi[e] = __float2bfloat16_rn(x[e]);
-                    lo[e] = __float2bfloat16_rn(x[e] - __bfloat162float(hi[e]));
+                    const float y = xr[e] * sc;
+                    hi[e] = __float2bfloat16_rn(y);
+                    lo[e] = __float2bfloat16_rn(y - __bfloat162float(hi[e]));
                 }
                 size_t off;
                 __nv_bfloat16 *dh, *dl;
@@ -245,18 +257,35 @@ __global__ void __launch_bounds__(512) norm_rope_kernel(NormRopeParams p)
     }
 }
 
+// The cos|sin table of the canvas positions pos0 .. pos0 + T - 1: row t = cos(hd) | sin(hd), both
+// halves of each equal, one thread per (t, frequency).
+__global__ void rope_table_kernel(float *cs, const float2 *inv_freq, int T, int hd, long long pos0)
+{
+    const int half = hd / 2;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)T * half) return;
+    const int t = (int)(i / half), k = (int)(i % half);
+    float c, s;
+    rope_angle_cos_sin((float)(pos0 + t), inv_freq[k], c, s);
+    float *row = cs + (size_t)t * 2 * hd;
+    row[k] = c;
+    row[k + half] = c;
+    row[hd + k] = s;
+    row[hd + k + half] = s;
+}
+
 template <int HD>
 cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
 {
+    const int jobs = p.nh + 2 * p.nkv;
+    const int chunks = (jobs + kChunkRows<HD> - 1) / kChunkRows<HD>;
+    const long long warps = (long long)p.T * chunks;
+    const int blocks = (int)((warps + 3) / 4);
     if (mode == kOutFp32) {
-        const int jobs = p.nh + 2 * p.nkv;
-        const int warps = jobs < 16 ? jobs : 16;
-        norm_rope_kernel<HD, kOutFp32><<<p.T, 32 * warps, 0, s>>>(p);
+        norm_rope_kernel<HD, kOutFp32><<<blocks, 128, 0, s>>>(p, chunks);
     } else {
         if constexpr (HD >= 64) {
-            const int jobs = p.nh + 2 * p.nkv;
-            const int warps = jobs < 16 ? jobs : 16;
-            norm_rope_kernel<HD, kOutTc><<<p.T, 32 * warps, 0, s>>>(p);
+            norm_rope_kernel<HD, kOutTc><<<blocks, 128, 0, s>>>(p, chunks);
         } else {
             return cudaErrorInvalidValue;
         }
@@ -265,6 +294,14 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
 }
 
 }  // namespace
+
+cudaError_t launch_rope_table(float *cs, const float2 *inv_freq, int T, int hd, long long pos0,
+                              cudaStream_t s)
+{
+    const long long n = (long long)T * (hd / 2);
+    rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cs, inv_freq, T, hd, pos0);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s)
 {

@@ -16,7 +16,9 @@
  *   q         [T, nh*hd]           k_canvas, v_canvas [T, nkv*hd] (raw, before the norms)
  *   k_cache   [nkv, ctx, hd]       v_cache [nkv, ctx, hd] (used as given: already normed/roped)
  *   q_norm_w  [hd] or NULL         k_norm_w [hd] or NULL (NULL = unweighted)
- *   cos_sin   [T, 2*hd] or NULL    row t = cos(hd) | sin(hd); NULL = computed on the device
+ *   cos_sin   [T, 2*hd] or NULL    row t = cos(hd) | sin(hd); NULL = the plan's own table of the
+ *                                  positions pos0 + t, built on the device by the first call after
+ *                                  plan creation or a change of DG_OPT_POS0 (one extra kernel)
  *   out       [T, nh*hd]
  *
  * Ownership: the caller owns every buffer passed in; inputs are only read.  A plan owns its
@@ -61,7 +63,8 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_OPT_POS0          2  /* position of canvas row 0 (default ctx, the cache length) */
 #define DG_OPT_SPLITS        3  /* key-range partitions per query tile (0..64); 0 = chosen per plan */
 #define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000) */
-#define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage */
+#define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage (inside a
+                                   stream capture as external records, taken on every replay) */
 #define DG_OPT_INJECT_STALL  6  /* test hook: 1 = the tensor-core kernel's softmax withholds its
                                    first "P ready" signal, so the bounded waits behind it run out
                                    and the forward ends with DG_ERR_TIMEOUT (no fault, no hang) */
@@ -69,7 +72,8 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_INFO_SPLITS_USED  16 /* partitions the next forward will use */
 #define DG_INFO_SCRATCH_BYTES 17 /* device bytes the plan holds */
 #define DG_INFO_CACHE_READY  18 /* 1 when dg_attn_cache_prepare has filled the plan's cache copy */
-#define DG_INFO_LAUNCHES     19 /* kernels one dg_attn_forward enqueues with the current options */
+#define DG_INFO_LAUNCHES     19 /* kernels the next dg_attn_forward enqueues with the current options
+                                   (without a caller's cos_sin table) */
 
 /* Create a plan for one geometry on the current device.  Requires nh % nkv == 0, nh, nkv, T >= 1,
  * ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in {64, 128, 256}),

@@ -168,15 +168,26 @@ def test_shapes(shape, path):
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], str(shape))
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+# (requested partitions, cache length, partitions the tensor-core path uses): with hd = 128 a key
+# tile is 64 keys, so ctx = 700 / 2000 / 2250 (+ T = 40) give 12 / 32 / 36 tiles.  2..8
+# partitions merge inside the kernel (thread-block clusters); 9 and 12 use the combine kernel.
+SPLIT_CASES = [(1, 700, 1), (2, 700, 2), (3, 2000, 3), (7, 2000, 7), (8, 2000, 8), (9, 2250, 9),
+               (64, 700, 12)]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "splits%d_ctx%d" % c[:2])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
-def test_forced_partitions(splits, path):
-    T, ctx, nh, nkv, hd = 40, 700, 4, 2, 128
+def test_forced_partitions(case, path):
+    splits, ctx, used = case
+    T, nh, nkv, hd = 40, 4, 2, 128
     d = make_inputs(T, ctx, nh, nkv, hd, seed=11, weighted=False)
     dd = to_dev(d)
     plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
     plan.set(B.DG_OPT_PATH, path).set(B.DG_OPT_SPLITS, splits)
-    assert plan.get(B.DG_INFO_SPLITS_USED) >= 1
+    if path == B.DG_PATH_TC:
+        assert plan.get(B.DG_INFO_SPLITS_USED) == used
+        run_forward(plan, dd)           # the cos/sin table is built by the first forward
+        assert plan.get(B.DG_INFO_LAUNCHES) == (3 if used > 8 else 2)
     out = run_forward(plan, dd)
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], f"splits={splits}")
 
@@ -287,3 +298,39 @@ def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable():
     plan.set(B.DG_OPT_INJECT_STALL, 0)
     out = run_forward(plan, dd)
     check(out, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, [(0, T)], "after-timeout")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_forward_replays_from_a_cuda_graph(path):
+    """Every call only enqueues work, so a captured cache conversion + forwards replays to the
+    same result as the eager calls, and the profiling events recorded during capture are taken
+    again on each replay."""
+    T, ctx, nh, nkv, hd = 70, 700, 8, 2, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=41)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path).set(B.DG_OPT_SPLITS, 3)
+    eager = run_forward(plan, dd).clone()
+    out = torch.empty_like(eager)
+    plan.set(B.DG_OPT_PROFILE, 1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # the library runs once outside capture on this stream
+        plan.cache_prepare(dd["k_cache"], dd["v_cache"])
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.cache_prepare(dd["k_cache"], dd["v_cache"])
+        for _ in range(2):
+            plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                         dd["k_norm_w"], out=out)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert plan.sync_status() == B.DG_OK
+    assert torch.equal(out, eager)
+    ms, n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_ATTENTION)
+    assert n == 2 and ms > 0.0
+    check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], "graph")
