@@ -112,6 +112,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     uint64_t *drain = q_ready + 1;          // [NQI + 1]: one per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + NQI + 1);
 
+    // the next kernel of the stream may be scheduled now; it waits for this one to finish
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int qt = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
@@ -145,6 +147,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // the operands are written by the kernel before this one in the stream
+    pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------------------- K producer
@@ -611,13 +615,14 @@ cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
     cfg.blockDim = dim3(Layout<HD>::THREADS);
     cfg.dynamicSmemBytes = Layout<HD>::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = p.splits;
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = p.splits;
     cfg.attrs = attr;
-    cfg.numAttrs = p.cluster_combine ? 1 : 0;
+    cfg.numAttrs = p.cluster_combine ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, p);
 }
 

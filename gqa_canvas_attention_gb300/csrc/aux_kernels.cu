@@ -54,6 +54,8 @@ constexpr int kCombineBatch = 8;      // partitions whose loads are issued toget
 template <int HD>
 __global__ void __launch_bounds__(32 * kCombineRowsPerCta) combine_kernel(CombineParams p)
 {
+    pdl_launch_dependents();
+    pdl_wait();   // the partial results come from the attention kernel just before
     constexpr int V4 = HD / 128 > 0 ? HD / 128 : 1;   // float4 per lane (hd 256: 2, 128: 1)
     constexpr bool PART = HD < 128;                   // hd 64 / 32: lanes beyond hd/4 idle
     const int lane = threadIdx.x & 31;
@@ -126,16 +128,20 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
     if (p.splits > kMaxCombineSplits) return cudaErrorInvalidValue;
-    dim3 grid((p.rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta, p.nkv);
-    const int threads = 32 * kCombineRowsPerCta;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta, p.nkv);
+    cfg.blockDim = dim3(32 * kCombineRowsPerCta);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     switch (p.hd) {
-    case 32: combine_kernel<32><<<grid, threads, 0, s>>>(p); break;
-    case 64: combine_kernel<64><<<grid, threads, 0, s>>>(p); break;
-    case 128: combine_kernel<128><<<grid, threads, 0, s>>>(p); break;
-    case 256: combine_kernel<256><<<grid, threads, 0, s>>>(p); break;
+    case 32: return cudaLaunchKernelEx(&cfg, combine_kernel<32>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+    case 256: return cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace dg

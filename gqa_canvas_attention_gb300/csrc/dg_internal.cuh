@@ -104,6 +104,17 @@ struct TcGeom {
 };
 TcGeom tc_geometry(int hd);
 
+// Launch attribute of the kernels that may start while the previous kernel of the stream is still
+// running (programmatic dependent launch): each of them calls pdl_wait() before it reads anything
+// an earlier kernel writes, so only its launch and set-up overlap.
+inline cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 // Host launchers (return cudaGetLastError()).
 cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);
 // cos|sin table [T, 2*hd] of the positions pos0 .. pos0 + T - 1 (layout of a caller's table).

@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     constexpr int CH = kChunkRows<HD>;
     // distinct frequencies per lane: with hd = 256 slots e and e + 4 share one
     constexpr int NU = HD == 256 ? 4 : EPL;
+    // the inputs may come from the kernel before this one in the stream
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int t = gw / chunks;
@@ -280,17 +283,19 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
     const int jobs = p.nh + 2 * p.nkv;
     const int chunks = (jobs + kChunkRows<HD> - 1) / kChunkRows<HD>;
     const long long warps = (long long)p.T * chunks;
-    const int blocks = (int)((warps + 3) / 4);
-    if (mode == kOutFp32) {
-        norm_rope_kernel<HD, kOutFp32><<<blocks, 128, 0, s>>>(p, chunks);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (mode == kOutFp32) return cudaLaunchKernelEx(&cfg, norm_rope_kernel<HD, kOutFp32>, p, chunks);
+    if constexpr (HD >= 64) {
+        return cudaLaunchKernelEx(&cfg, norm_rope_kernel<HD, kOutTc>, p, chunks);
     } else {
-        if constexpr (HD >= 64) {
-            norm_rope_kernel<HD, kOutTc><<<blocks, 128, 0, s>>>(p, chunks);
-        } else {
-            return cudaErrorInvalidValue;
-        }
+        return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -117,6 +117,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last()
     return pol;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Block until every grid this one depends on in the stream has completed and its memory
+// operations are visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled now (it still waits in pdl_wait for this one
+// to finish before touching what this grid writes).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 
 // Cluster-wide barrier: every thread of every CTA of the cluster arrives (release) and waits
