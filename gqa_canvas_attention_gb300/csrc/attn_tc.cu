@@ -28,7 +28,8 @@
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to fp16, packed two per column
 //            over the start of S, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
-//            has grown by more than 2^15 (so P <= 2^15 in between), and write the output.
+//            has grown by more than 15 (log2 units; so P <= 2^15 in between), and write the
+//            output.
 // TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit and the CTA unwinds.
 #include "dg_internal.cuh"
@@ -83,9 +84,13 @@ template <int HD> struct Layout {
     static_assert(C::NSP % C::NQI == 0 && C::KST % C::NQI == 0, "issuer-owned buffers and slots");
 };
 
-// log2 units: P stays <= 2^15 between rescales, inside the fp16 range (65504), and a rescale of O
-// (which every row of a warp takes when any one row needs it) is rare
+// log2 units: P stays <= 2^15 between rescales, inside the fp16 range (65504).  A rescale of O
+// (which every row of a warp takes when any one row needs it) sets the reference kHeadroom above
+// the row maximum, so the maximum may grow by 15 + 8 before the next one; the largest P of a row
+// stays >= 2^-8, a normal fp16 number with its full 11-bit precision, and the keys that fall into
+// the subnormal range (2^-6 or less of the largest) are off by at most 2^-25 each.
 constexpr float kRescaleThreshold = 15.0f;
+constexpr float kHeadroom = 8.0f;
 
 template <int HD>
 __global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
@@ -293,31 +298,29 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         const int Rg = qt * kTileM + r;                     // packed row in the group
         bool ok = true;
 
-        // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.
+        // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.  Every load of the
+        // row is issued before the first TMEM store (one memory round trip, not one per chunk).
         {
-            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh + ((size_t)g * p.rows_pad + Rg) * HD);
+            constexpr int NCH = (HD / 64) * (C::QL_TMEM ? 2 : 1);   // 32-column chunks
+            const size_t row = ((size_t)g * p.rows_pad + Rg) * HD;
+            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh + row);
+            const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql + row);
+            uint4 w[NCH][8];
 #pragma unroll
-            for (int c = 0; c < HD / 64; ++c) {
-                uint32_t w[32];
+            for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    w[c][v] = c < HD / 64 ? src_h[c * 8 + v] : src_l[(c - HD / 64) * 8 + v];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                uint32_t u[32];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
-                    const uint4 u = src_h[c * 8 + v];
-                    w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+                    u[4 * v] = w[c][v].x; u[4 * v + 1] = w[c][v].y;
+                    u[4 * v + 2] = w[c][v].z; u[4 * v + 3] = w[c][v].w;
                 }
-                tmem_st32(tbase + lane_off + C::QH_COL + 32 * c, w);
-            }
-            if constexpr (C::QL_TMEM) {
-                const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql + ((size_t)g * p.rows_pad + Rg) * HD);
-#pragma unroll
-                for (int c = 0; c < HD / 64; ++c) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 u = src_l[c * 8 + v];
-                        w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
-                    }
-                    tmem_st32(tbase + lane_off + C::QL_COL + 32 * c, w);
-                }
+                const int col = c < HD / 64 ? C::QH_COL + 32 * c : C::QL_COL + 32 * (c - HD / 64);
+                tmem_st32(tbase + lane_off + col, u);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -381,7 +384,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             }
             const bool need = mx > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
-                const float m_new = fmaxf(m_used, mx);
+                const float m_new = fmaxf(m_used, mx + kHeadroom);
                 const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
                 if (it > 0) {
                     // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
@@ -391,19 +394,30 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
                     const float2 a2 = make_float2(alpha, alpha);
+                    // two 32-column chunks per round trip to TMEM (one when the score row
+                    // already holds 64 registers)
+                    constexpr int RW = NK <= 32 ? 2 : 1;
 #pragma unroll 1
-                    for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t orr[32];
-                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                    for (int c = 0; c < HD / 32; c += RW) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                        if constexpr (RW == 2) tmem_ld32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float2 o = mul_f32x2(make_float2(__uint_as_float(orr[i]),
-                                                                   __uint_as_float(orr[i + 1])), a2);
-                            orr[i] = __float_as_uint(o.x);
-                            orr[i + 1] = __float_as_uint(o.y);
+                            const float2 x0 = mul_f32x2(
+                                make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
+                            o0[i] = __float_as_uint(x0.x);
+                            o0[i + 1] = __float_as_uint(x0.y);
+                            if constexpr (RW == 2) {
+                                const float2 x1 = mul_f32x2(
+                                    make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
+                                o1[i] = __float_as_uint(x1.x);
+                                o1[i + 1] = __float_as_uint(x1.y);
+                            }
                         }
-                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                        if constexpr (RW == 2) tmem_st32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
                     }
                     tmem_wait_st();
                 }

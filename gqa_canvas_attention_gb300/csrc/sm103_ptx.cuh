@@ -163,6 +163,13 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t caddr)
     return v;
 }
 
+__device__ __forceinline__ void dsmem_st_f4(uint32_t caddr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ float2 dsmem_ld_f2(uint32_t caddr)
 {
     float2 v;
