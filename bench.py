@@ -26,6 +26,20 @@ if ROOT not in sys.path:
 METRIC = "canvas-attention TFLOP/s and us/denoise-step, % of TF32 tensor peak"
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio of the part
 
+# DRAM bytes (read + write) per launch of the tensor-core attention kernel on the bench workload,
+# from one ncu capture (profiles/attn_tc_kernel_denoise48_ctx8k.md), valid only for the kernel
+# source it was taken on: the bench reports null once attn_tc.cu has changed.
+ATTN_TRAFFIC = {"source_sha1_prefix": "bd2c8fd9ea82", "bytes": 59.88e6}
+
+
+def attn_traffic():
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gqa_canvas_attention_gb300",
+                       "csrc", "attn_tc.cu")
+    with open(src, "rb") as f:
+        sha = hashlib.sha1(f.read()).hexdigest()
+    return ATTN_TRAFFIC["bytes"] if sha.startswith(ATTN_TRAFFIC["source_sha1_prefix"]) else None
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -387,7 +401,9 @@ def main():
         "us_per_denoise_step": ms_per_step * 1e3 / n_fwd,
         "canvas_steps_per_s": n_fwd * args.steps * world / (ms / 1e3),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf32_peak,
-                     "unit": "TFLOP/s", "frac": attn_tflops / tf32_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": attn_tflops / tf32_peak,
+                     "traffic": attn_traffic() if args.path == "tc" and w.name == "denoise48_ctx8k"
+                     else None,
                      "kernel": "attn_tc_kernel" if args.path == "tc" else "attn_fp32_kernel",
                      "peak_source": f"{src}: bf16_tflops_sustained x nominal tf32/bf16 (1.1/2.25)",
                      "avg_launch_us": attn_avg_s * 1e6, "launches": attn_n,
