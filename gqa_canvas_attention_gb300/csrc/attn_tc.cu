@@ -331,7 +331,31 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         // hi/lo split, so P = 2^(s - m) needs no multiply here.
         float m_used = -INFINITY;
         float2 l2 = make_float2(0.f, 0.f);   // running denominator, two partial sums
-        for (int it = 0; it < n_local; ++it) {
+        {
+            // Start the reference from the maximum over the first NSP score tiles (they are
+            // computed at once by the NSP issuers), not the first tile alone: the running
+            // maximum then grows less, and O is rescaled less often.  A buffer's first phase is
+            // waited for again in the loop below; that wait returns at once.
+            const int nw = min(NSP, n_local);
+            float m0 = -INFINITY;
+            for (int t = 0; t < nw; ++t) {
+                ok = mbar_wait_bounded(&s_full[t], 0, limit);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const int valid = p.S - (tile0 + t) * NK;
+#pragma unroll 1
+                for (int c = 0; c < NK / 32; ++c) {
+                    uint32_t sr[32];
+                    tmem_ld32(tbase + lane_off + C::SP_COL + t * NK + 32 * c, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
+                }
+            }
+            if (ok && nw > 0) m_used = m0 + kHeadroom;
+        }
+        for (int it = 0; ok && it < n_local; ++it) {
             const int b = it % NSP;
             ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
