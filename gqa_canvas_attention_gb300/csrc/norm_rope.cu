@@ -3,7 +3,7 @@
 // canvas_forward): per (token, head) RMSNorm with optional weight, NeoX rotate-half RoPE on q
 // and k, the weightless un-roped norm on v.
 //
-// One warp per (canvas token, chunk of up to 1024/hd of its nh + 2*nkv heads): the warp requests
+// One warp per (canvas token, chunk of up to 512/hd of its nh + 2*nkv heads): the warp requests
 // every row of its chunk, its norm weights and its cos/sin row before any arithmetic, then
 // normalises, rotates and stores the rows one by one.  The cos/sin rows come from a table (the
 // caller's, or the plan's, built once per set of positions by rope_table_kernel); without one each
@@ -117,8 +117,9 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
-// Rows (heads) of one token that one warp takes: 32 elements per lane in registers.
-template <int HD> constexpr int kChunkRows = 1024 / HD;
+// Rows (heads) of one token that one warp takes: 16 elements per lane in registers (more warps,
+// each with a shorter chain of dependent instructions, measured faster than 32 or 64).
+template <int HD> constexpr int kChunkRows = 512 / HD > 0 ? 512 / HD : 1;
 
 template <int HD, int MODE>
 __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int chunks)
@@ -226,7 +227,12 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
             if (kind == 2) {
                 __half v[EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) v[e] = __float2half_rn(xr[e]);
+                for (int e = 0; e + 1 < EPL; e += 2) {
+                    const __half2 h = __floats2half2_rn(xr[e], xr[e + 1]);
+                    v[e] = h.x;
+                    v[e + 1] = h.y;
+                }
+                if constexpr (EPL % 2) v[EPL - 1] = __float2half_rn(xr[EPL - 1]);
                 if constexpr (HD >= 64)
                     L::template store_16<__half, __half2>(p.vh + ((size_t)head * p.S + p.ctx + t) * HD,
                                                           lane, v);
@@ -234,12 +240,21 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
                 // q-hat is scaled by log2(e) (one fp32 rounding) so that the tensor-core kernel
                 // gets its scores in the log2 units of its exponentials
                 const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;
+                // hi = bf16(y), lo = bf16(y - hi), two elements per conversion
                 __nv_bfloat16 hi[EPL], lo[EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    const float y = xr[e] * sc;
-                    hi[e] = __float2bfloat16_rn(y);
-                    lo[e] = __float2bfloat16_rn(y - __bfloat162float(hi[e]));
+                for (int e = 0; e + 1 < EPL; e += 2) {
+                    const float y0 = xr[e] * sc, y1 = xr[e + 1] * sc;
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+                    const float2 hf = __bfloat1622float2(h);
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(y0 - hf.x, y1 - hf.y);
+                    hi[e] = h.x; hi[e + 1] = h.y;
+                    lo[e] = l.x; lo[e + 1] = l.y;
+                }
+                if constexpr (EPL % 2) {
+                    const float y = xr[EPL - 1] * sc;
+                    hi[EPL - 1] = __float2bfloat16_rn(y);
+                    lo[EPL - 1] = __float2bfloat16_rn(y - __bfloat162float(hi[EPL - 1]));
                 }
                 size_t off;
                 __nv_bfloat16 *dh, *dl;
