@@ -256,6 +256,8 @@ def main():
 
     plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
     plan.set(B.DG_OPT_PATH, B.DG_PATH_TC if args.path == "tc" else B.DG_PATH_FP32)
+    # the canvases are resident (or copied in ahead, ordered by events, in the end-to-end run)
+    plan.set(B.DG_OPT_INPUTS_RESIDENT, 1)
     if args.splits:
         plan.set(B.DG_OPT_SPLITS, args.splits)
     splits = plan.get(B.DG_INFO_SPLITS_USED)

@@ -85,6 +85,7 @@ struct dg_attn_plan {
     long long wait_limit_ms;
     int profile;
     int inject_stall;
+    int inputs_resident;
     int device, num_sms;
     bool tc_ok;
     // clusters of s CTAs (s = 2..8) the tensor-core kernel can hold at once (0: not launchable)
@@ -280,6 +281,7 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
     n.pos0 = p->pos0;
     n.eps = p->eps;
     n.do_norm = 1; n.do_rope = 1;
+    n.inputs_resident = p->inputs_resident;
     n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
     n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vh = p->vh;
     return n;
@@ -564,6 +566,9 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
     case DG_OPT_INJECT_STALL:
         p->inject_stall = value ? 1 : 0;
         return DG_OK;
+    case DG_OPT_INPUTS_RESIDENT:
+        p->inputs_resident = value ? 1 : 0;
+        return DG_OK;
     case DG_OPT_PROFILE:
         p->profile = value ? 1 : 0;
         for (size_t &u : p->ev_used) u = 0;
@@ -589,6 +594,7 @@ int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
     case DG_OPT_WAIT_LIMIT_MS: *value = p->wait_limit_ms; return DG_OK;
     case DG_OPT_PROFILE: *value = p->profile; return DG_OK;
     case DG_OPT_INJECT_STALL: *value = p->inject_stall; return DG_OK;
+    case DG_OPT_INPUTS_RESIDENT: *value = p->inputs_resident; return DG_OK;
     case DG_INFO_SPLITS_USED:
         split_layout(p, s, tps, nt);
         *value = s;

@@ -40,6 +40,8 @@ struct NormRopeParams {
     long long pos0;
     float eps;
     int do_norm, do_rope;          // 0/1 (the attention-only entry point passes 0, 0)
+    int inputs_resident;           // 1: q, k, v, weights and cos_sin are complete before the
+                                   // previous kernel in the stream started (DG_OPT_INPUTS_RESIDENT)
     // kOutFp32 destinations
     float *q_out, *k_out, *v_out;
     // kOutTc destinations

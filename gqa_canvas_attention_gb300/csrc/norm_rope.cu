@@ -130,9 +130,11 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     constexpr int CH = kChunkRows<HD>;
     // distinct frequencies per lane: with hd = 256 slots e and e + 4 share one
     constexpr int NU = HD == 256 ? 4 : EPL;
-    // the inputs may come from the kernel before this one in the stream
+    // The inputs may come from the kernel before this one in the stream: wait for it first,
+    // unless the caller has declared them resident (then only the stores below wait, and the
+    // loads and arithmetic overlap the end of the previous forward's attention kernel).
     pdl_launch_dependents();
-    pdl_wait();
+    if (!p.inputs_resident) pdl_wait();
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int t = gw / chunks;
@@ -188,7 +190,6 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
         if (r >= nj) break;
         const int job = j0 + r;
         const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
-        const int head = kind == 0 ? job : kind == 1 ? job - p.nh : job - p.nh - p.nkv;
         float *xr = x[r];
         if (p.do_norm) {
             float ss = 0.f;
@@ -218,6 +219,18 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
 #pragma unroll
             for (int e = 0; e < EPL; ++e) xr[e] = fmaf(xr[e], cs[e], part[e] * sn[e]);
         }
+    }
+
+    // the operand arrays are read by the previous forward's attention kernel until it ends
+    if (p.inputs_resident) pdl_wait();
+
+#pragma unroll
+    for (int r = 0; r < CH; ++r) {
+        if (r >= nj) break;
+        const int job = j0 + r;
+        const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
+        const int head = kind == 0 ? job : kind == 1 ? job - p.nh : job - p.nh - p.nkv;
+        const float *xr = x[r];
         if constexpr (MODE == kOutFp32) {
             float *dst = kind == 0 ? p.q_out + ((size_t)t * p.nh + head) * HD
                        : kind == 1 ? p.k_out + ((size_t)t * p.nkv + head) * HD

@@ -68,6 +68,13 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_OPT_INJECT_STALL  6  /* test hook: 1 = the tensor-core kernel's softmax withholds its
                                    first "P ready" signal, so the bounded waits behind it run out
                                    and the forward ends with DG_ERR_TIMEOUT (no fault, no hang) */
+#define DG_OPT_INPUTS_RESIDENT 7 /* 1 = the caller guarantees that the inputs of every call (q,
+                                   k_canvas, v_canvas, weights, cos_sin) are complete before the
+                                   work enqueued ahead of that call on the stream started, e.g.
+                                   canvases already resident in device memory: the first stage then
+                                   reads them while the previous call's attention kernel is still
+                                   running.  Default 0: the first stage waits for the preceding
+                                   kernel before reading anything */
 /* Read-only (dg_attn_get_option): */
 #define DG_INFO_SPLITS_USED  16 /* partitions the next forward will use */
 #define DG_INFO_SCRATCH_BYTES 17 /* device bytes the plan holds */

@@ -334,3 +334,29 @@ def test_forward_replays_from_a_cuda_graph(path):
     ms, n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_ATTENTION)
     assert n == 2 and ms > 0.0
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], "graph")
+
+
+def test_resident_inputs_give_the_same_bits():
+    """With DG_OPT_INPUTS_RESIDENT the first stage of each forward loads and computes while the
+    previous forward's attention kernel runs; the results must be bit-identical."""
+    T, ctx, nh, nkv, hd = 130, 1500, 8, 4, 256
+    plans, outs = [], []
+    canvases = [to_dev(make_inputs(T, ctx, nh, nkv, hd, seed=50 + i)) for i in range(4)]
+    for resident in (0, 1):
+        plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+        plan.set(B.DG_OPT_INPUTS_RESIDENT, resident)
+        assert plan.get(B.DG_OPT_INPUTS_RESIDENT) == resident
+        plan.cache_prepare(canvases[0]["k_cache"], canvases[0]["v_cache"])
+        res = [torch.empty((T, nh * hd), device="cuda") for _ in canvases]
+        for c, o in zip(canvases, res):
+            plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
+                         c["k_norm_w"], out=o)
+        assert plan.sync_status() == B.DG_OK
+        plans.append(plan)
+        outs.append(res)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=53)
+    d0 = make_inputs(T, ctx, nh, nkv, hd, seed=50)
+    d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]     # the prepared cache
+    check(outs[1][3], oracle_out(d, nh, nkv, hd, rows=(0, 8)), B.DG_PATH_TC, [(0, 8)], "resident")
