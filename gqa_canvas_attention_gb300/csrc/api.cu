@@ -284,6 +284,7 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
     n.inputs_resident = p->inputs_resident;
     n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
     n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vh = p->vh;
+    n.ql_interleaved = p->tc_ok ? dg::tc_geometry(p->hd).ql_in_tmem : 0;
     return n;
 }
 

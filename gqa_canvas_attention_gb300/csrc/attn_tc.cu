@@ -301,16 +301,19 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.  Every load of the
         // row is issued before the first TMEM store (one memory round trip, not one per chunk).
         {
+            // the operand is row-interleaved: 16-byte unit u of tile row r at (tile*HD/8 + u)*128
+            // + r, so each load instruction of a warp reads 512 contiguous bytes
             constexpr int NCH = (HD / 64) * (C::QL_TMEM ? 2 : 1);   // 32-column chunks
-            const size_t row = ((size_t)g * p.rows_pad + Rg) * HD;
-            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh + row);
-            const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql + row);
+            const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + qt) * (HD / 8) * kTileM;
+            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh) + tile + r;
+            const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql) + tile + r;
             uint4 w[NCH][8];
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
-                    w[c][v] = c < HD / 64 ? src_h[c * 8 + v] : src_l[(c - HD / 64) * 8 + v];
+                    w[c][v] = c < HD / 64 ? src_h[(c * 8 + v) * kTileM]
+                                          : src_l[((c - HD / 64) * 8 + v) * kTileM];
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
                 uint32_t u[32];

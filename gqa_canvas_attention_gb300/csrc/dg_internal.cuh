@@ -45,7 +45,10 @@ struct NormRopeParams {
     // kOutFp32 destinations
     float *q_out, *k_out, *v_out;
     // kOutTc destinations
-    __nv_bfloat16 *qh, *ql;        // [nkv, rows_pad, hd]
+    __nv_bfloat16 *qh, *ql;        // [nkv, rows_pad, hd] elements; qh row-interleaved per 128-row
+                                   // tile (unit u of row r at (tile * hd/8 + u) * 128 + r), ql too
+                                   // when ql_interleaved, else row-major (a TMA operand)
+    int ql_interleaved;
     __nv_bfloat16 *kh, *kl;        // [nkv, S, hd] (canvas rows ctx..ctx+T-1)
     __half *vh;                    // [nkv, S, hd] fp16 (canvas rows ctx..ctx+T-1)
 };
@@ -70,8 +73,8 @@ struct AttnFp32Params {
 };
 
 struct AttnTcParams {
-    const __nv_bfloat16 *qh;       // [nkv, rows_pad, hd] (q_hat hi, bf16), loaded into TMEM
-    const __nv_bfloat16 *ql;       // [nkv, rows_pad, hd] (q_hat lo), TMEM or TMA
+    const __nv_bfloat16 *qh;       // q_hat hi, bf16, row-interleaved tiles; loaded into TMEM
+    const __nv_bfloat16 *ql;       // q_hat lo: row-interleaved (into TMEM) or row-major (TMA)
     float *out;
     float *part_o;
     float2 *part_ml;

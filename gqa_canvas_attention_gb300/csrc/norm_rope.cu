@@ -96,6 +96,34 @@ struct Lane {
     }
 };
 
+// Q operand rows for the tensor-core kernel, "row-interleaved": 16-byte unit u (8 values) of row r
+// of 128-row tile T sits at unit index (T * (HD/8) + u) * 128 + r, so that 32 threads each
+// loading their own row read 512 contiguous bytes per instruction.  `tile` points at unit 0 of
+// the tile; lane `l` holds the elements Lane<HD>::idx(l, e).
+template <int HD>
+__device__ __forceinline__ void store_q_interleaved(__nv_bfloat16 *tile, int r, int l,
+                                                    const __nv_bfloat16 (&x)[HD / 32])
+{
+    constexpr int EPL = HD / 32;
+    char *base = reinterpret_cast<char *>(tile);
+    if constexpr (HD == 64) {
+        const int i = 2 * l;                                   // elements 2l, 2l+1
+        __nv_bfloat162 v; v.x = x[0]; v.y = x[1];
+        *reinterpret_cast<__nv_bfloat162 *>(base + ((size_t)(i / 8) * 128 + r) * 16 + (i % 8) * 2) = v;
+    } else {
+#pragma unroll
+        for (int g4 = 0; g4 < EPL / 4; ++g4) {                 // runs of 4 contiguous elements
+            const int i = Lane<HD>::idx(l, 4 * g4);
+            __nv_bfloat162 a, b;
+            a.x = x[4 * g4]; a.y = x[4 * g4 + 1]; b.x = x[4 * g4 + 2]; b.y = x[4 * g4 + 3];
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&a);
+            u.y = *reinterpret_cast<uint32_t *>(&b);
+            *reinterpret_cast<uint2 *>(base + ((size_t)(i / 8) * 128 + r) * 16 + (i % 8) * 2) = u;
+        }
+    }
+}
+
 // cos and sin of p * f with f = f_hi + f_lo (see the file comment for the method).
 __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c, float &s)
 {
@@ -269,19 +297,23 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
                     hi[EPL - 1] = __float2bfloat16_rn(y);
                     lo[EPL - 1] = __float2bfloat16_rn(y - __bfloat162float(hi[EPL - 1]));
                 }
-                size_t off;
-                __nv_bfloat16 *dh, *dl;
-                if (kind == 0) {
-                    const int g = head / G, R = t * G + head % G;
-                    off = ((size_t)g * p.rows_pad + R) * HD;
-                    dh = p.qh; dl = p.ql;
-                } else {
-                    off = ((size_t)head * p.S + p.ctx + t) * HD;
-                    dh = p.kh; dl = p.kl;
-                }
                 if constexpr (HD >= 64) {
-                    L::template store_16<__nv_bfloat16, __nv_bfloat162>(dh + off, lane, hi);
-                    L::template store_16<__nv_bfloat16, __nv_bfloat162>(dl + off, lane, lo);
+                    if (kind == 0) {
+                        // Q hi row-interleaved (the attention kernel's threads load it into
+                        // TMEM); Q lo likewise when it goes to TMEM, else row-major for TMA
+                        const int g = head / G, R = t * G + head % G;
+                        const size_t tile = ((size_t)g * (p.rows_pad / 128) + R / 128) * HD * 128;
+                        store_q_interleaved<HD>(p.qh + tile, R % 128, lane, hi);
+                        if (p.ql_interleaved)
+                            store_q_interleaved<HD>(p.ql + tile, R % 128, lane, lo);
+                        else
+                            L::template store_16<__nv_bfloat16, __nv_bfloat162>(
+                                p.ql + ((size_t)g * p.rows_pad + R) * HD, lane, lo);
+                    } else {
+                        const size_t off = ((size_t)head * p.S + p.ctx + t) * HD;
+                        L::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kh + off, lane, hi);
+                        L::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kl + off, lane, lo);
+                    }
                 }
             }
         }
