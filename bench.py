@@ -152,7 +152,7 @@ def oracle_sample(w, budget_s: float, rows_per_call: int = None):
 
     Returns (useful flops computed, seconds, threads, description)."""
     import oracle
-    from gqa_canvas_attention_gb300.workloads import EPS, ROPE_THETA
+    from gqa_canvas_attention_gb300.workloads import EPS
 
     threads = oracle.set_threads(0)
     (kc, vc), d = _oracle_inputs(w, 0)
@@ -160,7 +160,7 @@ def oracle_sample(w, budget_s: float, rows_per_call: int = None):
     # calibrate on a few rows of step 0
     t0 = time.perf_counter()
     oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], kc, vc, w.nh, w.nkv, w.hd,
-                   d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=ROPE_THETA, rows=(0, 16))
+                   d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta, pos0=w.pos0, rows=(0, 16))
     t_row = (time.perf_counter() - t0) / 16
     rows_total = max(1, int(budget_s / max(t_row, 1e-9)))
     rows = min(w.T, rows_total) if rows_per_call is None else rows_per_call
@@ -170,7 +170,7 @@ def oracle_sample(w, budget_s: float, rows_per_call: int = None):
         r = min(rows, rows_total - done)
         t0 = time.perf_counter()
         oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], kc, vc, w.nh, w.nkv, w.hd,
-                       d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=ROPE_THETA, rows=(0, r))
+                       d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta, pos0=w.pos0, rows=(0, r))
         secs += time.perf_counter() - t0
         flops += per_row * r
         done += r
@@ -230,7 +230,7 @@ def main():
     __graft_entry__.build()
     from gqa_canvas_attention_gb300 import binding as B
     from gqa_canvas_attention_gb300 import replicas
-    from gqa_canvas_attention_gb300.workloads import EPS, ROPE_THETA, shared_cache, workload_inputs
+    from gqa_canvas_attention_gb300.workloads import EPS, shared_cache, workload_inputs
 
     rank, world, local = dist_env()
     if world > 1:
@@ -254,7 +254,9 @@ def main():
                      for k in ("q", "k_canvas", "v_canvas", "q_norm_w", "k_norm_w")})
     out = torch.empty((w.T, w.nh * w.hd), dtype=torch.float32, device=dev)
 
-    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, w.theta)
+    if w.pos0 is not None:
+        plan.set(B.DG_OPT_POS0, w.pos0)
     plan.set(B.DG_OPT_PATH, B.DG_PATH_TC if args.path == "tc" else B.DG_PATH_FP32)
     # the canvases are resident (or copied in ahead, ordered by events, in the end-to-end run)
     plan.set(B.DG_OPT_INPUTS_RESIDENT, 1)

@@ -18,11 +18,13 @@ DG_PATH_TC, DG_PATH_FP32 = 0, 1
 DG_OPT_PATH, DG_OPT_POS0, DG_OPT_SPLITS, DG_OPT_WAIT_LIMIT_MS, DG_OPT_PROFILE = 1, 2, 3, 4, 5
 DG_OPT_INJECT_STALL = 6
 DG_OPT_INPUTS_RESIDENT = 7
+DG_DTYPE_F32, DG_DTYPE_F16, DG_DTYPE_BF16 = 0, 1, 2
 DG_INFO_SPLITS_USED, DG_INFO_SCRATCH_BYTES, DG_INFO_CACHE_READY, DG_INFO_LAUNCHES = 16, 17, 18, 19
 DG_STAGE_NORM_ROPE, DG_STAGE_ATTENTION, DG_STAGE_COMBINE, DG_STAGE_CACHE = 0, 1, 2, 3
 
 EXPORTED = [
-    "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare", "dg_attn_norm_rope",
+    "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare",
+    "dg_attn_cache_prepare_typed", "dg_attn_norm_rope",
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
     "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error",
@@ -52,6 +54,8 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_forward.restype = I
     lib.dg_attn_cache_prepare.argtypes = [P, P, P, P]
     lib.dg_attn_cache_prepare.restype = I
+    lib.dg_attn_cache_prepare_typed.argtypes = [P, P, P, I, P]
+    lib.dg_attn_cache_prepare_typed.restype = I
     lib.dg_attn_norm_rope.argtypes = [P] * 11
     lib.dg_attn_norm_rope.restype = I
     lib.dg_attn_attend.argtypes = [P] * 8
@@ -132,6 +136,12 @@ def dg_attn_forward(plan, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_n
 def dg_attn_cache_prepare(plan, k_cache, v_cache, stream=None):
     _check(load().dg_attn_cache_prepare(plan, _ptr(k_cache), _ptr(v_cache), _stream(stream)),
            "dg_attn_cache_prepare")
+
+
+def dg_attn_cache_prepare_typed(plan, k_cache, v_cache, dtype, stream=None):
+    _check(load().dg_attn_cache_prepare_typed(plan, _ptr(k_cache), _ptr(v_cache), int(dtype),
+                                              _stream(stream)),
+           "dg_attn_cache_prepare_typed")
 
 
 def dg_attn_norm_rope(plan, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, q_hat, k_hat,
@@ -219,7 +229,13 @@ class Plan:
         return out
 
     def cache_prepare(self, k_cache, v_cache, stream=None):
-        dg_attn_cache_prepare(self.handle, k_cache, v_cache, stream)
+        """fp32, float16 or bfloat16 cache tensors [nkv, ctx, hd] (both of one dtype)."""
+        import torch
+        types = {torch.float32: DG_DTYPE_F32, torch.float16: DG_DTYPE_F16,
+                 torch.bfloat16: DG_DTYPE_BF16}
+        if k_cache.dtype not in types or v_cache.dtype != k_cache.dtype:
+            raise ValueError("cache tensors must both be float32, float16 or bfloat16")
+        dg_attn_cache_prepare_typed(self.handle, k_cache, v_cache, types[k_cache.dtype], stream)
 
     def norm_rope(self, q, k_canvas, v_canvas, q_norm_w=None, k_norm_w=None, cos_sin=None,
                   stream=None):

@@ -104,7 +104,8 @@ struct dg_attn_plan {
     size_t scratch_bytes;
     // prepared cache
     bool cache_ready;
-    const float *prep_k, *prep_v;   // fp32 path: the caller's buffers
+    const float *prep_k, *prep_v;   // fp32 path: the caller's buffers, or c32k / c32v
+    float *c32k, *c32v;             // fp32 path: copy of a 16-bit cache (made on first need)
     dg::TcMaps maps;
     // profiling: per stage, pairs of events (start, stop) recorded around launches
     std::vector<cudaEvent_t> ev[4];
@@ -127,7 +128,7 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 
 void free_scratch(dg_attn_plan *p)
 {
-    void *ptrs[] = {p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
+    void *ptrs[] = {p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
                     p->kh, p->kl, p->vh, p->part_o, p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
@@ -368,8 +369,8 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
     if (p->path == DG_PATH_TC) {
         // the per-call conversion overwrites the plan's cache copy
         p->cache_ready = false;
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, p->nkv, p->ctx, p->S, p->S_pad,
-                              p->hd};
+        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
+                              p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);
@@ -615,7 +616,17 @@ int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
 int dg_attn_cache_prepare(dg_attn_plan *p, const float *k_cache, const float *v_cache,
                           cudaStream_t s)
 {
+    return dg_attn_cache_prepare_typed(p, k_cache, v_cache, DG_DTYPE_F32, s);
+}
+
+int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void *v_cache,
+                                int dtype, cudaStream_t s)
+{
     if (int rc = check_plan(p)) return rc;
+    if (dtype != DG_DTYPE_F32 && dtype != DG_DTYPE_F16 && dtype != DG_DTYPE_BF16) {
+        set_error("unknown cache element type %d", dtype);
+        return DG_ERR_ARG;
+    }
     if (p->ctx == 0) {
         set_error("ctx == 0: there is no cache to prepare");
         return DG_ERR_ARG;
@@ -628,17 +639,36 @@ int dg_attn_cache_prepare(dg_attn_plan *p, const float *k_cache, const float *v_
         set_error("cache pointers must be 16-byte aligned");
         return DG_ERR_ALIGN;
     }
-    if (p->path == DG_PATH_TC) {
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, p->nkv, p->ctx, p->S, p->S_pad,
-                              p->hd};
-        int rc = record_event(p, DG_STAGE_CACHE, s);
-        if (rc) return rc;
-        cudaError_t err = dg::launch_cache_prep(c, s);
-        if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
-        if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
-    } else {
-        p->prep_k = k_cache;
-        p->prep_v = v_cache;
+    const int type = dtype == DG_DTYPE_F16 ? dg::kCacheF16
+                   : dtype == DG_DTYPE_BF16 ? dg::kCacheBf16 : dg::kCacheF32;
+    dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
+                          p->nkv, p->ctx, p->S, p->S_pad, p->hd, type};
+    if (p->path == DG_PATH_FP32) {
+        if (dtype == DG_DTYPE_F32) {
+            p->prep_k = static_cast<const float *>(k_cache);
+            p->prep_v = static_cast<const float *>(v_cache);
+            p->cache_ready = true;
+            return DG_OK;
+        }
+        // a 16-bit cache is widened once into the plan's own fp32 copy
+        if (!p->c32k) {
+            cudaError_t err = cudaSuccess;
+            const size_t bytes = (size_t)p->nkv * p->ctx * p->hd * sizeof(float);
+            p->c32k = (float *)dalloc(p, bytes, err);
+            p->c32v = (float *)dalloc(p, bytes, err);
+            if (err != cudaSuccess) return cuda_fail(err, "allocating the fp32 cache copy");
+        }
+        c.k32 = p->c32k;
+        c.v32 = p->c32v;
+    }
+    int rc = record_event(p, DG_STAGE_CACHE, s);
+    if (rc) return rc;
+    cudaError_t err = dg::launch_cache_prep(c, s);
+    if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
+    if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
+    if (p->path == DG_PATH_FP32) {
+        p->prep_k = p->c32k;
+        p->prep_v = p->c32v;
     }
     p->cache_ready = true;
     return DG_OK;

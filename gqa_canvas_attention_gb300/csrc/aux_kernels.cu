@@ -1,7 +1,8 @@
 // aux_kernels.cu -- the two streaming helpers around the attention kernels:
 //  * cache_prep: converts an encoder cache [nkv, ctx, hd] (page "inferencelayer 0.2.3,
-//    src/diffusion_gemma_gpu.rs", DgGpuCache / upload_cache: already normed and roped) into the
-//    tensor-core operand arrays [nkv, S, hd]: K as a bf16 hi/lo pair, V rounded to fp16;
+//    src/diffusion_gemma_gpu.rs", DgGpuCache / upload_cache: already normed and roped), given in
+//    fp32 or as an f16 / bf16 twin, into the tensor-core operand arrays [nkv, S, hd] (K as a bf16
+//    hi/lo pair, V rounded to fp16) or, for the exact path, into an fp32 copy;
 //  * combine: merges the partial results of the key-range partitions (split-KV) of one query
 //    row with the log-sum-exp rule  out = sum_s w_s O_s / sum_s w_s l_s,  w_s = b^(m_s - max m).
 #include "dg_internal.cuh"
@@ -10,18 +11,46 @@
 namespace dg {
 namespace {
 
+// Four consecutive cache elements as floats (every f16 and bf16 value is exact in fp32).
+template <typename T> __device__ __forceinline__ float4 load4(const void *base, size_t i);
+template <> __device__ __forceinline__ float4 load4<float>(const void *base, size_t i)
+{
+    return reinterpret_cast<const float4 *>(base)[i];
+}
+template <> __device__ __forceinline__ float4 load4<__half>(const void *base, size_t i)
+{
+    const uint2 u = reinterpret_cast<const uint2 *>(base)[i];
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const void *base, size_t i)
+{
+    const uint2 u = reinterpret_cast<const uint2 *>(base)[i];
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T>
 __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
 {
     const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
     const int hd4 = p.hd / 4;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
+        const float4 k = load4<T>(p.k_cache, i);
+        const float4 v = load4<T>(p.v_cache, i);
+        if (p.k32) {
+            // exact path: an fp32 copy in the caller's layout
+            reinterpret_cast<float4 *>(p.k32)[i] = k;
+            reinterpret_cast<float4 *>(p.v32)[i] = v;
+            continue;
+        }
         const size_t row = i / hd4;              // g * ctx + j
         const int c4 = (int)(i % hd4);
         const size_t g = row / p.ctx, j = row % p.ctx;
         const size_t dst = (g * p.S + j) * p.hd + 4 * (size_t)c4;
-        const float4 k = reinterpret_cast<const float4 *>(p.k_cache)[i];
-        const float4 v = reinterpret_cast<const float4 *>(p.v_cache)[i];
         const float kx[4] = {k.x, k.y, k.z, k.w};
         __nv_bfloat16 hi[4], lo[4];
 #pragma unroll
@@ -121,7 +150,12 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
     if (n4 == 0) return cudaSuccess;
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    cache_kv_kernel<<<blocks, 256, 0, s>>>(p);
+    switch (p.dtype) {
+    case kCacheF32: cache_kv_kernel<float><<<blocks, 256, 0, s>>>(p); break;
+    case kCacheF16: cache_kv_kernel<__half><<<blocks, 256, 0, s>>>(p); break;
+    case kCacheBf16: cache_kv_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -54,11 +54,16 @@ struct NormRopeParams {
 };
 
 // Conversion of a cache [nkv, ctx, hd] into the tensor-core operand arrays (rows 0..ctx-1).
+// Element types of a cache handed to dg_attn_cache_prepare_typed (DG_DTYPE_*).
+enum CacheType : int { kCacheF32 = 0, kCacheF16 = 1, kCacheBf16 = 2 };
+
 struct CachePrepParams {
-    const float *k_cache, *v_cache;
-    __nv_bfloat16 *kh, *kl;
+    const void *k_cache, *v_cache; // [nkv, ctx, hd] of `dtype`
+    __nv_bfloat16 *kh, *kl;        // tensor-core layouts (k32 == nullptr) ...
     __half *vh;                    // [nkv, S, hd] fp16 (cache rows 0..ctx-1)
+    float *k32, *v32;              // ... or an fp32 copy [nkv, ctx, hd] for the exact path
     int nkv, ctx, S, S_pad, hd;
+    int dtype;                     // CacheType
 };
 
 struct AttnFp32Params {

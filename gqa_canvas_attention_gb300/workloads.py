@@ -31,6 +31,8 @@ class Workload:
     steps: int = 1           # denoising steps sharing one cache
     canvases: int = 1        # independent canvases (each its own seed)
     seeds: tuple = field(default_factory=tuple)
+    theta: float = ROPE_THETA
+    pos0: int | None = None  # position of canvas row 0 (None: ctx, the cache length)
 
     @property
     def S(self) -> int:
@@ -54,6 +56,13 @@ WORKLOADS = {
                                 weighted=False, steps=48),
     "mha_canvas4k_x4": Workload("mha_canvas4k_x4", T=4096, ctx=0, nh=16, nkv=16, hd=64, seed=10,
                                 weighted=False, canvases=4, seeds=(10, 11, 12, 13)),
+    # The two layer types of the decoder: a sliding-window layer, whose cache holds the last
+    # 1024 positions of an 8192-long sequence (canvas positions continue at 8192), and a global
+    # layer with its own kv-head count and rope base.
+    "sliding_w1k": Workload("sliding_w1k", T=512, ctx=1024, nh=8, nkv=4, hd=256, seed=20,
+                            weighted=True, pos0=8192),
+    "global_kv2_theta1m": Workload("global_kv2_theta1m", T=512, ctx=8192, nh=8, nkv=2, hd=256,
+                                   seed=21, weighted=True, theta=1.0e6),
 }
 
 

@@ -107,6 +107,20 @@ int dg_attn_forward(dg_attn_plan *plan, const float *q, const float *k_canvas,
 int dg_attn_cache_prepare(dg_attn_plan *plan, const float *k_cache, const float *v_cache,
                           cudaStream_t stream);
 
+/* Element types of a cache for dg_attn_cache_prepare_typed. */
+#define DG_DTYPE_F32  0
+#define DG_DTYPE_F16  1  /* IEEE half */
+#define DG_DTYPE_BF16 2  /* bfloat16 */
+
+/* dg_attn_cache_prepare for a cache held as fp32, or as a 16-bit twin (the f16 K/V twin the page
+ * names as a follow-up of its flash kernel: half the bytes to upload and read), [nkv, ctx, hd] of
+ * `dtype` each, 16-byte aligned.  Every f16 and bf16 value is exact in fp32, so the result equals
+ * dg_attn_cache_prepare on the widened cache.  On the tensor-core path the values go straight
+ * into the operand arrays; on the exact path a 16-bit cache is widened into an fp32 copy owned
+ * by the plan, allocated (cudaMalloc) by the first such call.  DG_ERR_ARG for an unknown dtype. */
+int dg_attn_cache_prepare_typed(dg_attn_plan *plan, const void *k_cache, const void *v_cache,
+                                int dtype, cudaStream_t stream);
+
 /* The first stage alone (RMSNorm + weight + RoPE on q and k, RMSNorm on v), in fp32, written in
  * the input layouts: q_hat [T, nh*hd], k_hat and v_hat [T, nkv*hd]. */
 int dg_attn_norm_rope(dg_attn_plan *plan, const float *q, const float *k_canvas,

@@ -34,11 +34,11 @@ def to_dev(d):
     return {k: (v.cuda() if v is not None else None) for k, v in d.items()}
 
 
-def oracle_out(d, nh, nkv, hd, rows=None, pos0=None, cos_sin=None):
+def oracle_out(d, nh, nkv, hd, rows=None, pos0=None, cos_sin=None, theta=ROPE_THETA):
     f = lambda x: None if x is None else x.numpy()
     return oracle.forward(f(d["q"]), f(d["k_canvas"]), f(d["v_canvas"]), f(d["k_cache"]),
                           f(d["v_cache"]), nh, nkv, hd, f(d["q_norm_w"]), f(d["k_norm_w"]),
-                          cos_sin=cos_sin, eps=EPS, theta=ROPE_THETA, pos0=pos0, rows=rows)
+                          cos_sin=cos_sin, eps=EPS, theta=theta, pos0=pos0, rows=rows)
 
 
 def row_ranges(T):
@@ -111,13 +111,15 @@ def test_workload_parity(name, path):
     w = WORKLOADS[name]
     d = workload_inputs(w)
     dd = to_dev(d)
-    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, w.theta)
     plan.set(B.DG_OPT_PATH, path)
+    if w.pos0 is not None:
+        plan.set(B.DG_OPT_POS0, w.pos0)
     out = run_forward(plan, dd)
     ranges = row_ranges(w.T)
     ref = np.zeros((w.T, w.nh * w.hd))
     for a, b in ranges:
-        ref[a:b] = oracle_out(d, w.nh, w.nkv, w.hd, rows=(a, b))[a:b]
+        ref[a:b] = oracle_out(d, w.nh, w.nkv, w.hd, rows=(a, b), pos0=w.pos0, theta=w.theta)[a:b]
     check(out, ref, path, ranges, name)
 
 
@@ -360,3 +362,30 @@ def test_resident_inputs_give_the_same_bits():
     d0 = make_inputs(T, ctx, nh, nkv, hd, seed=50)
     d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]     # the prepared cache
     check(outs[1][3], oracle_out(d, nh, nkv, hd, rows=(0, 8)), B.DG_PATH_TC, [(0, 8)], "resident")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
+def test_sixteen_bit_cache_twin(dtype, path):
+    """A cache held as an f16 / bf16 twin: every 16-bit value is exact in fp32, so the block must
+    match the oracle run on the widened cache; the prepared cache then serves later forwards."""
+    T, ctx, nh, nkv, hd = 100, 900, 8, 2, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=61)
+    k16, v16 = d["k_cache"].to(dtype), d["v_cache"].to(dtype)
+    d["k_cache"], d["v_cache"] = k16.float(), v16.float()       # what the oracle sees
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_PATH, path)
+    plan.cache_prepare(k16.cuda(), v16.cuda())
+    assert plan.get(B.DG_INFO_CACHE_READY) == 1
+    out = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                       dd["k_norm_w"])
+    assert plan.sync_status() == B.DG_OK
+    check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], f"twin-{dtype}")
+    # the fp32 cache through the same entry point gives the same bits as the 16-bit twin
+    ref = out.clone()
+    plan.cache_prepare(dd["k_cache"], dd["v_cache"])
+    out2 = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                        dd["k_norm_w"])
+    assert plan.sync_status() == B.DG_OK
+    assert torch.equal(out2, ref)
