@@ -47,6 +47,10 @@ def _load():
         lib.dgo_forward.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_double,
                                     ctypes.c_longlong] + [P] * 8 + [ctypes.c_int, ctypes.c_int, P])
         lib.dgo_forward.restype = ctypes.c_int
+        lib.dgo_rmsnorm_rows.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_double, P]
+        lib.dgo_rmsnorm_rows.restype = None
+        lib.dgo_linear.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P]
+        lib.dgo_linear.restype = None
         lib.dgo_set_threads.argtypes = [ctypes.c_int]
         lib.dgo_set_threads.restype = ctypes.c_int
         _lib = lib
@@ -145,3 +149,45 @@ def forward(q, k_canvas, v_canvas, k_cache, v_cache, nh: int, nkv: int, hd: int,
     if rc != 0:
         raise ValueError("oracle: bad sizes")
     return out
+
+
+def rmsnorm_rows(x, w=None, eps: float = 1e-6) -> np.ndarray:
+    """Row RMSNorm of x [rows, h] (fp32) with optional weight [h]; fp64 [rows, h]."""
+    x = _f32(x)
+    rows, h = x.shape
+    out = np.empty((rows, h), dtype=np.float64)
+    _load().dgo_rmsnorm_rows(_ptr(x), rows, h, _ptr(_f32(w)), float(eps), _ptr(out))
+    return out
+
+
+def linear(xhat, W) -> np.ndarray:
+    """y = xhat W^T with xhat [rows, k] (fp64) and W [n, k] (fp32); fp64 [rows, n]."""
+    xhat = _f64(xhat)
+    W = _f32(W)
+    rows, k = xhat.shape
+    n = W.shape[0]
+    assert W.shape[1] == k
+    out = np.empty((rows, n), dtype=np.float64)
+    _load().dgo_linear(_ptr(xhat), rows, k, _ptr(W), n, _ptr(out))
+    return out
+
+
+def project_qkv(x, ln_in_w, wq, wk, wv=None, eps: float = 1e-6):
+    """The attention branch's input RMSNorm and q / k / v projections (fp64).  With wv None the
+    value projection is the raw k projection (the page's k_eq_v layers)."""
+    xhat = rmsnorm_rows(x, ln_in_w, eps)
+    q = linear(xhat, wq)
+    k = linear(xhat, wk)
+    v = k.copy() if wv is None else linear(xhat, wv)
+    return q, k, v
+
+
+def forward_hidden(x, ln_in_w, wq, wk, wv, k_cache, v_cache, nh: int, nkv: int, hd: int,
+                   q_norm_w=None, k_norm_w=None, cos_sin=None, eps: float = 1e-6,
+                   theta: float = 10000.0, pos0=None, rows=None) -> np.ndarray:
+    """Projection then the block: the projections enter the block as fp32 (the page's buffers
+    hold them in f32).  Returns fp64 out [T, nh*hd]."""
+    q, k, v = project_qkv(x, ln_in_w, wq, wk, wv, eps)
+    f = lambda a: a.astype(np.float32)
+    return forward(f(q), f(k), f(v), k_cache, v_cache, nh, nkv, hd, q_norm_w, k_norm_w,
+                   cos_sin=cos_sin, eps=eps, theta=theta, pos0=pos0, rows=rows)

@@ -187,6 +187,43 @@ int dgo_forward(int nh, int nkv, int hd, int ctx, int T, double eps, double thet
     return 0;
 }
 
+/* The step before the block (canvas_forward, attention branch): the input RMSNorm of the
+ * residual stream, `rms!(&cur, &l.ln_in, 1, &nb)` (item DG_RMSNORM: x * (mean x^2 + eps)^-1/2,
+ * times w[i] when weighted), then the q / k / v projections, `gemm!` on GLin weights, which
+ * compute y = x W^T with W stored [n, k] (the page's "y = x.W^T", bias zero).
+ * x [rows, h] fp32, w [h] or NULL; xhat [rows, h] fp64. */
+void dgo_rmsnorm_rows(const float *x, int rows, int h, const float *w, double eps, double *xhat)
+{
+    for (int r = 0; r < rows; ++r) {
+        const float *xr = x + (size_t)r * h;
+        double ss = 0.0;
+        for (int i = 0; i < h; ++i) ss += (double)xr[i] * (double)xr[i];
+        double inv = 1.0 / sqrt(ss / (double)h + eps);
+        for (int i = 0; i < h; ++i) {
+            double v = (double)xr[i] * inv;
+            if (w) v *= (double)w[i];
+            xhat[(size_t)r * h + i] = v;
+        }
+    }
+}
+
+/* y[r, j] = sum_i xhat[r, i] * W[j, i] for W [n, k] fp32 (GLin layout before its upload
+ * transpose); fp64 accumulation in index order. */
+void dgo_linear(const double *xhat, int rows, int k, const float *W, int n, double *y)
+{
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (long long u = 0; u < (long long)rows * n; ++u) {
+        int r = (int)(u / n), j = (int)(u % n);
+        const double *xr = xhat + (size_t)r * k;
+        const float *wr = W + (size_t)j * k;
+        double acc = 0.0;
+        for (int i = 0; i < k; ++i) acc += xr[i] * (double)wr[i];
+        y[u] = acc;
+    }
+}
+
 /* Thread control for the timed CPU baseline (1 when built without OpenMP). */
 int dgo_set_threads(int n)
 {

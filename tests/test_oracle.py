@@ -339,3 +339,63 @@ def test_worked_example_by_hand():
     s = 7.0 / math.sqrt(12.5)
     w1 = 1.0 / (1.0 + math.exp(-s))
     np.testing.assert_allclose(out[0], [1.0 - w1, w1 * math.sqrt(2.0)], rtol=1e-14)
+
+
+# ---------------------------------------------------------------- input RMSNorm + projections
+# (canvas_forward, attention branch: rms!(cur, ln_in) then gemm! y = x W^T on GLin weights)
+
+def test_projection_hand_example():
+    """x = [3, 4], no weight, eps = 0: mean x^2 = 12.5, so xhat = x / sqrt(12.5); with W = [[1, 2]]
+    the projection is (3 + 8) / sqrt(12.5).  Catches: x W instead of x W^T, a missing norm."""
+    x = np.array([[3.0, 4.0]], dtype=np.float32)
+    q, k, v = oracle.project_qkv(x, None, np.array([[1.0, 2.0]], np.float32),
+                                 np.array([[0.0, 1.0], [1.0, 0.0]], np.float32), eps=0.0)
+    s = math.sqrt(12.5)
+    assert q.shape == (1, 1) and abs(q[0, 0] - 11.0 / s) < 1e-14
+    np.testing.assert_allclose(k[0], [4.0 / s, 3.0 / s], rtol=1e-14)
+    np.testing.assert_array_equal(v, k)     # no value projection: v is the raw k projection
+
+
+def test_projection_rows_of_w_select_columns():
+    """A W row with a single 1 at column i returns column i of the normed input, so each output
+    column j is row j of W dotted with the row of x: W is [n, k], applied transposed.
+    Catches: transposed W, a row/column index swap, an output column offset."""
+    h, n = 12, 5
+    x = rnd(4, h)
+    cols = [7, 0, 11, 3, 3]
+    W = np.zeros((n, h), np.float32)
+    for j, i in enumerate(cols):
+        W[j, i] = 1.0
+    lnw = 1.0 + 0.2 * rnd(h)
+    q, _, _ = oracle.project_qkv(x, lnw, W, W, eps=1e-6)
+    xd = x.astype(np.float64)
+    m = (xd ** 2).mean(axis=1, keepdims=True)
+    xhat = xd / np.sqrt(m + 1e-6) * lnw.astype(np.float64)
+    np.testing.assert_allclose(q, xhat[:, cols], rtol=1e-14)
+
+
+def test_input_norm_weight_scales_linearly_and_norm_is_scale_free():
+    """RMSNorm removes any positive scale of x; the ln_in weight scales every projection
+    linearly.  Catches: eps applied wrongly at scale, weight applied before the mean."""
+    h, n = 16, 6
+    x, W, lnw = rnd(3, h), rnd(n, h), 1.0 + 0.1 * rnd(h)
+    q1, _, _ = oracle.project_qkv(x, lnw, W, W, eps=0.0)
+    q2, _, _ = oracle.project_qkv((8.0 * x).astype(np.float32), lnw, W, W, eps=0.0)
+    q3, _, _ = oracle.project_qkv(x, (2.0 * lnw).astype(np.float32), W, W, eps=0.0)
+    np.testing.assert_allclose(q2, q1, rtol=1e-12)
+    np.testing.assert_allclose(q3, 2.0 * q1, rtol=1e-12)
+
+
+def test_projection_brute_force_with_fsum():
+    """An independent restatement with Python loops and math.fsum on a small case."""
+    h, n, rows = 10, 7, 3
+    x, W, lnw = rnd(rows, h), rnd(n, h), 1.0 + 0.1 * rnd(h)
+    eps = 1e-3
+    q, _, _ = oracle.project_qkv(x, lnw, W, W, eps=eps)
+    for r in range(rows):
+        ms = math.fsum(float(v) * float(v) for v in x[r]) / h
+        inv = 1.0 / math.sqrt(ms + eps)
+        xr = [float(x[r, i]) * inv * float(lnw[i]) for i in range(h)]
+        for j in range(n):
+            ref = math.fsum(xr[i] * float(W[j, i]) for i in range(h))
+            assert abs(q[r, j] - ref) <= 1e-12 * (1.0 + abs(ref))
