@@ -21,10 +21,12 @@ DG_OPT_INPUTS_RESIDENT = 7
 DG_DTYPE_F32, DG_DTYPE_F16, DG_DTYPE_BF16 = 0, 1, 2
 DG_INFO_SPLITS_USED, DG_INFO_SCRATCH_BYTES, DG_INFO_CACHE_READY, DG_INFO_LAUNCHES = 16, 17, 18, 19
 DG_STAGE_NORM_ROPE, DG_STAGE_ATTENTION, DG_STAGE_COMBINE, DG_STAGE_CACHE = 0, 1, 2, 3
+DG_STAGE_PROJECTION = 4
 
 EXPORTED = [
     "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare",
-    "dg_attn_cache_prepare_typed", "dg_attn_norm_rope",
+    "dg_attn_cache_prepare_typed", "dg_attn_proj_prepare", "dg_attn_forward_hidden",
+    "dg_attn_norm_rope",
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
     "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error",
@@ -56,6 +58,10 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_cache_prepare.restype = I
     lib.dg_attn_cache_prepare_typed.argtypes = [P, P, P, I, P]
     lib.dg_attn_cache_prepare_typed.restype = I
+    lib.dg_attn_proj_prepare.argtypes = [P, I, P, P, P, P, P]
+    lib.dg_attn_proj_prepare.restype = I
+    lib.dg_attn_forward_hidden.argtypes = [P] * 9
+    lib.dg_attn_forward_hidden.restype = I
     lib.dg_attn_norm_rope.argtypes = [P] * 11
     lib.dg_attn_norm_rope.restype = I
     lib.dg_attn_attend.argtypes = [P] * 8
@@ -136,6 +142,18 @@ def dg_attn_forward(plan, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_n
 def dg_attn_cache_prepare(plan, k_cache, v_cache, stream=None):
     _check(load().dg_attn_cache_prepare(plan, _ptr(k_cache), _ptr(v_cache), _stream(stream)),
            "dg_attn_cache_prepare")
+
+
+def dg_attn_proj_prepare(plan, H, ln_in_w, wq, wk, wv=None, stream=None):
+    _check(load().dg_attn_proj_prepare(plan, int(H), _ptr(ln_in_w), _ptr(wq), _ptr(wk), _ptr(wv),
+                                       _stream(stream)), "dg_attn_proj_prepare")
+
+
+def dg_attn_forward_hidden(plan, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out,
+                           stream=None):
+    _check(load().dg_attn_forward_hidden(plan, _ptr(x), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(q_norm_w), _ptr(k_norm_w), _ptr(cos_sin), _ptr(out),
+                                         _stream(stream)), "dg_attn_forward_hidden")
 
 
 def dg_attn_cache_prepare_typed(plan, k_cache, v_cache, dtype, stream=None):
@@ -226,6 +244,18 @@ class Plan:
             out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=q.device)
         dg_attn_forward(self.handle, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w,
                         cos_sin, out, stream)
+        return out
+
+    def proj_prepare(self, H, ln_in_w, wq, wk, wv=None, stream=None):
+        dg_attn_proj_prepare(self.handle, H, ln_in_w, wq, wk, wv, stream)
+
+    def forward_hidden(self, x, k_cache=None, v_cache=None, q_norm_w=None, k_norm_w=None,
+                       cos_sin=None, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=x.device)
+        dg_attn_forward_hidden(self.handle, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out,
+                               stream)
         return out
 
     def cache_prepare(self, k_cache, v_cache, stream=None):

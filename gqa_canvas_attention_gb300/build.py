@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "dgattn")
 LIB = os.path.join(PKG, "libdgattn.so")
-SOURCES = ["api.cu", "norm_rope.cu", "attn_fp32.cu", "attn_tc.cu", "aux_kernels.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "norm_rope.cu", "attn_fp32.cu", "attn_tc.cu", "aux_kernels.cu", "noalloc.cu",
+           "proj_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

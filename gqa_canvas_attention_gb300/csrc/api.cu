@@ -108,8 +108,17 @@ struct dg_attn_plan {
     float *c32k, *c32v;             // fp32 path: copy of a 16-bit cache (made on first need)
     dg::TcMaps maps;
     // profiling: per stage, pairs of events (start, stop) recorded around launches
-    std::vector<cudaEvent_t> ev[4];
-    size_t ev_used[4];
+    std::vector<cudaEvent_t> ev[5];
+    size_t ev_used[5];
+    // projection step (dg_attn_proj_prepare / dg_attn_forward_hidden)
+    int H;                          // hidden size the projection weights were prepared for
+    int proj_rows;                  // rows of W: (nh + nkv [+ nkv]) * hd
+    bool kv_shared;                 // no value projection: v is the raw k projection
+    bool proj_ready;
+    __nv_bfloat16 *wh, *wl;         // [proj_rows, H] W diag(ln_in_w), bf16 hi / lo
+    __nv_bfloat16 *xh, *xl;         // [T_pad, H] the residual stream, bf16 hi / lo
+    float *rin;                     // [T] input-norm scale
+    dg::ProjMaps pmaps;
 };
 
 namespace {
@@ -128,7 +137,7 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 
 void free_scratch(dg_attn_plan *p)
 {
-    void *ptrs[] = {p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
+    void *ptrs[] = {p->wh, p->wl, p->xh, p->xl, p->rin, p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
                     p->kh, p->kl, p->vh, p->part_o, p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
@@ -753,6 +762,127 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
     return enqueue_attention(p, k_cache, v_cache, out, s);
 }
 
+int dg_attn_proj_prepare(dg_attn_plan *p, int H, const float *ln_in_w, const float *wq,
+                         const float *wk, const float *wv, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!p->tc_ok || (p->hd != 128 && p->hd != 256)) {
+        set_error("the projection step needs the tensor-core path with hd 128 or 256");
+        return DG_ERR_UNSUPPORTED;
+    }
+    if (H < 64 || H % 64 != 0) {
+        set_error("H=%d: the hidden size must be a positive multiple of 64", H);
+        return DG_ERR_ARG;
+    }
+    if (!wq || !wk) {
+        set_error("wq and wk are required");
+        return DG_ERR_ARG;
+    }
+    const void *all[] = {ln_in_w, wq, wk, wv};
+    for (const void *x : all)
+        if (x && !aligned16(x)) {
+            set_error("pointers must be 16-byte aligned");
+            return DG_ERR_ALIGN;
+        }
+    static bool attrs_done = false;
+    cudaError_t err = cudaSuccess;
+    if (!attrs_done) {
+        err = dg::proj_prepare_attrs();
+        if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
+        attrs_done = true;
+    }
+    const bool shared = wv == nullptr;
+    const int rows = (p->nh + p->nkv + (shared ? 0 : p->nkv)) * p->hd;
+    const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
+    if (H != p->H || rows != p->proj_rows) {
+        void *old[] = {p->wh, p->wl, p->xh, p->xl, p->rin};
+        for (void *x : old)
+            if (x) cudaFree(x);
+        p->wh = p->wl = p->xh = p->xl = nullptr;
+        p->rin = nullptr;
+        p->proj_ready = false;
+        p->H = 0;
+        p->wh = (__nv_bfloat16 *)dalloc(p, (size_t)rows * H * 2, err);
+        p->wl = (__nv_bfloat16 *)dalloc(p, (size_t)rows * H * 2, err);
+        p->xh = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * H * 2, err);
+        p->xl = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * H * 2, err);
+        p->rin = (float *)dalloc(p, (size_t)p->T * sizeof(float), err);
+        if (err != cudaSuccess) return cuda_fail(err, "allocating the projection operands");
+        bool ok = true;
+        ok &= encode_3d(&p->pmaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xh, H, t_pad, 1, 64,
+                        dg::kTileM, H);
+        ok &= encode_3d(&p->pmaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xl, H, t_pad, 1, 64,
+                        dg::kTileM, H);
+        ok &= encode_3d(&p->pmaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wh, H, rows, 1, 64,
+                        64, H);
+        ok &= encode_3d(&p->pmaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wl, H, rows, 1, 64,
+                        64, H);
+        if (!ok) {
+            set_error("cuTensorMapEncodeTiled failed for the projection operands");
+            return DG_ERR_CUDA;
+        }
+        p->H = H;
+        p->proj_rows = rows;
+    }
+    dg::ProjWeightParams w{wq, wk, wv, ln_in_w, p->wh, p->wl, p->nh * p->hd, p->nkv * p->hd, rows,
+                           H};
+    err = dg::launch_proj_weights(w, s);
+    if (err != cudaSuccess) return cuda_fail(err, "projection weight preparation launch");
+    p->kv_shared = shared;
+    p->proj_ready = true;
+    return DG_OK;
+}
+
+int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache,
+                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                           const float *cos_sin, float *out, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!p->proj_ready) {
+        set_error("no projection weights prepared (dg_attn_proj_prepare)");
+        return DG_ERR_STATE;
+    }
+    if (p->path != DG_PATH_TC) {
+        set_error("the projection step runs on the tensor-core path only");
+        return DG_ERR_UNSUPPORTED;
+    }
+    if (!x || !out) {
+        set_error("x and out are required");
+        return DG_ERR_ARG;
+    }
+    const void *all[] = {x, q_norm_w, k_norm_w, cos_sin, out};
+    for (const void *a : all)
+        if (a && !aligned16(a)) {
+            set_error("pointers must be 16-byte aligned");
+            return DG_ERR_ALIGN;
+        }
+    if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+    if (int rc = rope_table(p, cos_sin, s)) return rc;
+    int rc = record_event(p, DG_STAGE_PROJECTION, s);
+    if (rc) return rc;
+    dg::ProjPrepParams pp{x, p->rin, p->xh, p->xl, p->T, p->H, p->eps};
+    cudaError_t err = dg::launch_hidden_prep(pp, s);
+    if (err != cudaSuccess) return cuda_fail(err, "input norm launch");
+    dg::ProjParams q{};
+    q.rin = p->rin;
+    q.wq_norm = q_norm_w;
+    q.wk_norm = k_norm_w;
+    q.cos_sin = cos_sin;
+    q.qh = p->qh; q.ql = p->ql; q.kh = p->kh; q.kl = p->kl; q.vh = p->vh;
+    q.status = p->status;
+    q.wait_limit_ns = (unsigned long long)p->wait_limit_ms * 1000000ull;
+    q.T = p->T; q.H = p->H; q.nh = p->nh; q.nkv = p->nkv; q.G = p->G; q.ctx = p->ctx; q.S = p->S;
+    q.rows_pad = p->rows_pad;
+    q.rows_pad_tokens = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
+    q.ql_interleaved = dg::tc_geometry(p->hd).ql_in_tmem;
+    q.kv_shared = p->kv_shared ? 1 : 0;
+    q.eps = p->eps;
+    err = dg::launch_qkv_proj(q, p->pmaps, p->hd, p->proj_rows / 128, s);
+    if (err != cudaSuccess) return cuda_fail(err, "projection launch");
+    if ((rc = record_event(p, DG_STAGE_PROJECTION, s))) return rc;
+    return enqueue_attention(p, k_cache, v_cache, out, s);
+}
+
 int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
 {
     if (int rc = check_plan(p)) return rc;
@@ -773,7 +903,7 @@ int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
 int dg_attn_profile_read(dg_attn_plan *p, int stage, double *total_ms, long long *launches)
 {
     if (int rc = check_plan(p)) return rc;
-    if (!total_ms || !launches || stage < 0 || stage > 3) {
+    if (!total_ms || !launches || stage < 0 || stage > 4) {
         set_error("bad stage or NULL output pointer");
         return DG_ERR_ARG;
     }

@@ -100,6 +100,46 @@ struct CombineParams {
     int log2_domain;               // 1: weights are 2^(s - m) (tensor-core path), 0: e^(s - m)
 };
 
+// ---- the projection step before the block (proj_tc.cu) ----
+struct ProjPrepParams {            // input RMSNorm scale and the bf16 hi/lo split of x
+    const float *x;                // [T, H] residual stream
+    float *rin;                    // [T] (mean x^2 + eps)^-1/2
+    __nv_bfloat16 *xh, *xl;        // [T_pad, H]
+    int T, H;
+    float eps;
+};
+
+struct ProjWeightParams {          // W' = W diag(ln_w), split bf16 hi/lo, rows q | k | v
+    const float *wq, *wk, *wv;     // [nq, H], [nk, H], [n_rows - nq - nk, H]
+    const float *ln_w;             // [H] or null
+    __nv_bfloat16 *wh, *wl;        // [n_rows, H]
+    int nq, nk, n_rows, H;
+};
+
+struct ProjParams {
+    const float *rin;              // [T]
+    const float *wq_norm, *wk_norm;// [hd] or null
+    const float *cos_sin;          // [T, 2*hd]
+    __nv_bfloat16 *qh, *ql, *kh, *kl;
+    __half *vh;
+    uint32_t *status;
+    unsigned long long wait_limit_ns;
+    int T, H, nh, nkv, G, ctx, S, rows_pad, rows_pad_tokens;
+    int ql_interleaved, kv_shared;
+    float eps;
+};
+
+struct ProjMaps {
+    CUtensorMap xh, xl;            // bf16 [T_pad][H], box {64, 128}
+    CUtensorMap wh, wl;            // bf16 [n_rows][H], box {64, 64}
+};
+
+cudaError_t proj_prepare_attrs();
+cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s);
+cudaError_t launch_proj_weights(const ProjWeightParams &p, cudaStream_t s);
+cudaError_t launch_qkv_proj(const ProjParams &p, const ProjMaps &maps, int hd, int n_tiles,
+                            cudaStream_t s);
+
 // Tensor maps handed to the tensor-core kernel (by value, __grid_constant__).
 struct TcMaps {
     CUtensorMap ql;                // bf16 [nkv][rows_pad][hd], box {64, 128, 1}

@@ -1,0 +1,436 @@
+// proj_tc.cu -- the step before the attention block on the tensor cores (page "inferencelayer
+// 0.2.3, src/diffusion_gemma_gpu.rs", canvas_forward, attention branch): the input RMSNorm of the
+// residual stream (`rms!(&cur, &l.ln_in, 1, &nb)`, item DG_RMSNORM), the q / k / v projections
+// (`gemm!` on GLin weights: y = x W^T, W stored [n, k]; with no value projection, v is the raw k
+// projection), and then -- fused into the GEMM's epilogue -- the block's own first stage (the
+// per-head qk-norm + NeoX RoPE and the weightless v-norm of DG_HEADNORM_ROPE), written straight
+// into the attention kernel's operand arrays.
+//
+// Precision: fp32 inputs and weights.  The input norm's per-token scale r_t = (mean x^2 + eps)^-1/2
+// is applied in the epilogue; the norm weight is folded into W once (W' = W diag(ln_w), one fp32
+// rounding).  x and W' are split into bf16 hi/lo pairs and the product is taken as
+// x_hi W'_hi + x_hi W'_lo + x_lo W'_hi (three kind::f16 MMAs, fp32 accumulation in TMEM), about
+// 16 significant bits per operand, as in the attention kernel's scores.
+//
+// Work unit: one CTA per (128 tokens, 128 output columns).  Columns are taken in groups of 64
+// (one 128-byte swizzled panel of W rows).  A CTA holds two groups whose columns are RoPE partners
+// (i and i + hd/2): hd = 128 -> one head; hd = 256 -> half a head (groups c and c + 2), the two
+// halves of a head being a cluster of 2 CTAs that exchange one partial sum of squares per token.
+// Roles: warp 0 TMA producer (3-stage ring), warp 1 MMA issuer and TMEM owner, warps 2-5
+// epilogue (thread = token row = TMEM lane).  Every mbarrier wait is bounded.
+#include "dg_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kProjStages = 3;
+constexpr int kProjThreads = 192;
+constexpr int kPanelBytes = kTileM * 128;                   // 128 rows x 64 bf16
+constexpr int kStageBytes = 4 * kPanelBytes;                // A hi, A lo, B hi, B lo
+constexpr int kProjBarOff = kProjStages * kStageBytes;
+constexpr int kProjSmem = kProjBarOff + 256 + 512 + 1024;   // barriers, sum exchange, alignment
+
+__global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
+{
+    // one warp per token row: r_t and the bf16 hi/lo split of the row
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= p.T) return;
+    const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)t * p.H);
+    __nv_bfloat16 *xh = p.xh + (size_t)t * p.H, *xl = p.xl + (size_t)t * p.H;
+    float ss = 0.f;
+    for (int i = lane; i < p.H / 4; i += 32) {
+        const float4 v = x[i];
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+        uint2 uh, ul;
+        uh.x = *reinterpret_cast<const uint32_t *>(&h01);
+        uh.y = *reinterpret_cast<const uint32_t *>(&h23);
+        ul.x = *reinterpret_cast<const uint32_t *>(&l01);
+        ul.y = *reinterpret_cast<const uint32_t *>(&l23);
+        reinterpret_cast<uint2 *>(xh)[i] = uh;
+        reinterpret_cast<uint2 *>(xl)[i] = ul;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) p.rin[t] = rsqrtf(ss / (float)p.H + p.eps);
+}
+
+__global__ void __launch_bounds__(256) proj_weights_kernel(ProjWeightParams p)
+{
+    // W' = W diag(ln_w) split into bf16 hi/lo, rows in the order q | k | v
+    const size_t n4 = (size_t)p.n_rows * p.H / 4;
+    const int h4 = p.H / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / h4;
+        const int c4 = (int)(i % h4);
+        const float *src = row < (size_t)p.nq ? p.wq + row * p.H
+                         : row < (size_t)(p.nq + p.nk) ? p.wk + (row - p.nq) * p.H
+                                                       : p.wv + (row - p.nq - p.nk) * p.H;
+        float4 v = reinterpret_cast<const float4 *>(src)[c4];
+        if (p.ln_w) {
+            const float4 w = reinterpret_cast<const float4 *>(p.ln_w)[c4];
+            v.x *= w.x; v.y *= w.y; v.z *= w.z; v.w *= w.w;
+        }
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+        uint2 uh, ul;
+        uh.x = *reinterpret_cast<const uint32_t *>(&h01);
+        uh.y = *reinterpret_cast<const uint32_t *>(&h23);
+        ul.x = *reinterpret_cast<const uint32_t *>(&l01);
+        ul.y = *reinterpret_cast<const uint32_t *>(&l23);
+        reinterpret_cast<uint2 *>(p.wh)[i] = uh;
+        reinterpret_cast<uint2 *>(p.wl)[i] = ul;
+    }
+}
+
+// 64 values (one column group of a token row) as bf16 into 128 contiguous bytes.
+__device__ __forceinline__ void store_bf16_row64(__nv_bfloat16 *dst, const float *v)
+{
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        uint4 w;
+        uint32_t *pw = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * u + 2 * e], v[8 * u + 2 * e + 1]);
+            pw[e] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(dst)[u] = w;
+    }
+}
+
+// The bf16 hi/lo split of 64 values: hi = bf16(v) (exact in fp32), lo = v - hi (rounded to bf16
+// when stored).
+__device__ __forceinline__ void split64(const float *v, float *hi, float *lo)
+{
+#pragma unroll
+    for (int e = 0; e < 64; e += 2) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[e], v[e + 1]);
+        const float2 f = __bfloat1622float2(h);
+        hi[e] = f.x;
+        hi[e + 1] = f.y;
+        lo[e] = v[e] - f.x;
+        lo[e + 1] = v[e + 1] - f.y;
+    }
+}
+
+// The q operand's row-interleaved layout (see the first-stage kernel): 16-byte unit u of tile
+// row r at (tile * hd/8 + u) * 128 + r.  Writes the 8 units of 64 columns starting at c0.
+template <int HD>
+__device__ __forceinline__ void store_q_rows64(__nv_bfloat16 *tile_base, int r, int c0,
+                                               const float *v)
+{
+    uint4 *base = reinterpret_cast<uint4 *>(tile_base);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        uint4 w;
+        uint32_t *pw = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * u + 2 * e], v[8 * u + 2 * e + 1]);
+            pw[e] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        base[(size_t)(c0 / 8 + u) * kTileM + r] = w;
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kProjThreads, 1)
+qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kProjBarOff);
+    uint64_t *full = bars;
+    uint64_t *empty = full + kProjStages;
+    uint64_t *acc_full = empty + kProjStages;
+    uint64_t *drain = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    float *ss_ex = reinterpret_cast<float *>(smem + kProjBarOff + 256);   // [128]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const int m0 = blockIdx.y * kTileM;
+    const int j = blockIdx.x;
+    // the two column groups of this CTA (RoPE partners) and the head they belong to
+    const int head = HD == 256 ? j / 2 : j;
+    const int g0 = HD == 256 ? 4 * head + (j & 1) : 2 * head;
+    const int g1 = g0 + HD / 128;
+    const int c0 = (g0 % (HD / 64)) * 64;                    // first column of g0 in its head
+    const int nk = p.H / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kProjStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        prefetch_tmap(&maps.xh);
+        prefetch_tmap(&maps.xl);
+        prefetch_tmap(&maps.wh);
+        prefetch_tmap(&maps.wl);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tacc = *tmem_slot;
+
+    float a[64], b[64];          // epilogue: the token row's values of groups g0 and g1
+    float ss_local = 0.f;
+    bool epi_ok = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued[kProjStages] = {};
+            for (int it = 0; it < nk; ++it) {
+                const int s = it % kProjStages;
+                if (it >= kProjStages &&
+                    !mbar_wait_bounded(&empty[s], ((it / kProjStages) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * kStageBytes;
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                tma_load_3d(st, &maps.xh, &full[s], it * 64, m0, 0);
+                tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], it * 64, m0, 0);
+                tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], it * 64, g0 * 64, 0);
+                tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], it * 64,
+                            g1 * 64, 0);
+                tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], it * 64, g0 * 64, 0);
+                tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], it * 64,
+                            g1 * 64, 0);
+                ++issued[s];
+            }
+            if (!ok) atomicOr(p.status, kErrWaitProducer);
+            for (int s = 0; s < kProjStages; ++s)
+                if (issued[s] > 0) mbar_wait_bounded(&full[s], (issued[s] - 1) & 1, limit);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, 128);
+            const uint64_t d0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+            bool ok = true;
+            for (int it = 0; ok && it < nk; ++it) {
+                const int s = it % kProjStages;
+                if (!mbar_wait_bounded(&full[s], (it / kProjStages) & 1, limit)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t base = d0 + (uint64_t)((s * kStageBytes) >> 4);
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    const uint64_t ah = base + (uint64_t)((sub * 32) >> 4);
+                    const uint64_t al = base + (uint64_t)((kPanelBytes + sub * 32) >> 4);
+                    const uint64_t bh = base + (uint64_t)((2 * kPanelBytes + sub * 32) >> 4);
+                    const uint64_t bl = base + (uint64_t)((3 * kPanelBytes + sub * 32) >> 4);
+                    mma_bf16_ss(tacc, ah, bh, idesc, (it > 0 || sub > 0) ? 1u : 0u);
+                    mma_bf16_ss(tacc, ah, bl, idesc, 1u);
+                    mma_bf16_ss(tacc, al, bh, idesc, 1u);
+                }
+                mma_commit(&empty[s]);
+            }
+            if (ok) mma_commit(acc_full);
+            else atomicOr(p.status, kErrWaitMma);
+            mma_commit(drain);
+            if (!mbar_wait_bounded(drain, 0, limit)) atomicOr(p.status, kErrWaitDrain);
+        }
+        __syncwarp();
+    } else {
+        // epilogue part 1: accumulator rows into registers, input-norm scale, sum of squares
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, limit));
+        if (ok) {
+            tc_fence_after();
+            uint32_t u[32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld32(tacc + lane_off + 32 * c, u);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[32 * c + i] = __uint_as_float(u[i]);
+                tmem_ld32(tacc + lane_off + 64 + 32 * c, u);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) b[32 * c + i] = __uint_as_float(u[i]);
+            }
+            const int t = m0 + r;
+            const float rs = t < p.T ? p.rin[t] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                a[i] *= rs;
+                b[i] *= rs;
+                ss_local = fmaf(a[i], a[i], fmaf(b[i], b[i], ss_local));
+            }
+            epi_ok = true;
+        } else if (lane == 0) {
+            atomicOr(p.status, kErrWaitSoftmax);
+        }
+        if (HD == 256) ss_ex[r] = ss_local;
+    }
+
+    // hd = 256: the two halves of a head exchange their partial sums of squares
+    if constexpr (HD == 256) {
+        __syncwarp();
+        cluster_sync_all();
+    }
+
+    if (warp >= 2 && epi_ok) {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int t = m0 + r;
+        float ss = ss_local;
+        if constexpr (HD == 256)
+            ss += dsmem_ld_f32(dsmem_map(smem_u32(&ss_ex[r]), cluster_ctarank() ^ 1u));
+        const float rn = rsqrtf(ss / (float)HD + p.eps);
+        const int nq = p.nh, nkh = p.nkv;
+        const int kind = head < nq ? 0 : head < nq + nkh ? 1 : 2;   // q, k, v
+        const int hh = kind == 0 ? head : kind == 1 ? head - nq : head - nq - nkh;
+        if (t < p.T) {
+            // v-hat: the weightless, un-roped norm (of the k projection when v is not projected)
+            if (kind == 2 || (kind == 1 && p.kv_shared)) {
+                float va[64], vb[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) { va[i] = a[i] * rn; vb[i] = b[i] * rn; }
+                __half *vrow = p.vh + ((size_t)hh * p.S + p.ctx + t) * HD;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint4 wa, wb;
+                    uint32_t *pa = reinterpret_cast<uint32_t *>(&wa);
+                    uint32_t *pb = reinterpret_cast<uint32_t *>(&wb);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 ha = __floats2half2_rn(va[8 * u + 2 * e], va[8 * u + 2 * e + 1]);
+                        const __half2 hb = __floats2half2_rn(vb[8 * u + 2 * e], vb[8 * u + 2 * e + 1]);
+                        pa[e] = *reinterpret_cast<const uint32_t *>(&ha);
+                        pb[e] = *reinterpret_cast<const uint32_t *>(&hb);
+                    }
+                    reinterpret_cast<uint4 *>(vrow + c0)[u] = wa;
+                    reinterpret_cast<uint4 *>(vrow + c0 + HD / 2)[u] = wb;
+                }
+            }
+            if (kind < 2) {
+                // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (c0 + i, c0 + hd/2 + i)
+                const float *w = kind == 0 ? p.wq_norm : p.wk_norm;
+                const float *cs = p.cos_sin + (size_t)t * 2 * HD;
+                const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;   // q in log2 units
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    float ya = a[i] * rn, yb = b[i] * rn;
+                    if (w) {
+                        ya *= w[c0 + i];
+                        yb *= w[c0 + HD / 2 + i];
+                    }
+                    const float c = cs[c0 + i], s = cs[HD + c0 + i];
+                    a[i] = fmaf(ya, c, -yb * s) * sc;
+                    b[i] = fmaf(yb, c, ya * s) * sc;
+                }
+                float ha[64], la[64];
+                if (kind == 0) {
+                    const int g = hh / p.G, R = t * p.G + hh % p.G;
+                    const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + R / kTileM) * HD * kTileM;
+                    split64(a, ha, la);
+                    store_q_rows64<HD>(p.qh + tile, R % kTileM, c0, ha);
+                    if (p.ql_interleaved) store_q_rows64<HD>(p.ql + tile, R % kTileM, c0, la);
+                    else store_bf16_row64(p.ql + ((size_t)g * p.rows_pad + R) * HD + c0, la);
+                    split64(b, ha, la);
+                    store_q_rows64<HD>(p.qh + tile, R % kTileM, c0 + HD / 2, ha);
+                    if (p.ql_interleaved) store_q_rows64<HD>(p.ql + tile, R % kTileM, c0 + HD / 2, la);
+                    else store_bf16_row64(p.ql + ((size_t)g * p.rows_pad + R) * HD + c0 + HD / 2, la);
+                } else {
+                    const size_t row = ((size_t)hh * p.S + p.ctx + t) * HD;
+                    split64(a, ha, la);
+                    store_bf16_row64(p.kh + row + c0, ha);
+                    store_bf16_row64(p.kl + row + c0, la);
+                    split64(b, ha, la);
+                    store_bf16_row64(p.kh + row + c0 + HD / 2, ha);
+                    store_bf16_row64(p.kl + row + c0 + HD / 2, la);
+                }
+            }
+        }
+    }
+
+    // no CTA leaves while its peer may still read its partial sums; TMEM is released last
+    if constexpr (HD == 256) {
+        __syncwarp();
+        cluster_sync_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tacc, 128);
+    }
+}
+
+template <int HD>
+cudaError_t launch_proj_hd(const ProjParams &p, const ProjMaps &maps, int n_tiles, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_tiles, p.rows_pad_tokens / kTileM);
+    cfg.blockDim = dim3(kProjThreads);
+    cfg.dynamicSmemBytes = kProjSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = HD == 256 ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = HD == 256 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, qkv_proj_kernel<HD>, maps, p);
+}
+
+}  // namespace
+
+cudaError_t proj_prepare_attrs()
+{
+    cudaError_t e = cudaFuncSetAttribute(qkv_proj_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kProjSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(qkv_proj_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kProjSmem);
+    return e;
+}
+
+cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s)
+{
+    hidden_prep_kernel<<<(p.T + 7) / 8, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_proj_weights(const ProjWeightParams &p, cudaStream_t s)
+{
+    const size_t n4 = (size_t)p.n_rows * p.H / 4;
+    int blocks = (int)((n4 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    proj_weights_kernel<<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_proj(const ProjParams &p, const ProjMaps &maps, int hd, int n_tiles,
+                            cudaStream_t s)
+{
+    switch (hd) {
+    case 128: return launch_proj_hd<128>(p, maps, n_tiles, s);
+    case 256: return launch_proj_hd<256>(p, maps, n_tiles, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dg

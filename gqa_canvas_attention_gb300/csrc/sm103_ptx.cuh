@@ -170,6 +170,13 @@ __device__ __forceinline__ void dsmem_st_f4(uint32_t caddr, float4 v)
                  : "memory");
 }
 
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t caddr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float2 dsmem_ld_f2(uint32_t caddr)
 {
     float2 v;

@@ -146,6 +146,7 @@ int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 #define DG_STAGE_ATTENTION 1  /* the attention kernel (tensor-core or fp32) */
 #define DG_STAGE_COMBINE   2  /* the split-KV combine kernel */
 #define DG_STAGE_CACHE     3  /* the cache conversion kernel */
+#define DG_STAGE_PROJECTION 4 /* the input norm + q/k/v projection kernels (dg_attn_forward_hidden) */
 
 /* With DG_OPT_PROFILE on: synchronise on the recorded events, then return the summed device time
  * (ms) and the count of the launches of one stage recorded since the last read of that stage
@@ -153,6 +154,31 @@ int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 int dg_attn_profile_read(dg_attn_plan *plan, int stage, double *total_ms, long long *launches);
 
 void dg_attn_plan_destroy(dg_attn_plan *plan);
+
+/* The step before the block (page, canvas_forward, attention branch): the input RMSNorm of the
+ * residual stream (`rms!(cur, ln_in)`, item DG_RMSNORM) and the q / k / v projections (`gemm!`:
+ * y = x W^T with W [n, k] as GLin stores it), on the tensor cores, with the block's first stage
+ * (qk-norm + RoPE, v-norm) fused into the projection's epilogue.
+ *
+ * dg_attn_proj_prepare stores W diag(ln_in_w) in the plan (bf16 hi/lo, like the block's other
+ * tensor-core operands), once per set of weights:
+ *   H          hidden size, a positive multiple of 64;
+ *   ln_in_w    [H] or NULL (unweighted);
+ *   wq [nh*hd, H], wk [nkv*hd, H], wv [nkv*hd, H] or NULL (no value projection: v is the raw k
+ *   projection, the page's k_eq_v layers).
+ * The weights are read on `stream`; the caller may reuse them once the stream has passed this
+ * point.  The first call (and a call with another H or another wv-NULLness) allocates the plan's
+ * projection scratch with cudaMalloc.  Needs the tensor-core path and hd 128 or 256
+ * (DG_ERR_UNSUPPORTED otherwise); DG_ERR_ARG for a bad H or a NULL wq/wk. */
+int dg_attn_proj_prepare(dg_attn_plan *plan, int H, const float *ln_in_w, const float *wq,
+                         const float *wk, const float *wv, cudaStream_t stream);
+
+/* The block from the residual stream x [T, H] (fp32): input norm, projections, first stage,
+ * attention, output as dg_attn_forward.  Cache, weights, table and out as in dg_attn_forward.
+ * DG_ERR_STATE without dg_attn_proj_prepare; DG_ERR_UNSUPPORTED on the exact path. */
+int dg_attn_forward_hidden(dg_attn_plan *plan, const float *x, const float *k_cache,
+                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                           const float *cos_sin, float *out, cudaStream_t stream);
 
 /* Allocation-free forward.  The pages have no counterpart: this entry point exists for callers
  * that cannot call cudaMalloc when they run attention (code inside a memory pool or arena it does

@@ -1,0 +1,76 @@
+"""GPU parity of the projection step before the block (dg_attn_proj_prepare +
+dg_attn_forward_hidden): input RMSNorm, q/k/v projections on the tensor cores with the block's
+first stage fused into their epilogue, then the attention block, against the fp64 oracle
+(oracle.forward_hidden) at the tensor-core tolerances (max 5e-3, mean 5e-4)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_canvas_attention_gb300 import binding as B
+from gqa_canvas_attention_gb300.workloads import EPS, ROPE_THETA, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def weights(H, nh, nkv, hd, seed, with_v=True):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float32)
+    ln = 1.0 + 0.1 * r(H)
+    wq = r(nh * hd, H) / H ** 0.5
+    wk = r(nkv * hd, H) / H ** 0.5
+    wv = r(nkv * hd, H) / H ** 0.5 if with_v else None
+    return ln, wq, wk, wv
+
+
+@pytest.mark.parametrize("shape", [(130, 700, 8, 4, 256, 512), (70, 300, 8, 2, 128, 384),
+                                   (256, 1024, 8, 4, 256, 1024)],
+                         ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d_H%d" % s)
+@pytest.mark.parametrize("with_v", [True, False], ids=["wv", "k_eq_v"])
+def test_hidden_to_output_parity(shape, with_v):
+    T, ctx, nh, nkv, hd, H = shape
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=71)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(72), dtype=torch.float32)
+    ln, wq, wk, wv = weights(H, nh, nkv, hd, 73, with_v)
+    cu = lambda t: None if t is None else t.cuda()
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.proj_prepare(H, cu(ln), cu(wq), cu(wk), cu(wv))
+    out = plan.forward_hidden(cu(x), cu(d["k_cache"]), cu(d["v_cache"]), cu(d["q_norm_w"]),
+                              cu(d["k_norm_w"]))
+    assert plan.sync_status() == B.DG_OK
+    n = lambda t: None if t is None else t.numpy()
+    rows = (0, T) if T <= 130 else (T - 40, T)
+    ref = oracle.forward_hidden(n(x), n(ln), n(wq), n(wk), n(wv), n(d["k_cache"]),
+                                n(d["v_cache"]), nh, nkv, hd, n(d["q_norm_w"]), n(d["k_norm_w"]),
+                                eps=EPS, theta=ROPE_THETA, rows=rows)
+    o = out.cpu().double().numpy()[rows[0]:rows[1]]
+    e = np.abs(o - ref[rows[0]:rows[1]])
+    print(f"max {e.max():.3e} mean {e.mean():.3e}")
+    assert np.isfinite(o).all()
+    assert e.max() <= 5e-3 and e.mean() <= 5e-4
+
+
+def test_projection_needs_prepared_weights_and_the_tensor_core_path():
+    T, ctx, nh, nkv, hd, H = 8, 16, 2, 1, 128, 64
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    x = torch.zeros(T, H, device="cuda")
+    with pytest.raises(B.DgAttnError) as e:
+        plan.forward_hidden(x)
+    assert e.value.status == B.DG_ERR_STATE
+    with pytest.raises(B.DgAttnError) as e:
+        plan.proj_prepare(100, None, torch.zeros(nh * hd, 100, device="cuda"),
+                          torch.zeros(nkv * hd, 100, device="cuda"))
+    assert e.value.status == B.DG_ERR_ARG
+    p64 = B.Plan(nh, nkv, 64, ctx, T, EPS, ROPE_THETA)
+    with pytest.raises(B.DgAttnError) as e:
+        p64.proj_prepare(H, None, torch.zeros(nh * 64, H, device="cuda"),
+                         torch.zeros(nkv * 64, H, device="cuda"))
+    assert e.value.status == B.DG_ERR_UNSUPPORTED
+    assert plan.sync_status() == B.DG_OK
