@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--hidden", type=int, default=0,
+                    help="run each forward from a residual stream of this width through the "
+                         "projection step (input norm + q/k/v projections) instead of from q/k/v")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the 48 forwards one by one instead of replaying a CUDA graph")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
@@ -264,13 +267,30 @@ def main():
         plan.set(B.DG_OPT_SPLITS, args.splits)
     splits = plan.get(B.DG_INFO_SPLITS_USED)
 
+    hid = None
+    if args.hidden:
+        # residual-stream inputs [T, H] per forward and one set of projection weights
+        # (1/sqrt(H)-scaled normals, so the projections are O(1) like the q/k/v draws)
+        H = args.hidden
+        g = torch.Generator().manual_seed(1000 + w.seed)
+        r = lambda *sh: torch.randn(*sh, generator=g, dtype=torch.float32)
+        ln = (1.0 + 0.1 * r(H)).to(dev)
+        wq, wk, wv = (r(w.nh * w.hd, H) / H ** 0.5).to(dev), (r(w.nkv * w.hd, H) / H ** 0.5).to(dev), \
+            (r(w.nkv * w.hd, H) / H ** 0.5).to(dev)
+        plan.proj_prepare(H, ln, wq, wk, wv)
+        hid = [r(w.T, H).to(dev) for _ in canv]
+        del wq, wk, wv
+
     def one_step():
         """One canvas: cache conversion once, then every denoising step's forward."""
         if w.ctx > 0:
             plan.cache_prepare(kc, vc)
-        for c in canv:
-            plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
-                         c["k_norm_w"], None, out)
+        for i, c in enumerate(canv):
+            if hid is not None:
+                plan.forward_hidden(hid[i], None, None, c["q_norm_w"], c["k_norm_w"], None, out)
+            else:
+                plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
+                             c["k_norm_w"], None, out)
 
     for _ in range(max(3, args.warmup)):
         one_step()
@@ -331,6 +351,7 @@ def main():
     norm_ms, norm_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_NORM_ROPE)
     comb_ms, comb_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_COMBINE)
     cache_ms, cache_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_CACHE)
+    proj_ms, proj_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_PROJECTION)
     plan.set(B.DG_OPT_PROFILE, 0)
     del graph
     rec_steps = max(1, attn_n // n_fwd)      # steps whose launches the record holds
@@ -347,7 +368,8 @@ def main():
     attn_tflops = flops_fwd / attn_avg_s / 1e12
     norm_bytes = 2 * 4 * w.T * (w.nh + 2 * w.nkv) * w.hd     # fp32 in + 4 bytes out per element
     norm_avg_s = norm_ms / max(1, norm_n) / 1e3
-    norm_gbs = norm_bytes / norm_avg_s / 1e9
+    norm_gbs = norm_bytes / norm_avg_s / 1e9 if norm_n else 0.0   # no first-stage launch on the
+                                                                    # projection path (fused)
 
     # ---------------------------------------------------------------- end to end from host memory
     # Each forward's canvas goes host -> device and its output device -> host through pinned
@@ -355,7 +377,7 @@ def main():
     # forwards on the compute stream, double-buffered and ordered by events, so the transfers of
     # forward i+1 and i-1 overlap the kernels of forward i (as a serving loop would run them).
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not args.hidden:
         pin = lambda t: None if t is None else t.cpu().pin_memory()
         h_kc, h_vc = pin(kc), pin(vc)
         h_canv = [{k: pin(v) for k, v in c.items()} for c in canv]
@@ -431,7 +453,8 @@ def main():
                "ms_per_step": ems / args.e2e_steps,
                "overlap": "copies on two streams, double-buffered against the forwards"}
 
-    launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * plan.get(B.DG_INFO_LAUNCHES)
+    launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (plan.get(B.DG_INFO_LAUNCHES)
+                                                           + (1 if args.hidden else 0))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
@@ -459,6 +482,17 @@ def main():
         "stage_ms_per_step": {k: v / rec_steps for k, v in (("norm_rope", norm_ms),
                               ("attention", attn_ms), ("combine", comb_ms), ("cache", cache_ms))},
         "gpu_launches": launches_per_step * args.steps,
+        "projection": None if not args.hidden else {
+            "H": args.hidden, "bound": "tensor",
+            "useful_gflop_per_launch": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd / 1e9,
+            "avg_launch_us": proj_ms / max(1, proj_n) * 1e3,
+            "achieved": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd
+                        / (proj_ms / max(1, proj_n) / 1e3) / 1e12,
+            "unit": "TFLOP/s", "peak": tf32_peak,
+            "frac": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd
+                    / (proj_ms / max(1, proj_n) / 1e3) / 1e12 / tf32_peak,
+            "note": "input norm + q/k/v projections with the first stage fused (two launches), "
+                    "useful fp32-GEMM FLOPs; the step's value then includes this work"},
         "e2e": e2e,
         "clocks": clk.summary(),
     }
