@@ -144,6 +144,74 @@ __device__ __forceinline__ void store_q_rows64(__nv_bfloat16 *tile_base, int r, 
     }
 }
 
+// ---- the bf16x3 split GEMM main loop shared by the two projection kernels ----
+// D[128 x 128] (TMEM, fp32) = sum over H of A_hi B_hi + A_hi B_lo + A_lo B_hi, A rows m0..m0+127
+// of maps.xh / maps.xl, B rows brow0..brow0+63 and brow1..brow1+63 of maps.wh / maps.wl, in
+// 64-wide steps of the contraction through a kProjStages ring.
+
+// TMA producer (one thread): returns false when a wait ran out.
+__device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
+                                               const ProjMaps &maps, int m0, int brow0, int brow1,
+                                               int nk, uint64_t limit)
+{
+    bool ok = true;
+    int issued[kProjStages] = {};
+    for (int it = 0; it < nk; ++it) {
+        const int s = it % kProjStages;
+        if (it >= kProjStages && !mbar_wait_bounded(&empty[s], ((it / kProjStages) - 1) & 1, limit)) {
+            ok = false;
+            break;
+        }
+        uint8_t *st = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tma_load_3d(st, &maps.xh, &full[s], it * 64, m0, 0);
+        tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], it * 64, m0, 0);
+        tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], it * 64, brow0, 0);
+        tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], it * 64, brow1, 0);
+        tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], it * 64, brow0, 0);
+        tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], it * 64, brow1, 0);
+        ++issued[s];
+    }
+    // let every load issued here land before the CTA can exit
+    for (int s = 0; s < kProjStages; ++s)
+        if (issued[s] > 0) mbar_wait_bounded(&full[s], (issued[s] - 1) & 1, limit);
+    return ok;
+}
+
+// MMA issuer (one thread): accumulates into tacc, signals acc_full; drains before returning.
+// Returns a DG status bit, or 0.
+__device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
+                                                  uint64_t *acc_full, uint64_t *drain,
+                                                  uint32_t tacc, int nk, uint64_t limit)
+{
+    constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, 128);
+    const uint64_t d0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+    uint32_t err = 0;
+    bool ok = true;
+    for (int it = 0; ok && it < nk; ++it) {
+        const int s = it % kProjStages;
+        if (!mbar_wait_bounded(&full[s], (it / kProjStages) & 1, limit)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t base = d0 + (uint64_t)((s * kStageBytes) >> 4);
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+            const uint64_t ah = base + (uint64_t)((sub * 32) >> 4);
+            const uint64_t al = base + (uint64_t)((kPanelBytes + sub * 32) >> 4);
+            const uint64_t bh = base + (uint64_t)((2 * kPanelBytes + sub * 32) >> 4);
+            const uint64_t bl = base + (uint64_t)((3 * kPanelBytes + sub * 32) >> 4);
+            mma_bf16_ss(tacc, ah, bh, idesc, (it > 0 || sub > 0) ? 1u : 0u);
+            mma_bf16_ss(tacc, ah, bl, idesc, 1u);
+            mma_bf16_ss(tacc, al, bh, idesc, 1u);
+        }
+        mma_commit(&empty[s]);
+    }
+    if (ok) mma_commit(acc_full);
+    else err |= kErrWaitMma;
+    mma_commit(drain);      // no tcgen05 operation of this thread may still run when TMEM goes
+    if (!mbar_wait_bounded(drain, 0, limit)) err |= kErrWaitDrain;
+    return err;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kProjThreads, 1)
 qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
@@ -194,59 +262,13 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     bool epi_ok = false;
 
     if (warp == 0) {
-        if (lane == 0) {
-            bool ok = true;
-            int issued[kProjStages] = {};
-            for (int it = 0; it < nk; ++it) {
-                const int s = it % kProjStages;
-                if (it >= kProjStages &&
-                    !mbar_wait_bounded(&empty[s], ((it / kProjStages) - 1) & 1, limit)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *st = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
-                tma_load_3d(st, &maps.xh, &full[s], it * 64, m0, 0);
-                tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], it * 64, m0, 0);
-                tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], it * 64, g0 * 64, 0);
-                tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], it * 64,
-                            g1 * 64, 0);
-                tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], it * 64, g0 * 64, 0);
-                tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], it * 64,
-                            g1 * 64, 0);
-                ++issued[s];
-            }
-            if (!ok) atomicOr(p.status, kErrWaitProducer);
-            for (int s = 0; s < kProjStages; ++s)
-                if (issued[s] > 0) mbar_wait_bounded(&full[s], (issued[s] - 1) & 1, limit);
-        }
+        if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, g0 * 64, g1 * 64, nk, limit))
+            atomicOr(p.status, kErrWaitProducer);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, 128);
-            const uint64_t d0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
-            bool ok = true;
-            for (int it = 0; ok && it < nk; ++it) {
-                const int s = it % kProjStages;
-                if (!mbar_wait_bounded(&full[s], (it / kProjStages) & 1, limit)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t base = d0 + (uint64_t)((s * kStageBytes) >> 4);
-#pragma unroll
-                for (int sub = 0; sub < 4; ++sub) {
-                    const uint64_t ah = base + (uint64_t)((sub * 32) >> 4);
-                    const uint64_t al = base + (uint64_t)((kPanelBytes + sub * 32) >> 4);
-                    const uint64_t bh = base + (uint64_t)((2 * kPanelBytes + sub * 32) >> 4);
-                    const uint64_t bl = base + (uint64_t)((3 * kPanelBytes + sub * 32) >> 4);
-                    mma_bf16_ss(tacc, ah, bh, idesc, (it > 0 || sub > 0) ? 1u : 0u);
-                    mma_bf16_ss(tacc, ah, bl, idesc, 1u);
-                    mma_bf16_ss(tacc, al, bh, idesc, 1u);
-                }
-                mma_commit(&empty[s]);
-            }
-            if (ok) mma_commit(acc_full);
-            else atomicOr(p.status, kErrWaitMma);
-            mma_commit(drain);
-            if (!mbar_wait_bounded(drain, 0, limit)) atomicOr(p.status, kErrWaitDrain);
+            const uint32_t e = gemm_mma_loop(smem, full, empty, acc_full, drain, tacc, nk, limit);
+            if (e) atomicOr(p.status, e);
         }
         __syncwarp();
     } else {

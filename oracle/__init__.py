@@ -51,6 +51,9 @@ def _load():
         lib.dgo_rmsnorm_rows.restype = None
         lib.dgo_linear.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P]
         lib.dgo_linear.restype = None
+        lib.dgo_oproj_residual.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P,
+                                           ctypes.c_double, ctypes.c_double, P, P]
+        lib.dgo_oproj_residual.restype = None
         lib.dgo_set_threads.argtypes = [ctypes.c_int]
         lib.dgo_set_threads.restype = ctypes.c_int
         _lib = lib
@@ -191,3 +194,18 @@ def forward_hidden(x, ln_in_w, wq, wk, wv, k_cache, v_cache, nh: int, nkv: int, 
     f = lambda a: a.astype(np.float32)
     return forward(f(q), f(k), f(v), k_cache, v_cache, nh, nkv, hd, q_norm_w, k_norm_w,
                    cos_sin=cos_sin, eps=eps, theta=theta, pos0=pos0, rows=rows)
+
+
+def oproj_residual(attn, wo, ln_post_w, resid, eps: float = 1e-6, scale: float = 1.0):
+    """The residual stream after the attention branch: (resid + RMSNorm(attn Wo^T) w) * scale,
+    attn [T, k], Wo [h, k], w [h] or None, resid [T, h] (all fp32).  fp64 [T, h]."""
+    attn = _f32(attn)
+    rows, k = attn.shape
+    wo = _f32(wo)
+    h = wo.shape[0]
+    assert wo.shape[1] == k
+    resid = _f32(resid).reshape(rows, h)
+    out = np.empty((rows, h), dtype=np.float64)
+    _load().dgo_oproj_residual(_ptr(attn), rows, k, _ptr(wo), h, _ptr(_f32(ln_post_w)),
+                               float(eps), float(scale), _ptr(resid), _ptr(out))
+    return out

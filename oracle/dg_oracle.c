@@ -224,6 +224,33 @@ void dgo_linear(const double *xhat, int rows, int k, const float *W, int n, doub
     }
 }
 
+/* The step after the block (canvas_forward, attention branch): `gemm!(&sb, &l.o, t_len, &nb)`
+ * (o_proj, y = attn W_o^T with W_o [h, nh*hd]), `rms!(&nb, &l.ln_post_attn, 1, &sb)` (weighted
+ * RMSNorm of the projection, item DG_RMSNORM) and `add_scale!(&cur, &sb, 1.0)` (item DG_ADD_SCALE:
+ * cur = (cur + sb) * 1.0).  attn [rows, k] fp32, Wo [h, k], w [h] or NULL, resid [rows, h] fp32;
+ * out [rows, h] fp64 = the updated residual stream. */
+void dgo_oproj_residual(const float *attn, int rows, int k, const float *Wo, int h,
+                        const float *w, double eps, double scale, const float *resid, double *out)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)rows * k);
+    double *y = (double *)malloc(sizeof(double) * (size_t)rows * h);
+    for (size_t i = 0; i < (size_t)rows * k; ++i) a[i] = (double)attn[i];
+    dgo_linear(a, rows, k, Wo, h, y);
+    for (int r = 0; r < rows; ++r) {
+        const double *yr = y + (size_t)r * h;
+        double ss = 0.0;
+        for (int i = 0; i < h; ++i) ss += yr[i] * yr[i];
+        double inv = 1.0 / sqrt(ss / (double)h + eps);
+        for (int i = 0; i < h; ++i) {
+            double v = yr[i] * inv;
+            if (w) v *= (double)w[i];
+            out[(size_t)r * h + i] = ((double)resid[(size_t)r * h + i] + v) * scale;
+        }
+    }
+    free(a);
+    free(y);
+}
+
 /* Thread control for the timed CPU baseline (1 when built without OpenMP). */
 int dgo_set_threads(int n)
 {

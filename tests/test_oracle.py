@@ -399,3 +399,43 @@ def test_projection_brute_force_with_fsum():
         for j in range(n):
             ref = math.fsum(xr[i] * float(W[j, i]) for i in range(h))
             assert abs(q[r, j] - ref) <= 1e-12 * (1.0 + abs(ref))
+
+
+# ---------------------------------------------------------------- o_proj + post-attention norm + residual
+# (canvas_forward: gemm!(sb, o) then rms!(nb, ln_post_attn) then add_scale!(cur, sb, 1.0))
+
+def test_oproj_residual_hand_example():
+    """attn = [1, 2], Wo = [[1, 0], [0, 1], [1, 1]]: y = [1, 2, 3], mean y^2 = 14/3, so the update
+    is y / sqrt(14/3) (eps = 0, no weight) added to the residual.  Catches: the norm over the
+    input instead of the projection, a missing residual, transposed Wo."""
+    attn = np.array([[1.0, 2.0]], np.float32)
+    wo = np.array([[1, 0], [0, 1], [1, 1]], np.float32)
+    resid = np.array([[10.0, 20.0, 30.0]], np.float32)
+    out = oracle.oproj_residual(attn, wo, None, resid, eps=0.0)
+    s = math.sqrt(14.0 / 3.0)
+    np.testing.assert_allclose(out[0], [10 + 1 / s, 20 + 2 / s, 30 + 3 / s], rtol=1e-14)
+
+
+def test_oproj_residual_is_scale_free_in_the_attention_output():
+    """The post-attention RMSNorm removes any positive scale of the projected vector (eps = 0), and
+    the weight multiplies the normalised update.  Catches: weight inside the mean, no norm."""
+    k, h = 12, 20
+    attn, wo, resid, w = rnd(3, k), rnd(h, k), rnd(3, h), 1.0 + 0.2 * rnd(h)
+    o1 = oracle.oproj_residual(attn, wo, w, resid, eps=0.0)
+    o2 = oracle.oproj_residual((5.0 * attn).astype(np.float32), wo, w, resid, eps=0.0)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12)
+    upd = o1 - resid.astype(np.float64)
+    np.testing.assert_allclose(((upd / w.astype(np.float64)) ** 2).mean(axis=1), 1.0, rtol=1e-12)
+
+
+def test_oproj_residual_brute_force_with_fsum():
+    k, h, rows = 9, 11, 2
+    attn, wo, resid, w = rnd(rows, k), rnd(h, k), rnd(rows, h), 1.0 + 0.1 * rnd(h)
+    eps = 1e-2
+    out = oracle.oproj_residual(attn, wo, w, resid, eps=eps)
+    for r in range(rows):
+        y = [math.fsum(float(attn[r, i]) * float(wo[j, i]) for i in range(k)) for j in range(h)]
+        inv = 1.0 / math.sqrt(math.fsum(v * v for v in y) / h + eps)
+        for j in range(h):
+            ref = float(resid[r, j]) + y[j] * inv * float(w[j])
+            assert abs(out[r, j] - ref) <= 1e-12 * (1.0 + abs(ref))
