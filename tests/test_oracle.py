@@ -422,7 +422,7 @@ def test_oproj_residual_is_scale_free_in_the_attention_output():
     k, h = 12, 20
     attn, wo, resid, w = rnd(3, k), rnd(h, k), rnd(3, h), 1.0 + 0.2 * rnd(h)
     o1 = oracle.oproj_residual(attn, wo, w, resid, eps=0.0)
-    o2 = oracle.oproj_residual((5.0 * attn).astype(np.float32), wo, w, resid, eps=0.0)
+    o2 = oracle.oproj_residual((8.0 * attn).astype(np.float32), wo, w, resid, eps=0.0)
     np.testing.assert_allclose(o2, o1, rtol=1e-12)
     upd = o1 - resid.astype(np.float64)
     np.testing.assert_allclose(((upd / w.astype(np.float64)) ** 2).mean(axis=1), 1.0, rtol=1e-12)
