@@ -26,6 +26,7 @@ DG_STAGE_PROJECTION = 4
 EXPORTED = [
     "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare",
     "dg_attn_cache_prepare_typed", "dg_attn_proj_prepare", "dg_attn_forward_hidden",
+    "dg_attn_oproj_prepare", "dg_attn_oproj_residual", "dg_attn_forward_layer",
     "dg_attn_norm_rope",
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
@@ -62,6 +63,12 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_proj_prepare.restype = I
     lib.dg_attn_forward_hidden.argtypes = [P] * 9
     lib.dg_attn_forward_hidden.restype = I
+    lib.dg_attn_oproj_prepare.argtypes = [P, I, P, P, P]
+    lib.dg_attn_oproj_prepare.restype = I
+    lib.dg_attn_oproj_residual.argtypes = [P, P, P, P]
+    lib.dg_attn_oproj_residual.restype = I
+    lib.dg_attn_forward_layer.argtypes = [P] * 8
+    lib.dg_attn_forward_layer.restype = I
     lib.dg_attn_norm_rope.argtypes = [P] * 11
     lib.dg_attn_norm_rope.restype = I
     lib.dg_attn_attend.argtypes = [P] * 8
@@ -154,6 +161,23 @@ def dg_attn_forward_hidden(plan, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_si
     _check(load().dg_attn_forward_hidden(plan, _ptr(x), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(q_norm_w), _ptr(k_norm_w), _ptr(cos_sin), _ptr(out),
                                          _stream(stream)), "dg_attn_forward_hidden")
+
+
+def dg_attn_oproj_prepare(plan, H, wo, ln_post_w=None, stream=None):
+    _check(load().dg_attn_oproj_prepare(plan, int(H), _ptr(wo), _ptr(ln_post_w), _stream(stream)),
+           "dg_attn_oproj_prepare")
+
+
+def dg_attn_oproj_residual(plan, attn_out, resid, stream=None):
+    _check(load().dg_attn_oproj_residual(plan, _ptr(attn_out), _ptr(resid), _stream(stream)),
+           "dg_attn_oproj_residual")
+
+
+def dg_attn_forward_layer(plan, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                          stream=None):
+    _check(load().dg_attn_forward_layer(plan, _ptr(resid), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(q_norm_w), _ptr(k_norm_w), _ptr(cos_sin),
+                                        _stream(stream)), "dg_attn_forward_layer")
 
 
 def dg_attn_cache_prepare_typed(plan, k_cache, v_cache, dtype, stream=None):
@@ -257,6 +281,18 @@ class Plan:
         dg_attn_forward_hidden(self.handle, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out,
                                stream)
         return out
+
+    def oproj_prepare(self, H, wo, ln_post_w=None, stream=None):
+        dg_attn_oproj_prepare(self.handle, H, wo, ln_post_w, stream)
+
+    def oproj_residual(self, attn_out, resid, stream=None):
+        dg_attn_oproj_residual(self.handle, attn_out, resid, stream)
+
+    def forward_layer(self, resid, k_cache=None, v_cache=None, q_norm_w=None, k_norm_w=None,
+                      cos_sin=None, stream=None):
+        dg_attn_forward_layer(self.handle, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                              stream)
+        return resid
 
     def cache_prepare(self, k_cache, v_cache, stream=None):
         """fp32, float16 or bfloat16 cache tensors [nkv, ctx, hd] (both of one dtype)."""

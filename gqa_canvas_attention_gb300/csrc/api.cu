@@ -119,6 +119,15 @@ struct dg_attn_plan {
     __nv_bfloat16 *xh, *xl;         // [T_pad, H] the residual stream, bf16 hi / lo
     float *rin;                     // [T] input-norm scale
     dg::ProjMaps pmaps;
+    // o_proj step (dg_attn_oproj_prepare / dg_attn_oproj_residual / dg_attn_forward_layer)
+    int oH;                         // hidden size W_o was prepared for
+    bool oproj_ready, has_ln_post;
+    __nv_bfloat16 *woh, *wol;       // [oH, nh*hd] W_o, bf16 hi / lo
+    __nv_bfloat16 *aoh, *aol;       // [T_pad, nh*hd] the attention output, bf16 hi / lo
+    float *ybuf, *part_ss;          // [T, oH] the projection, [T, oH/128] its partial sums
+    float *ln_post;                 // [oH] post-attention norm weight
+    float *attn_buf;                // [T, nh*hd] the block's output inside dg_attn_forward_layer
+    dg::ProjMaps omaps;
 };
 
 namespace {
@@ -137,7 +146,8 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 
 void free_scratch(dg_attn_plan *p)
 {
-    void *ptrs[] = {p->wh, p->wl, p->xh, p->xl, p->rin, p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
+    void *ptrs[] = {p->woh, p->wol, p->aoh, p->aol, p->ybuf, p->part_ss, p->ln_post, p->attn_buf,
+                    p->wh, p->wl, p->xh, p->xl, p->rin, p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
                     p->kh, p->kl, p->vh, p->part_o, p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
@@ -881,6 +891,118 @@ int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache
     if (err != cudaSuccess) return cuda_fail(err, "projection launch");
     if ((rc = record_event(p, DG_STAGE_PROJECTION, s))) return rc;
     return enqueue_attention(p, k_cache, v_cache, out, s);
+}
+
+int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *ln_post_w,
+                          cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (H < 128 || H % 128 != 0) {
+        set_error("H=%d: the hidden size must be a positive multiple of 128", H);
+        return DG_ERR_ARG;
+    }
+    if (!wo) {
+        set_error("wo is required");
+        return DG_ERR_ARG;
+    }
+    if (!aligned16(wo) || (ln_post_w && !aligned16(ln_post_w))) {
+        set_error("pointers must be 16-byte aligned");
+        return DG_ERR_ALIGN;
+    }
+    static bool attrs_done = false;
+    cudaError_t err = cudaSuccess;
+    if (!attrs_done) {
+        err = dg::proj_prepare_attrs();
+        if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
+        attrs_done = true;
+    }
+    const int K = p->nh * p->hd;
+    const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
+    if (H != p->oH) {
+        void *old[] = {p->woh, p->wol, p->aoh, p->aol, p->ybuf, p->part_ss, p->ln_post, p->attn_buf};
+        for (void *x : old)
+            if (x) cudaFree(x);
+        p->woh = p->wol = p->aoh = p->aol = nullptr;
+        p->ybuf = p->part_ss = p->ln_post = p->attn_buf = nullptr;
+        p->oproj_ready = false;
+        p->oH = 0;
+        p->woh = (__nv_bfloat16 *)dalloc(p, (size_t)H * K * 2, err);
+        p->wol = (__nv_bfloat16 *)dalloc(p, (size_t)H * K * 2, err);
+        p->aoh = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * K * 2, err);
+        p->aol = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * K * 2, err);
+        p->ybuf = (float *)dalloc(p, (size_t)p->T * H * 4, err);
+        p->part_ss = (float *)dalloc(p, (size_t)p->T * (H / 128) * 4, err);
+        p->ln_post = (float *)dalloc(p, (size_t)H * 4, err);
+        p->attn_buf = (float *)dalloc(p, (size_t)p->T * K * 4, err);
+        if (err != cudaSuccess) return cuda_fail(err, "allocating the o_proj operands");
+        bool ok = true;
+        ok &= encode_3d(&p->omaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aoh, K, t_pad, 1, 64,
+                        dg::kTileM, K);
+        ok &= encode_3d(&p->omaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aol, K, t_pad, 1, 64,
+                        dg::kTileM, K);
+        ok &= encode_3d(&p->omaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->woh, K, H, 1, 64, 64, K);
+        ok &= encode_3d(&p->omaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wol, K, H, 1, 64, 64, K);
+        if (!ok) {
+            set_error("cuTensorMapEncodeTiled failed for the o_proj operands");
+            return DG_ERR_CUDA;
+        }
+        p->oH = H;
+    }
+    dg::ProjWeightParams w{wo, nullptr, nullptr, nullptr, p->woh, p->wol, H, 0, H, K};
+    err = dg::launch_proj_weights(w, s);
+    if (err == cudaSuccess && ln_post_w)
+        err = cudaMemcpyAsync(p->ln_post, ln_post_w, (size_t)H * 4, cudaMemcpyDeviceToDevice, s);
+    if (err != cudaSuccess) return cuda_fail(err, "o_proj weight preparation");
+    p->has_ln_post = ln_post_w != nullptr;
+    p->oproj_ready = true;
+    return DG_OK;
+}
+
+int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!p->oproj_ready) {
+        set_error("no o_proj weights prepared (dg_attn_oproj_prepare)");
+        return DG_ERR_STATE;
+    }
+    if (!attn_out || !resid) {
+        set_error("attn_out and resid are required");
+        return DG_ERR_ARG;
+    }
+    if (!aligned16(attn_out) || !aligned16(resid)) {
+        set_error("pointers must be 16-byte aligned");
+        return DG_ERR_ALIGN;
+    }
+    const int K = p->nh * p->hd;
+    int rc = record_event(p, DG_STAGE_PROJECTION, s);
+    if (rc) return rc;
+    dg::ProjPrepParams pp{attn_out, nullptr, p->aoh, p->aol, p->T, K, p->eps};
+    cudaError_t err = dg::launch_hidden_prep(pp, s);
+    if (err != cudaSuccess) return cuda_fail(err, "o_proj operand launch");
+    dg::OprojParams o{p->ybuf, p->part_ss, p->status,
+                      (unsigned long long)p->wait_limit_ms * 1000000ull, p->T, p->oH, K};
+    err = dg::launch_oproj(o, p->omaps, s);
+    if (err != cudaSuccess) return cuda_fail(err, "o_proj launch");
+    dg::PostNormParams n{p->ybuf, p->part_ss, p->has_ln_post ? p->ln_post : nullptr, resid, p->T,
+                         p->oH, p->oH / 128, p->eps, 1.0f};
+    err = dg::launch_post_norm(n, s);
+    if (err != cudaSuccess) return cuda_fail(err, "post-attention norm launch");
+    return record_event(p, DG_STAGE_PROJECTION, s);
+}
+
+int dg_attn_forward_layer(dg_attn_plan *p, float *resid, const float *k_cache,
+                          const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                          const float *cos_sin, cudaStream_t s)
+{
+    if (int rc = check_plan(p)) return rc;
+    if (!p->proj_ready || !p->oproj_ready || p->H != p->oH) {
+        set_error("the layer needs dg_attn_proj_prepare and dg_attn_oproj_prepare with one H");
+        return DG_ERR_STATE;
+    }
+    if (int rc = dg_attn_forward_hidden(p, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                                        p->attn_buf, s))
+        return rc;
+    return dg_attn_oproj_residual(p, p->attn_buf, resid, s);
 }
 
 int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)

@@ -102,8 +102,8 @@ struct CombineParams {
 
 // ---- the projection step before the block (proj_tc.cu) ----
 struct ProjPrepParams {            // input RMSNorm scale and the bf16 hi/lo split of x
-    const float *x;                // [T, H] residual stream
-    float *rin;                    // [T] (mean x^2 + eps)^-1/2
+    const float *x;                // [T, H] residual stream (or the attention output)
+    float *rin;                    // [T] (mean x^2 + eps)^-1/2, or null (split only)
     __nv_bfloat16 *xh, *xl;        // [T_pad, H]
     int T, H;
     float eps;
@@ -134,7 +134,25 @@ struct ProjMaps {
     CUtensorMap wh, wl;            // bf16 [n_rows][H], box {64, 64}
 };
 
+// o_proj + post-attention RMSNorm + residual add (the step after the block)
+struct OprojParams {
+    float *y;                      // [T, H] the projection, fp32
+    float *part_ss;                // [T, H/128] partial sums of squares of y per column tile
+    uint32_t *status;
+    unsigned long long wait_limit_ns;
+    int T, H, K;                   // K = nh * hd
+};
+
+struct PostNormParams {
+    const float *y, *part_ss, *w;  // w [H] or null
+    float *resid;                  // [T, H], updated in place
+    int T, H, n_tiles;
+    float eps, scale;
+};
+
 cudaError_t proj_prepare_attrs();
+cudaError_t launch_oproj(const OprojParams &p, const ProjMaps &maps, cudaStream_t s);
+cudaError_t launch_post_norm(const PostNormParams &p, cudaStream_t s);
 cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s);
 cudaError_t launch_proj_weights(const ProjWeightParams &p, cudaStream_t s);
 cudaError_t launch_qkv_proj(const ProjParams &p, const ProjMaps &maps, int hd, int n_tiles,

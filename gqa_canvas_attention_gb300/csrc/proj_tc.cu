@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) p.rin[t] = rsqrtf(ss / (float)p.H + p.eps);
+    if (lane == 0 && p.rin) p.rin[t] = rsqrtf(ss / (float)p.H + p.eps);
 }
 
 __global__ void __launch_bounds__(256) proj_weights_kernel(ProjWeightParams p)
@@ -400,6 +400,118 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     }
 }
 
+// The step after the block: y = attn W_o^T (the same split GEMM: A = the attention output, B = W_o,
+// one CTA per 128 tokens x 128 output columns), y and its partial sums of squares to memory; the
+// post-attention RMSNorm needs the whole row of H columns, so it and the residual add run in
+// post_norm_kernel.
+__global__ void __launch_bounds__(kProjThreads, 1)
+oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kProjBarOff);
+    uint64_t *full = bars;
+    uint64_t *empty = full + kProjStages;
+    uint64_t *acc_full = empty + kProjStages;
+    uint64_t *drain = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const int m0 = blockIdx.y * kTileM, n0 = blockIdx.x * 128;
+    const int nk = p.K / 64;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kProjStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        prefetch_tmap(&maps.xh);
+        prefetch_tmap(&maps.xl);
+        prefetch_tmap(&maps.wh);
+        prefetch_tmap(&maps.wl);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tacc = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, n0, n0 + 64, nk, limit))
+            atomicOr(p.status, kErrWaitProducer);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t e = gemm_mma_loop(smem, full, empty, acc_full, drain, tacc, nk, limit);
+            if (e) atomicOr(p.status, e);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int t = m0 + r;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, limit));
+        if (ok) {
+            tc_fence_after();
+            float ss = 0.f;
+            float4 *dst = reinterpret_cast<float4 *>(p.y + (size_t)t * p.H + n0);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t u[32];
+                tmem_ld32(tacc + lane_off + 32 * c, u);
+                tmem_wait_ld();
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const float4 f = make_float4(__uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
+                                                 __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
+                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
+                    if (t < p.T) dst[8 * c + v] = f;
+                }
+            }
+            if (t < p.T) p.part_ss[(size_t)t * gridDim.x + blockIdx.x] = ss;
+        } else if (lane == 0) {
+            atomicOr(p.status, kErrWaitSoftmax);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tacc, 128);
+    }
+}
+
+// resid = (resid + y (mean y^2 + eps)^-1/2 w) * scale per token row (one warp per row).
+__global__ void __launch_bounds__(256) post_norm_kernel(PostNormParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= p.T) return;
+    float ss = 0.f;
+    for (int i = lane; i < p.n_tiles; i += 32) ss += p.part_ss[(size_t)t * p.n_tiles + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rn = rsqrtf(ss / (float)p.H + p.eps);
+    const float4 *y = reinterpret_cast<const float4 *>(p.y + (size_t)t * p.H);
+    float4 *x = reinterpret_cast<float4 *>(p.resid + (size_t)t * p.H);
+    const float4 *w = reinterpret_cast<const float4 *>(p.w);
+    for (int i = lane; i < p.H / 4; i += 32) {
+        const float4 a = y[i];
+        float4 r = x[i];
+        const float4 ww = w ? w[i] : make_float4(1.f, 1.f, 1.f, 1.f);
+        r.x = (r.x + a.x * rn * ww.x) * p.scale;
+        r.y = (r.y + a.y * rn * ww.y) * p.scale;
+        r.z = (r.z + a.z * rn * ww.z) * p.scale;
+        r.w = (r.w + a.w * rn * ww.w) * p.scale;
+        x[i] = r;
+    }
+}
+
 template <int HD>
 cudaError_t launch_proj_hd(const ProjParams &p, const ProjMaps &maps, int n_tiles, cudaStream_t s)
 {
@@ -427,7 +539,23 @@ cudaError_t proj_prepare_attrs()
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(qkv_proj_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kProjSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(oproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kProjSmem);
     return e;
+}
+
+cudaError_t launch_oproj(const OprojParams &p, const ProjMaps &maps, cudaStream_t s)
+{
+    const dim3 grid(p.H / 128, (p.T + kTileM - 1) / kTileM);
+    oproj_kernel<<<grid, kProjThreads, kProjSmem, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_post_norm(const PostNormParams &p, cudaStream_t s)
+{
+    post_norm_kernel<<<(p.T + 7) / 8, 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s)

@@ -180,6 +180,29 @@ int dg_attn_forward_hidden(dg_attn_plan *plan, const float *x, const float *k_ca
                            const float *v_cache, const float *q_norm_w, const float *k_norm_w,
                            const float *cos_sin, float *out, cudaStream_t stream);
 
+/* The step after the block (page, canvas_forward, attention branch): `gemm!(sb, o)` (o_proj,
+ * y = attn W_o^T, W_o [H, nh*hd]), `rms!(nb, ln_post_attn)` (weighted RMSNorm of y, item
+ * DG_RMSNORM) and `add_scale!(cur, sb, 1.0)` (item DG_ADD_SCALE): resid = resid + RMSNorm(y) w.
+ * The product runs on the tensor cores (bf16 hi/lo split, like the projection step); the norm,
+ * which needs whole rows of H, and the residual add run in a second kernel.
+ *
+ * dg_attn_oproj_prepare stores W_o [H, nh*hd] (and ln_post_w [H], or NULL for unweighted) in the
+ * plan, once per set of weights; H a positive multiple of 128.  The first call (and a call with
+ * another H) allocates the plan's o_proj scratch with cudaMalloc.
+ * dg_attn_oproj_residual applies the step to attn_out [T, nh*hd] (fp32, e.g. dg_attn_forward's
+ * out) and updates resid [T, H] (fp32) in place.  DG_ERR_STATE without preparation. */
+int dg_attn_oproj_prepare(dg_attn_plan *plan, int H, const float *wo, const float *ln_post_w,
+                          cudaStream_t stream);
+int dg_attn_oproj_residual(dg_attn_plan *plan, const float *attn_out, float *resid,
+                           cudaStream_t stream);
+
+/* The whole attention branch of a decoder layer on the residual stream resid [T, H], in place:
+ * input norm and projections (dg_attn_proj_prepare), the block, o_proj, post-attention norm and
+ * residual add (dg_attn_oproj_prepare, same H).  The block's output is kept in the plan. */
+int dg_attn_forward_layer(dg_attn_plan *plan, float *resid, const float *k_cache,
+                          const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                          const float *cos_sin, cudaStream_t stream);
+
 /* Allocation-free forward.  The pages have no counterpart: this entry point exists for callers
  * that cannot call cudaMalloc when they run attention (code inside a memory pool or arena it does
  * not own, or a process whose device memory is reserved up front).  It computes the same block

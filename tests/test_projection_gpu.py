@@ -74,3 +74,49 @@ def test_projection_needs_prepared_weights_and_the_tensor_core_path():
                          torch.zeros(nkv * 64, H, device="cuda"))
     assert e.value.status == B.DG_ERR_UNSUPPORTED
     assert plan.sync_status() == B.DG_OK
+
+
+def test_oproj_residual_parity():
+    """o_proj + post-attention RMSNorm + residual add on the tensor cores against the oracle."""
+    T, nh, nkv, hd, H = 130, 8, 4, 256, 512
+    K = nh * hd
+    g = torch.Generator().manual_seed(81)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float32)
+    attn, wo, ln, resid = r(T, K), r(H, K) / K ** 0.5, 1.0 + 0.1 * r(H), r(T, H)
+    plan = B.Plan(nh, nkv, hd, 64, T, EPS, ROPE_THETA)
+    plan.oproj_prepare(H, wo.cuda(), ln.cuda())
+    res_d = resid.cuda()
+    plan.oproj_residual(attn.cuda(), res_d)
+    assert plan.sync_status() == B.DG_OK
+    ref = oracle.oproj_residual(attn.numpy(), wo.numpy(), ln.numpy(), resid.numpy(), eps=EPS)
+    e = np.abs(res_d.cpu().double().numpy() - ref)
+    print(f"max {e.max():.3e} mean {e.mean():.3e}")
+    assert e.max() <= 1e-4 and e.mean() <= 1e-5
+
+
+def test_attention_branch_of_a_layer_parity():
+    """The whole attention branch on the residual stream (input norm, projections, block, o_proj,
+    post-attention norm, residual add) against the oracle chain, at the block's tolerances."""
+    T, ctx, nh, nkv, hd, H = 130, 700, 8, 4, 256, 512
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=91)
+    g = torch.Generator().manual_seed(92)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float32)
+    x = r(T, H)
+    ln, wq, wk, wv = weights(H, nh, nkv, hd, 93)
+    wo, ln_post = r(H, nh * hd) / (nh * hd) ** 0.5, 1.0 + 0.1 * r(H)
+    cu = lambda t: None if t is None else t.cuda()
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.proj_prepare(H, cu(ln), cu(wq), cu(wk), cu(wv))
+    plan.oproj_prepare(H, cu(wo), cu(ln_post))
+    xd = cu(x)
+    plan.forward_layer(xd, cu(d["k_cache"]), cu(d["v_cache"]), cu(d["q_norm_w"]), cu(d["k_norm_w"]))
+    assert plan.sync_status() == B.DG_OK
+    n = lambda t: None if t is None else t.numpy()
+    attn = oracle.forward_hidden(n(x), n(ln), n(wq), n(wk), n(wv), n(d["k_cache"]),
+                                 n(d["v_cache"]), nh, nkv, hd, n(d["q_norm_w"]), n(d["k_norm_w"]),
+                                 eps=EPS, theta=ROPE_THETA)
+    ref = oracle.oproj_residual(attn.astype(np.float32), n(wo), n(ln_post), n(x), eps=EPS)
+    e = np.abs(xd.cpu().double().numpy() - ref)
+    print(f"max {e.max():.3e} mean {e.mean():.3e}")
+    assert np.isfinite(e).all()
+    assert e.max() <= 5e-3 and e.mean() <= 5e-4
