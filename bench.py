@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--hidden", type=int, default=0,
                     help="run each forward from a residual stream of this width through the "
                          "projection step (input norm + q/k/v projections) instead of from q/k/v")
+    ap.add_argument("--layer", action="store_true",
+                    help="with --hidden: the whole attention branch of a layer (projections, "
+                         "block, o_proj, post-attention norm, residual add) on the residual stream")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the 48 forwards one by one instead of replaying a CUDA graph")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
@@ -280,13 +283,18 @@ def main():
         plan.proj_prepare(H, ln, wq, wk, wv)
         hid = [r(w.T, H).to(dev) for _ in canv]
         del wq, wk, wv
+        if args.layer:
+            K = w.nh * w.hd
+            plan.oproj_prepare(H, (r(H, K) / K ** 0.5).to(dev), (1.0 + 0.1 * r(H)).to(dev))
 
     def one_step():
         """One canvas: cache conversion once, then every denoising step's forward."""
         if w.ctx > 0:
             plan.cache_prepare(kc, vc)
         for i, c in enumerate(canv):
-            if hid is not None:
+            if hid is not None and args.layer:
+                plan.forward_layer(hid[i], None, None, c["q_norm_w"], c["k_norm_w"], None)
+            elif hid is not None:
                 plan.forward_hidden(hid[i], None, None, c["q_norm_w"], c["k_norm_w"], None, out)
             else:
                 plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
@@ -352,6 +360,7 @@ def main():
     comb_ms, comb_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_COMBINE)
     cache_ms, cache_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_CACHE)
     proj_ms, proj_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_PROJECTION)
+    oproj_ms, oproj_n = B.dg_attn_profile_read(plan.handle, B.DG_STAGE_OPROJ)
     plan.set(B.DG_OPT_PROFILE, 0)
     del graph
     rec_steps = max(1, attn_n // n_fwd)      # steps whose launches the record holds
@@ -454,7 +463,8 @@ def main():
                "overlap": "copies on two streams, double-buffered against the forwards"}
 
     launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (plan.get(B.DG_INFO_LAUNCHES)
-                                                           + (1 if args.hidden else 0))
+                                                           + (1 if args.hidden else 0)
+                                                           + (3 if args.layer else 0))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
@@ -493,6 +503,17 @@ def main():
                     / (proj_ms / max(1, proj_n) / 1e3) / 1e12 / tf32_peak,
             "note": "input norm + q/k/v projections with the first stage fused (two launches), "
                     "useful fp32-GEMM FLOPs; the step's value then includes this work"},
+        "oproj": None if not args.layer else {
+            "H": args.hidden, "bound": "tensor",
+            "useful_gflop_per_launch": 2 * w.T * args.hidden * w.nh * w.hd / 1e9,
+            "avg_launch_us": oproj_ms / max(1, oproj_n) * 1e3,
+            "achieved": 2 * w.T * args.hidden * w.nh * w.hd / (oproj_ms / max(1, oproj_n) / 1e3) / 1e12,
+            "unit": "TFLOP/s", "peak": tf32_peak,
+            "frac": 2 * w.T * args.hidden * w.nh * w.hd / (oproj_ms / max(1, oproj_n) / 1e3) / 1e12
+                    / tf32_peak,
+            "note": "operand split + o_proj GEMM + post-attention norm and residual add (three "
+                    "launches), useful fp32-GEMM FLOPs"},
+        "layer_us_per_forward": ms_per_step * 1e3 / n_fwd if args.layer else None,
         "e2e": e2e,
         "clocks": clk.summary(),
     }

@@ -22,6 +22,7 @@ DG_DTYPE_F32, DG_DTYPE_F16, DG_DTYPE_BF16 = 0, 1, 2
 DG_INFO_SPLITS_USED, DG_INFO_SCRATCH_BYTES, DG_INFO_CACHE_READY, DG_INFO_LAUNCHES = 16, 17, 18, 19
 DG_STAGE_NORM_ROPE, DG_STAGE_ATTENTION, DG_STAGE_COMBINE, DG_STAGE_CACHE = 0, 1, 2, 3
 DG_STAGE_PROJECTION = 4
+DG_STAGE_OPROJ = 5
 
 EXPORTED = [
     "dg_attn_plan_create", "dg_attn_forward", "dg_attn_cache_prepare",

@@ -108,8 +108,8 @@ struct dg_attn_plan {
     float *c32k, *c32v;             // fp32 path: copy of a 16-bit cache (made on first need)
     dg::TcMaps maps;
     // profiling: per stage, pairs of events (start, stop) recorded around launches
-    std::vector<cudaEvent_t> ev[5];
-    size_t ev_used[5];
+    std::vector<cudaEvent_t> ev[6];
+    size_t ev_used[6];
     // projection step (dg_attn_proj_prepare / dg_attn_forward_hidden)
     int H;                          // hidden size the projection weights were prepared for
     int proj_rows;                  // rows of W: (nh + nkv [+ nkv]) * hd
@@ -974,7 +974,7 @@ int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid,
         return DG_ERR_ALIGN;
     }
     const int K = p->nh * p->hd;
-    int rc = record_event(p, DG_STAGE_PROJECTION, s);
+    int rc = record_event(p, DG_STAGE_OPROJ, s);
     if (rc) return rc;
     dg::ProjPrepParams pp{attn_out, nullptr, p->aoh, p->aol, p->T, K, p->eps};
     cudaError_t err = dg::launch_hidden_prep(pp, s);
@@ -987,7 +987,7 @@ int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid,
                          p->oH, p->oH / 128, p->eps, 1.0f};
     err = dg::launch_post_norm(n, s);
     if (err != cudaSuccess) return cuda_fail(err, "post-attention norm launch");
-    return record_event(p, DG_STAGE_PROJECTION, s);
+    return record_event(p, DG_STAGE_OPROJ, s);
 }
 
 int dg_attn_forward_layer(dg_attn_plan *p, float *resid, const float *k_cache,
@@ -1025,7 +1025,7 @@ int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
 int dg_attn_profile_read(dg_attn_plan *p, int stage, double *total_ms, long long *launches)
 {
     if (int rc = check_plan(p)) return rc;
-    if (!total_ms || !launches || stage < 0 || stage > 4) {
+    if (!total_ms || !launches || stage < 0 || stage > 5) {
         set_error("bad stage or NULL output pointer");
         return DG_ERR_ARG;
     }

@@ -147,6 +147,7 @@ int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 #define DG_STAGE_COMBINE   2  /* the split-KV combine kernel */
 #define DG_STAGE_CACHE     3  /* the cache conversion kernel */
 #define DG_STAGE_PROJECTION 4 /* the input norm + q/k/v projection kernels (dg_attn_forward_hidden) */
+#define DG_STAGE_OPROJ      5 /* the o_proj, post-attention norm and residual kernels */
 
 /* With DG_OPT_PROFILE on: synchronise on the recorded events, then return the summed device time
  * (ms) and the count of the launches of one stage recorded since the last read of that stage
