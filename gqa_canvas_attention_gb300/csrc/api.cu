@@ -60,7 +60,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 // 3-D tiled map over [d2][d1][d0] (rows of `row` elements, row >= d0) with a 128-byte
 // swizzle; box {b0, b1, 1}; reads outside the dims return zeros.
 bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, uint64_t d0,
-               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t row)
+               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t row,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     auto fn = get_encode_fn();
     if (!fn) return false;
@@ -69,7 +70,7 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, ui
     cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -819,14 +820,15 @@ int dg_attn_proj_prepare(dg_attn_plan *p, int H, const float *ln_in_w, const flo
         p->rin = (float *)dalloc(p, (size_t)p->T * sizeof(float), err);
         if (err != cudaSuccess) return cuda_fail(err, "allocating the projection operands");
         bool ok = true;
-        ok &= encode_3d(&p->pmaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xh, H, t_pad, 1, 64,
-                        dg::kTileM, H);
-        ok &= encode_3d(&p->pmaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xl, H, t_pad, 1, 64,
-                        dg::kTileM, H);
-        ok &= encode_3d(&p->pmaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wh, H, rows, 1, 64,
-                        64, H);
-        ok &= encode_3d(&p->pmaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wl, H, rows, 1, 64,
-                        64, H);
+        const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B;   // 32-wide steps of the contraction
+        ok &= encode_3d(&p->pmaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xh, H, t_pad, 1, 32,
+                        dg::kTileM, H, sw64);
+        ok &= encode_3d(&p->pmaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->xl, H, t_pad, 1, 32,
+                        dg::kTileM, H, sw64);
+        ok &= encode_3d(&p->pmaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wh, H, rows, 1, 32,
+                        64, H, sw64);
+        ok &= encode_3d(&p->pmaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wl, H, rows, 1, 32,
+                        64, H, sw64);
         if (!ok) {
             set_error("cuTensorMapEncodeTiled failed for the projection operands");
             return DG_ERR_CUDA;
@@ -936,12 +938,15 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
         p->attn_buf = (float *)dalloc(p, (size_t)p->T * K * 4, err);
         if (err != cudaSuccess) return cuda_fail(err, "allocating the o_proj operands");
         bool ok = true;
-        ok &= encode_3d(&p->omaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aoh, K, t_pad, 1, 64,
-                        dg::kTileM, K);
-        ok &= encode_3d(&p->omaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aol, K, t_pad, 1, 64,
-                        dg::kTileM, K);
-        ok &= encode_3d(&p->omaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->woh, K, H, 1, 64, 64, K);
-        ok &= encode_3d(&p->omaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wol, K, H, 1, 64, 64, K);
+        const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+        ok &= encode_3d(&p->omaps.xh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aoh, K, t_pad, 1, 32,
+                        dg::kTileM, K, sw64);
+        ok &= encode_3d(&p->omaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aol, K, t_pad, 1, 32,
+                        dg::kTileM, K, sw64);
+        ok &= encode_3d(&p->omaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->woh, K, H, 1, 32, 64, K,
+                        sw64);
+        ok &= encode_3d(&p->omaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wol, K, H, 1, 32, 64, K,
+                        sw64);
         if (!ok) {
             set_error("cuTensorMapEncodeTiled failed for the o_proj operands");
             return DG_ERR_CUDA;

@@ -16,20 +16,26 @@
 // (one 128-byte swizzled panel of W rows).  A CTA holds two groups whose columns are RoPE partners
 // (i and i + hd/2): hd = 128 -> one head; hd = 256 -> half a head (groups c and c + 2), the two
 // halves of a head being a cluster of 2 CTAs that exchange one partial sum of squares per token.
-// Roles: warp 0 TMA producer (3-stage ring), warp 1 MMA issuer and TMEM owner, warps 2-5
-// epilogue (thread = token row = TMEM lane).  Every mbarrier wait is bounded.
+// Roles: warp 0 TMA producer (6-stage ring), warp 1 MMA issuer and TMEM owner, warps 2-9
+// epilogue (two threads per token row = TMEM lane, each taking half of the columns).  Every
+// mbarrier wait is bounded.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
 namespace dg {
 namespace {
 
-constexpr int kProjStages = 3;
-constexpr int kProjThreads = 192;
-constexpr int kPanelBytes = kTileM * 128;                   // 128 rows x 64 bf16
+// Steps of 32 along the contraction (64-byte swizzled rows), six stages deep: with the
+// producer refilling a slot only once the MMAs that read it have completed, the ring must hold
+// enough steps ahead to cover the load latency (three 64-wide steps measured 2 kcycles a step).
+constexpr int kProjStages = 6;
+constexpr int kProjThreads = 192;                         // o_proj: producer, MMA, 4 epilogue warps
+constexpr int kQkvThreads = 320;                          // projection: producer, MMA, 8 epilogue warps
+constexpr int kStepK = 32;
+constexpr int kPanelBytes = kTileM * kStepK * 2;            // 128 rows x 32 bf16
 constexpr int kStageBytes = 4 * kPanelBytes;                // A hi, A lo, B hi, B lo
 constexpr int kProjBarOff = kProjStages * kStageBytes;
-constexpr int kProjSmem = kProjBarOff + 256 + 512 + 1024;   // barriers, sum exchange, alignment
+constexpr int kProjSmem = kProjBarOff + 256 + 1536 + 1024;  // barriers, sum exchange, alignment
 
 __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
 {
@@ -93,11 +99,12 @@ __global__ void __launch_bounds__(256) proj_weights_kernel(ProjWeightParams p)
     }
 }
 
-// 64 values (one column group of a token row) as bf16 into 128 contiguous bytes.
-__device__ __forceinline__ void store_bf16_row64(__nv_bfloat16 *dst, const float *v)
+// N values of a token row as bf16 into 2N contiguous bytes.
+template <int N>
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16 *dst, const float *v)
 {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < N / 8; ++u) {
         uint4 w;
         uint32_t *pw = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
@@ -109,12 +116,13 @@ __device__ __forceinline__ void store_bf16_row64(__nv_bfloat16 *dst, const float
     }
 }
 
-// The bf16 hi/lo split of 64 values: hi = bf16(v) (exact in fp32), lo = v - hi (rounded to bf16
+// The bf16 hi/lo split of N values: hi = bf16(v) (exact in fp32), lo = v - hi (rounded to bf16
 // when stored).
-__device__ __forceinline__ void split64(const float *v, float *hi, float *lo)
+template <int N>
+__device__ __forceinline__ void split_n(const float *v, float *hi, float *lo)
 {
 #pragma unroll
-    for (int e = 0; e < 64; e += 2) {
+    for (int e = 0; e < N; e += 2) {
         const __nv_bfloat162 h = __floats2bfloat162_rn(v[e], v[e + 1]);
         const float2 f = __bfloat1622float2(h);
         hi[e] = f.x;
@@ -125,14 +133,13 @@ __device__ __forceinline__ void split64(const float *v, float *hi, float *lo)
 }
 
 // The q operand's row-interleaved layout (see the first-stage kernel): 16-byte unit u of tile
-// row r at (tile * hd/8 + u) * 128 + r.  Writes the 8 units of 64 columns starting at c0.
-template <int HD>
-__device__ __forceinline__ void store_q_rows64(__nv_bfloat16 *tile_base, int r, int c0,
-                                               const float *v)
+// row r at (tile * hd/8 + u) * 128 + r.  Writes the N/8 units of N columns starting at c0.
+template <int N>
+__device__ __forceinline__ void store_q_rows(__nv_bfloat16 *tile_base, int r, int c0, const float *v)
 {
     uint4 *base = reinterpret_cast<uint4 *>(tile_base);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < N / 8; ++u) {
         uint4 w;
         uint32_t *pw = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
@@ -147,7 +154,7 @@ __device__ __forceinline__ void store_q_rows64(__nv_bfloat16 *tile_base, int r, 
 // ---- the bf16x3 split GEMM main loop shared by the two projection kernels ----
 // D[128 x 128] (TMEM, fp32) = sum over H of A_hi B_hi + A_hi B_lo + A_lo B_hi, A rows m0..m0+127
 // of maps.xh / maps.xl, B rows brow0..brow0+63 and brow1..brow1+63 of maps.wh / maps.wl, in
-// 64-wide steps of the contraction through a kProjStages ring.
+// kStepK-wide steps of the contraction through a kProjStages ring.
 
 // TMA producer (one thread): returns false when a wait ran out.
 __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
@@ -164,12 +171,13 @@ __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, ui
         }
         uint8_t *st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_3d(st, &maps.xh, &full[s], it * 64, m0, 0);
-        tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], it * 64, m0, 0);
-        tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], it * 64, brow0, 0);
-        tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], it * 64, brow1, 0);
-        tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], it * 64, brow0, 0);
-        tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], it * 64, brow1, 0);
+        const int k0 = it * kStepK;
+        tma_load_3d(st, &maps.xh, &full[s], k0, m0, 0);
+        tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], k0, m0, 0);
+        tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], k0, brow0, 0);
+        tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], k0, brow1, 0);
+        tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], k0, brow0, 0);
+        tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], k0, brow1, 0);
         ++issued[s];
     }
     // let every load issued here land before the CTA can exit
@@ -185,7 +193,7 @@ __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full,
                                                   uint32_t tacc, int nk, uint64_t limit)
 {
     constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, 128);
-    const uint64_t d0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+    const uint64_t d0 = smem_desc_sw64(smem_u32(smem));
     uint32_t err = 0;
     bool ok = true;
     for (int it = 0; ok && it < nk; ++it) {
@@ -194,7 +202,7 @@ __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full,
         tc_fence_after();
         const uint64_t base = d0 + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
+        for (int sub = 0; sub < kStepK / 16; ++sub) {
             const uint64_t ah = base + (uint64_t)((sub * 32) >> 4);
             const uint64_t al = base + (uint64_t)((kPanelBytes + sub * 32) >> 4);
             const uint64_t bh = base + (uint64_t)((2 * kPanelBytes + sub * 32) >> 4);
@@ -213,7 +221,7 @@ __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full,
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kProjThreads, 1)
+__global__ void __launch_bounds__(kQkvThreads, 1)
 qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -236,7 +244,7 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     const int g0 = HD == 256 ? 4 * head + (j & 1) : 2 * head;
     const int g1 = g0 + HD / 128;
     const int c0 = (g0 % (HD / 64)) * 64;                    // first column of g0 in its head
-    const int nk = p.H / 64;
+    const int nk = p.H / kStepK;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kProjStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
@@ -257,9 +265,14 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     tc_fence_after();
     const uint32_t tacc = *tmem_slot;
 
-    float a[64], b[64];          // epilogue: the token row's values of groups g0 and g1
+    // Epilogue: eight warps, two per TMEM lane quarter.  Thread (row r, half h) takes columns
+    // 32h..32h+31 of each of the two groups (RoPE partners stay in one thread).
+    constexpr int CW = 32;
+    float a[CW], b[CW];           // the token row's values of groups g0 and g1 (this half)
     float ss_local = 0.f;
     bool epi_ok = false;
+    const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
+    float *ss_part = ss_ex + kTileM;                         // [2][128] per-half partial sums
 
     if (warp == 0) {
         if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, g0 * 64, g1 * 64, nk, limit))
@@ -272,7 +285,7 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         }
         __syncwarp();
     } else {
-        // epilogue part 1: accumulator rows into registers, input-norm scale, sum of squares
+        // part 1: accumulator columns into registers, input-norm scale, partial sum of squares
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -280,21 +293,18 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         if (ok) {
             tc_fence_after();
             uint32_t u[32];
+            tmem_ld32(tacc + lane_off + CW * half, u);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(tacc + lane_off + 32 * c, u);
-                tmem_wait_ld();
+            for (int i = 0; i < CW; ++i) a[i] = __uint_as_float(u[i]);
+            tmem_ld32(tacc + lane_off + 64 + CW * half, u);
+            tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[32 * c + i] = __uint_as_float(u[i]);
-                tmem_ld32(tacc + lane_off + 64 + 32 * c, u);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) b[32 * c + i] = __uint_as_float(u[i]);
-            }
+            for (int i = 0; i < CW; ++i) b[i] = __uint_as_float(u[i]);
             const int t = m0 + r;
             const float rs = t < p.T ? p.rin[t] : 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < CW; ++i) {
                 a[i] *= rs;
                 b[i] *= rs;
                 ss_local = fmaf(a[i], a[i], fmaf(b[i], b[i], ss_local));
@@ -303,85 +313,96 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         } else if (lane == 0) {
             atomicOr(p.status, kErrWaitSoftmax);
         }
-        if (HD == 256) ss_ex[r] = ss_local;
+        ss_part[half * kTileM + r] = ss_local;
+        named_barrier_sync(1, 256);                          // the eight epilogue warps
+        if (half == 0) ss_ex[r] = ss_part[r] + ss_part[kTileM + r];
     }
 
     // hd = 256: the two halves of a head exchange their partial sums of squares
     if constexpr (HD == 256) {
         __syncwarp();
         cluster_sync_all();
+    } else {
+        __syncthreads();
     }
 
     if (warp >= 2 && epi_ok) {
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int t = m0 + r;
-        float ss = ss_local;
+        float ss = ss_ex[r];
         if constexpr (HD == 256)
             ss += dsmem_ld_f32(dsmem_map(smem_u32(&ss_ex[r]), cluster_ctarank() ^ 1u));
         const float rn = rsqrtf(ss / (float)HD + p.eps);
         const int nq = p.nh, nkh = p.nkv;
         const int kind = head < nq ? 0 : head < nq + nkh ? 1 : 2;   // q, k, v
         const int hh = kind == 0 ? head : kind == 1 ? head - nq : head - nq - nkh;
+        const int ca = c0 + CW * half, cb = ca + HD / 2;         // first columns (in the head)
         if (t < p.T) {
             // v-hat: the weightless, un-roped norm (of the k projection when v is not projected)
             if (kind == 2 || (kind == 1 && p.kv_shared)) {
-                float va[64], vb[64];
-#pragma unroll
-                for (int i = 0; i < 64; ++i) { va[i] = a[i] * rn; vb[i] = b[i] * rn; }
                 __half *vrow = p.vh + ((size_t)hh * p.S + p.ctx + t) * HD;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < CW / 8; ++u) {
                     uint4 wa, wb;
                     uint32_t *pa = reinterpret_cast<uint32_t *>(&wa);
                     uint32_t *pb = reinterpret_cast<uint32_t *>(&wb);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const __half2 ha = __floats2half2_rn(va[8 * u + 2 * e], va[8 * u + 2 * e + 1]);
-                        const __half2 hb = __floats2half2_rn(vb[8 * u + 2 * e], vb[8 * u + 2 * e + 1]);
+                        const int i = 8 * u + 2 * e;
+                        const __half2 ha = __floats2half2_rn(a[i] * rn, a[i + 1] * rn);
+                        const __half2 hb = __floats2half2_rn(b[i] * rn, b[i + 1] * rn);
                         pa[e] = *reinterpret_cast<const uint32_t *>(&ha);
                         pb[e] = *reinterpret_cast<const uint32_t *>(&hb);
                     }
-                    reinterpret_cast<uint4 *>(vrow + c0)[u] = wa;
-                    reinterpret_cast<uint4 *>(vrow + c0 + HD / 2)[u] = wb;
+                    reinterpret_cast<uint4 *>(vrow + ca)[u] = wa;
+                    reinterpret_cast<uint4 *>(vrow + cb)[u] = wb;
                 }
             }
             if (kind < 2) {
-                // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (c0 + i, c0 + hd/2 + i)
+                // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (ca + i, cb + i)
                 const float *w = kind == 0 ? p.wq_norm : p.wk_norm;
                 const float *cs = p.cos_sin + (size_t)t * 2 * HD;
                 const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;   // q in log2 units
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    float ya = a[i] * rn, yb = b[i] * rn;
+                for (int i = 0; i < CW; i += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + ca + i);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + HD + ca + i);
+                    float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
                     if (w) {
-                        ya *= w[c0 + i];
-                        yb *= w[c0 + HD / 2 + i];
+                        wa = *reinterpret_cast<const float4 *>(w + ca + i);
+                        wb = *reinterpret_cast<const float4 *>(w + cb + i);
                     }
-                    const float c = cs[c0 + i], s = cs[HD + c0 + i];
-                    a[i] = fmaf(ya, c, -yb * s) * sc;
-                    b[i] = fmaf(yb, c, ya * s) * sc;
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+                    const float ww[4] = {wa.x, wa.y, wa.z, wa.w}, vv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float ya = a[i + e] * rn * ww[e], yb = b[i + e] * rn * vv[e];
+                        a[i + e] = fmaf(ya, cc[e], -yb * sn[e]) * sc;
+                        b[i + e] = fmaf(yb, cc[e], ya * sn[e]) * sc;
+                    }
                 }
-                float ha[64], la[64];
+                float hi[CW], lo[CW];
                 if (kind == 0) {
                     const int g = hh / p.G, R = t * p.G + hh % p.G;
                     const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + R / kTileM) * HD * kTileM;
-                    split64(a, ha, la);
-                    store_q_rows64<HD>(p.qh + tile, R % kTileM, c0, ha);
-                    if (p.ql_interleaved) store_q_rows64<HD>(p.ql + tile, R % kTileM, c0, la);
-                    else store_bf16_row64(p.ql + ((size_t)g * p.rows_pad + R) * HD + c0, la);
-                    split64(b, ha, la);
-                    store_q_rows64<HD>(p.qh + tile, R % kTileM, c0 + HD / 2, ha);
-                    if (p.ql_interleaved) store_q_rows64<HD>(p.ql + tile, R % kTileM, c0 + HD / 2, la);
-                    else store_bf16_row64(p.ql + ((size_t)g * p.rows_pad + R) * HD + c0 + HD / 2, la);
+                    const size_t qrow = ((size_t)g * p.rows_pad + R) * HD;
+                    split_n<CW>(a, hi, lo);
+                    store_q_rows<CW>(p.qh + tile, R % kTileM, ca, hi);
+                    if (p.ql_interleaved) store_q_rows<CW>(p.ql + tile, R % kTileM, ca, lo);
+                    else store_bf16_row<CW>(p.ql + qrow + ca, lo);
+                    split_n<CW>(b, hi, lo);
+                    store_q_rows<CW>(p.qh + tile, R % kTileM, cb, hi);
+                    if (p.ql_interleaved) store_q_rows<CW>(p.ql + tile, R % kTileM, cb, lo);
+                    else store_bf16_row<CW>(p.ql + qrow + cb, lo);
                 } else {
                     const size_t row = ((size_t)hh * p.S + p.ctx + t) * HD;
-                    split64(a, ha, la);
-                    store_bf16_row64(p.kh + row + c0, ha);
-                    store_bf16_row64(p.kl + row + c0, la);
-                    split64(b, ha, la);
-                    store_bf16_row64(p.kh + row + c0 + HD / 2, ha);
-                    store_bf16_row64(p.kl + row + c0 + HD / 2, la);
+                    split_n<CW>(a, hi, lo);
+                    store_bf16_row<CW>(p.kh + row + ca, hi);
+                    store_bf16_row<CW>(p.kl + row + ca, lo);
+                    split_n<CW>(b, hi, lo);
+                    store_bf16_row<CW>(p.kh + row + cb, hi);
+                    store_bf16_row<CW>(p.kl + row + cb, lo);
                 }
             }
         }
@@ -420,7 +441,7 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
     const int m0 = blockIdx.y * kTileM, n0 = blockIdx.x * 128;
-    const int nk = p.K / 64;
+    const int nk = p.K / kStepK;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kProjStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
         mbar_init(acc_full, 1);
@@ -517,7 +538,7 @@ cudaError_t launch_proj_hd(const ProjParams &p, const ProjMaps &maps, int n_tile
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_tiles, p.rows_pad_tokens / kTileM);
-    cfg.blockDim = dim3(kProjThreads);
+    cfg.blockDim = dim3(kQkvThreads);
     cfg.dynamicSmemBytes = kProjSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

@@ -117,6 +117,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last()
     return pol;
 }
 
+// Barrier among `count` threads (whole warps) of the CTA on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 
 // Block until every grid this one depends on in the stream has completed and its memory
@@ -222,6 +228,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1u << 46;
     d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// The same descriptor for a K-major operand in the 64-byte swizzle (rows of 32 bf16, 8-row
+// atoms of 512 bytes: stride offset 512), layout code 4.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(512u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)4u << 61;
     return d;
 }
 
