@@ -122,6 +122,7 @@ struct dg_attn_plan {
     dg::ProjMaps pmaps;
     // o_proj step (dg_attn_oproj_prepare / dg_attn_oproj_residual / dg_attn_forward_layer)
     int oH;                         // hidden size W_o was prepared for
+    int otile;                      // o_proj output columns per CTA
     bool oproj_ready, has_ln_post;
     __nv_bfloat16 *woh, *wol;       // [oH, nh*hd] W_o, bf16 hi / lo
     __nv_bfloat16 *aoh, *aol;       // [T_pad, nh*hd] the attention output, bf16 hi / lo
@@ -899,8 +900,9 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
                           cudaStream_t s)
 {
     if (int rc = check_plan(p)) return rc;
-    if (H < 128 || H % 128 != 0) {
-        set_error("H=%d: the hidden size must be a positive multiple of 128", H);
+    const int tile = dg::oproj_tile_n(H, p->T, p->num_sms);
+    if (H < 64 || tile == 0) {
+        set_error("H=%d: the hidden size must be a positive multiple of 64", H);
         return DG_ERR_ARG;
     }
     if (!wo) {
@@ -921,6 +923,7 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
     const int K = p->nh * p->hd;
     const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
     if (H != p->oH) {
+        p->otile = tile;
         void *old[] = {p->woh, p->wol, p->aoh, p->aol, p->ybuf, p->part_ss, p->ln_post, p->attn_buf};
         for (void *x : old)
             if (x) cudaFree(x);
@@ -933,7 +936,7 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
         p->aoh = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * K * 2, err);
         p->aol = (__nv_bfloat16 *)dalloc(p, (size_t)t_pad * K * 2, err);
         p->ybuf = (float *)dalloc(p, (size_t)p->T * H * 4, err);
-        p->part_ss = (float *)dalloc(p, (size_t)p->T * (H / 128) * 4, err);
+        p->part_ss = (float *)dalloc(p, (size_t)p->T * (H / tile) * 4, err);
         p->ln_post = (float *)dalloc(p, (size_t)H * 4, err);
         p->attn_buf = (float *)dalloc(p, (size_t)p->T * K * 4, err);
         if (err != cudaSuccess) return cuda_fail(err, "allocating the o_proj operands");
@@ -943,10 +946,10 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
                         dg::kTileM, K, sw64);
         ok &= encode_3d(&p->omaps.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->aol, K, t_pad, 1, 32,
                         dg::kTileM, K, sw64);
-        ok &= encode_3d(&p->omaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->woh, K, H, 1, 32, 64, K,
-                        sw64);
-        ok &= encode_3d(&p->omaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wol, K, H, 1, 32, 64, K,
-                        sw64);
+        ok &= encode_3d(&p->omaps.wh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->woh, K, H, 1, 32, tile,
+                        K, sw64);
+        ok &= encode_3d(&p->omaps.wl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->wol, K, H, 1, 32, tile,
+                        K, sw64);
         if (!ok) {
             set_error("cuTensorMapEncodeTiled failed for the o_proj operands");
             return DG_ERR_CUDA;
@@ -985,11 +988,11 @@ int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid,
     cudaError_t err = dg::launch_hidden_prep(pp, s);
     if (err != cudaSuccess) return cuda_fail(err, "o_proj operand launch");
     dg::OprojParams o{p->ybuf, p->part_ss, p->status,
-                      (unsigned long long)p->wait_limit_ms * 1000000ull, p->T, p->oH, K};
+                      (unsigned long long)p->wait_limit_ms * 1000000ull, p->T, p->oH, K, p->otile};
     err = dg::launch_oproj(o, p->omaps, s);
     if (err != cudaSuccess) return cuda_fail(err, "o_proj launch");
     dg::PostNormParams n{p->ybuf, p->part_ss, p->has_ln_post ? p->ln_post : nullptr, resid, p->T,
-                         p->oH, p->oH / 128, p->eps, 1.0f};
+                         p->oH, p->oH / p->otile, p->eps, 1.0f};
     err = dg::launch_post_norm(n, s);
     if (err != cudaSuccess) return cuda_fail(err, "post-attention norm launch");
     return record_event(p, DG_STAGE_OPROJ, s);

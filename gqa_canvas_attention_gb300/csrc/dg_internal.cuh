@@ -137,10 +137,11 @@ struct ProjMaps {
 // o_proj + post-attention RMSNorm + residual add (the step after the block)
 struct OprojParams {
     float *y;                      // [T, H] the projection, fp32
-    float *part_ss;                // [T, H/128] partial sums of squares of y per column tile
+    float *part_ss;                // [T, H/tile_n] partial sums of squares of y per column tile
     uint32_t *status;
     unsigned long long wait_limit_ns;
     int T, H, K;                   // K = nh * hd
+    int tile_n;                    // output columns per CTA (128, 80 or 64)
 };
 
 struct PostNormParams {
@@ -152,6 +153,7 @@ struct PostNormParams {
 
 cudaError_t proj_prepare_attrs();
 cudaError_t launch_oproj(const OprojParams &p, const ProjMaps &maps, cudaStream_t s);
+int oproj_tile_n(int H, int T, int num_sms);   // 0: H has none of the supported tile widths
 cudaError_t launch_post_norm(const PostNormParams &p, cudaStream_t s);
 cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s);
 cudaError_t launch_proj_weights(const ProjWeightParams &p, cudaStream_t s);

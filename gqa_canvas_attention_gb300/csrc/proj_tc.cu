@@ -39,14 +39,16 @@ constexpr int kProjSmem = kProjBarOff + 256 + 1536 + 1024;  // barriers, sum exc
 
 __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
 {
-    // one warp per token row: r_t and the bf16 hi/lo split of the row
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= p.T) return;
+    // one CTA per token row: r_t and the bf16 hi/lo split of the row (each thread's loads of the
+    // row are issued together)
+    __shared__ float red[8];
+    const int t = blockIdx.x;
     const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)t * p.H);
-    __nv_bfloat16 *xh = p.xh + (size_t)t * p.H, *xl = p.xl + (size_t)t * p.H;
+    uint2 *xh = reinterpret_cast<uint2 *>(p.xh + (size_t)t * p.H);
+    uint2 *xl = reinterpret_cast<uint2 *>(p.xl + (size_t)t * p.H);
     float ss = 0.f;
-    for (int i = lane; i < p.H / 4; i += 32) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < p.H / 4; i += 256) {
         const float4 v = x[i];
         ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
         const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
@@ -59,12 +61,19 @@ __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
         uh.y = *reinterpret_cast<const uint32_t *>(&h23);
         ul.x = *reinterpret_cast<const uint32_t *>(&l01);
         ul.y = *reinterpret_cast<const uint32_t *>(&l23);
-        reinterpret_cast<uint2 *>(xh)[i] = uh;
-        reinterpret_cast<uint2 *>(xl)[i] = ul;
+        xh[i] = uh;
+        xl[i] = ul;
     }
+    if (!p.rin) return;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0 && p.rin) p.rin[t] = rsqrtf(ss / (float)p.H + p.eps);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        p.rin[t] = rsqrtf(tot / (float)p.H + p.eps);
+    }
 }
 
 __global__ void __launch_bounds__(256) proj_weights_kernel(ProjWeightParams p)
@@ -159,8 +168,10 @@ __device__ __forceinline__ void store_q_rows(__nv_bfloat16 *tile_base, int r, in
 // TMA producer (one thread): returns false when a wait ran out.
 __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
                                                const ProjMaps &maps, int m0, int brow0, int brow1,
-                                               int nk, uint64_t limit)
+                                               int nk, uint64_t limit, int b_rows = 128)
 {
+    // brow1 >= 0: two boxes of 64 W rows; brow1 < 0: one box of b_rows rows from brow0
+    const uint32_t tx = 2 * kPanelBytes + 2 * (uint32_t)b_rows * kStepK * 2;
     bool ok = true;
     int issued[kProjStages] = {};
     for (int it = 0; it < nk; ++it) {
@@ -170,14 +181,16 @@ __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, ui
             break;
         }
         uint8_t *st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        mbar_arrive_expect_tx(&full[s], tx);
         const int k0 = it * kStepK;
         tma_load_3d(st, &maps.xh, &full[s], k0, m0, 0);
         tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], k0, m0, 0);
         tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], k0, brow0, 0);
-        tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], k0, brow1, 0);
         tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], k0, brow0, 0);
-        tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], k0, brow1, 0);
+        if (brow1 >= 0) {
+            tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], k0, brow1, 0);
+            tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], k0, brow1, 0);
+        }
         ++issued[s];
     }
     // let every load issued here land before the CTA can exit
@@ -188,11 +201,12 @@ __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, ui
 
 // MMA issuer (one thread): accumulates into tacc, signals acc_full; drains before returning.
 // Returns a DG status bit, or 0.
+template <int N = 128>
 __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
                                                   uint64_t *acc_full, uint64_t *drain,
                                                   uint32_t tacc, int nk, uint64_t limit)
 {
-    constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, 128);
+    constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, N);
     const uint64_t d0 = smem_desc_sw64(smem_u32(smem));
     uint32_t err = 0;
     bool ok = true;
@@ -422,9 +436,11 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
 }
 
 // The step after the block: y = attn W_o^T (the same split GEMM: A = the attention output, B = W_o,
-// one CTA per 128 tokens x 128 output columns), y and its partial sums of squares to memory; the
+// one CTA per 128 tokens x N output columns, N chosen per H so that the CTAs fill the GPU), y and
+// its partial sums of squares to memory; the
 // post-attention RMSNorm needs the whole row of H columns, so it and the residual add run in
 // post_norm_kernel.
+template <int N>
 __global__ void __launch_bounds__(kProjThreads, 1)
 oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
 {
@@ -440,7 +456,7 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
-    const int m0 = blockIdx.y * kTileM, n0 = blockIdx.x * 128;
+    const int m0 = blockIdx.y * kTileM, n0 = blockIdx.x * N;
     const int nk = p.K / kStepK;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kProjStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
@@ -462,12 +478,12 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
     const uint32_t tacc = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, n0, n0 + 64, nk, limit))
+        if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, n0, -1, nk, limit, N))
             atomicOr(p.status, kErrWaitProducer);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t e = gemm_mma_loop(smem, full, empty, acc_full, drain, tacc, nk, limit);
+            const uint32_t e = gemm_mma_loop<N>(smem, full, empty, acc_full, drain, tacc, nk, limit);
             if (e) atomicOr(p.status, e);
         }
         __syncwarp();
@@ -482,16 +498,16 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
             float ss = 0.f;
             float4 *dst = reinterpret_cast<float4 *>(p.y + (size_t)t * p.H + n0);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t u[32];
-                tmem_ld32(tacc + lane_off + 32 * c, u);
+            for (int c = 0; c < N / 16; ++c) {
+                uint32_t u[16];
+                tmem_ld16(tacc + lane_off + 16 * c, u);
                 tmem_wait_ld();
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
+                for (int v = 0; v < 4; ++v) {
                     const float4 f = make_float4(__uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
                                                  __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
                     ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
-                    if (t < p.T) dst[8 * c + v] = f;
+                    if (t < p.T) dst[4 * c + v] = f;
                 }
             }
             if (t < p.T) p.part_ss[(size_t)t * gridDim.x + blockIdx.x] = ss;
@@ -507,13 +523,12 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
     }
 }
 
-// resid = (resid + y (mean y^2 + eps)^-1/2 w) * scale per token row (one warp per row).
+// resid = (resid + y (mean y^2 + eps)^-1/2 w) * scale, one CTA per token row.
 __global__ void __launch_bounds__(256) post_norm_kernel(PostNormParams p)
 {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= p.T) return;
-    float ss = 0.f;
+    const int t = blockIdx.x;
+    float ss = 0.f;     // every warp sums the row's partial sums itself
     for (int i = lane; i < p.n_tiles; i += 32) ss += p.part_ss[(size_t)t * p.n_tiles + i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -521,7 +536,8 @@ __global__ void __launch_bounds__(256) post_norm_kernel(PostNormParams p)
     const float4 *y = reinterpret_cast<const float4 *>(p.y + (size_t)t * p.H);
     float4 *x = reinterpret_cast<float4 *>(p.resid + (size_t)t * p.H);
     const float4 *w = reinterpret_cast<const float4 *>(p.w);
-    for (int i = lane; i < p.H / 4; i += 32) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < p.H / 4; i += 256) {
         const float4 a = y[i];
         float4 r = x[i];
         const float4 ww = w ? w[i] : make_float4(1.f, 1.f, 1.f, 1.f);
@@ -561,27 +577,56 @@ cudaError_t proj_prepare_attrs()
         e = cudaFuncSetAttribute(qkv_proj_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kProjSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(oproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(oproj_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kProjSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(oproj_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kProjSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(oproj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kProjSmem);
     return e;
 }
 
+int oproj_tile_n(int H, int T, int num_sms)
+{
+    // the column tile giving the fewest waves x columns per CTA (time per CTA ~ its columns)
+    const int opts[3] = {128, 80, 64};
+    int best = 0;
+    long long best_cost = -1;
+    for (int n : opts) {
+        if (H % n) continue;
+        const long long ctas = (long long)(H / n) * ((T + kTileM - 1) / kTileM);
+        const long long cost = ((ctas + num_sms - 1) / num_sms) * n;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = n;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_oproj(const OprojParams &p, const ProjMaps &maps, cudaStream_t s)
 {
-    const dim3 grid(p.H / 128, (p.T + kTileM - 1) / kTileM);
-    oproj_kernel<<<grid, kProjThreads, kProjSmem, s>>>(maps, p);
+    const dim3 grid(p.H / p.tile_n, (p.T + kTileM - 1) / kTileM);
+    switch (p.tile_n) {
+    case 128: oproj_kernel<128><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
+    case 80: oproj_kernel<80><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
+    case 64: oproj_kernel<64><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_post_norm(const PostNormParams &p, cudaStream_t s)
 {
-    post_norm_kernel<<<(p.T + 7) / 8, 256, 0, s>>>(p);
+    post_norm_kernel<<<p.T, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s)
 {
-    hidden_prep_kernel<<<(p.T + 7) / 8, 256, 0, s>>>(p);
+    hidden_prep_kernel<<<p.T, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -188,7 +188,7 @@ int dg_attn_forward_hidden(dg_attn_plan *plan, const float *x, const float *k_ca
  * which needs whole rows of H, and the residual add run in a second kernel.
  *
  * dg_attn_oproj_prepare stores W_o [H, nh*hd] (and ln_post_w [H], or NULL for unweighted) in the
- * plan, once per set of weights; H a positive multiple of 128.  The first call (and a call with
+ * plan, once per set of weights; H a positive multiple of 64.  The first call (and a call with
  * another H) allocates the plan's o_proj scratch with cudaMalloc.
  * dg_attn_oproj_residual applies the step to attn_out [T, nh*hd] (fp32, e.g. dg_attn_forward's
  * out) and updates resid [T, H] (fp32) in place.  DG_ERR_STATE without preparation. */
