@@ -63,3 +63,15 @@ def test_noalloc_entry_point_checks_sizes_on_the_host(lib):
     assert B.dg_attn_forward_noalloc(16, 16, 64, 0, 4096, 1e-6, 1e4, -1, 16, 16, 16, None,
                                      None, None, None, None, 16, stream=0) == B.DG_ERR_ARG
     assert "scratch" in lib.dg_attn_noalloc_last_error().decode()
+
+
+def test_null_plan_is_an_argument_error_for_every_entry_point(lib):
+    """Every entry point that takes a plan checks it on the host before any CUDA call."""
+    assert lib.dg_attn_cache_prepare_typed(None, None, None, B.DG_DTYPE_F16, None) == B.DG_ERR_ARG
+    assert lib.dg_attn_proj_prepare(None, 64, None, None, None, None, None) == B.DG_ERR_ARG
+    assert lib.dg_attn_forward_hidden(None, *([None] * 8)) == B.DG_ERR_ARG
+    assert lib.dg_attn_oproj_prepare(None, 128, None, None, None) == B.DG_ERR_ARG
+    assert lib.dg_attn_oproj_residual(None, None, None, None) == B.DG_ERR_ARG
+    assert lib.dg_attn_forward_layer(None, *([None] * 7)) == B.DG_ERR_ARG
+    assert lib.dg_attn_norm_rope(None, *([None] * 10)) == B.DG_ERR_ARG
+    assert lib.dg_attn_attend(None, *([None] * 7)) == B.DG_ERR_ARG
