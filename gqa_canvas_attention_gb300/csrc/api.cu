@@ -277,7 +277,8 @@ int record_event(dg_attn_plan *p, int stage, cudaStream_t s)
 
 int build_maps(dg_attn_plan *p)
 {
-    const int nk = dg::tc_geometry(p->hd).nk;
+    const dg::TcGeom geo = dg::tc_geometry(p->hd);
+    const int nk = geo.nk;
     bool ok = true;
     ok &= encode_3d(&p->maps.ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->ql, p->hd, p->rows_pad,
                     p->nkv, 64, dg::kTileM, p->hd);
@@ -286,7 +287,7 @@ int build_maps(dg_attn_plan *p)
     ok &= encode_3d(&p->maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kl, p->hd, p->S, p->nkv,
                     64, nk, p->hd);
     ok &= encode_3d(&p->maps.vh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->vh, p->hd, p->S, p->nkv,
-                    64, nk, p->hd);
+                    64, geo.vk, p->hd);
     if (!ok) {
         set_error("cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
         return DG_ERR_CUDA;

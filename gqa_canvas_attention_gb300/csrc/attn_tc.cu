@@ -17,20 +17,25 @@
 // Roles (32 * (7 + NQI) threads):
 //   warp 0   K producer: TMA of the K hi/lo tile into a KST-deep ring (and the Q lo tile when it
 //            lives in shared memory);
-//   warp 1   P.V issuer (one thread) and TMEM owner;
+//   warp 1   P.V issuer and TMEM owner;
 //   warp 2   V producer: TMA of the fp16 V tile ([keys, hd], an MN-major operand) into a
-//            VST-deep ring;
-//   warp 3, 8.. Q.K^T issuers (one thread each).  A single thread can hand the tensor core only
-//            about one tcgen05.mma per ~60 cycles, far less than the 16-64 cycles of work in each
-//            128 x NK x 16 product, so key tiles are dealt round-robin to NQI issuers; issuer q
-//            owns the score buffers and K ring slots of the tiles j = q (mod NQI), so every
-//            mbarrier keeps a single in-order consumer;
+//            VST-deep ring of VK-key stages;
+//   warp 3, 8.. Q.K^T issuers.  Key tiles are dealt round-robin to NQI issuers; issuer q owns
+//            the score buffers and K ring slots of the tiles j = q (mod NQI), so every mbarrier
+//            keeps a single in-order consumer.
+//            An issuing warp runs its loop as a whole (warp-uniform indices and descriptors) and
+//            one elected lane issues the tcgen05 instructions: from a lone lane in a divergent
+//            branch the same 48 MMAs of a tile took ~40% longer to hand over, and at NK = 64
+//            that hand-over, not the tensor pipe, set the pace of the loop;
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to fp16, packed two per column
 //            over the start of S, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
 //            has grown by more than 15 (log2 units; so P <= 2^15 in between), and write the
 //            output.
 // TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
+// hd = 256 uses 64-key score tiles in two buffers (TMEM holds 128 columns for them): the product
+// ql.kh takes its Q lo operand from shared memory (4 KiB per k-step), so wider tiles read it
+// fewer times per key; 16- and 32-key tiles in 8 and 4 buffers were slower.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit and the CTA unwinds.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
@@ -38,19 +43,31 @@
 namespace dg {
 namespace {
 
+// A score chunk of W columns (32 or 16) from TMEM, and its fp16 probabilities (W/2 columns) back.
+template <int W> __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[W])
+{
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else tmem_ld16(taddr, r);
+}
+template <int W> __device__ __forceinline__ void tmem_st_half_chunk(uint32_t taddr, const uint32_t *r)
+{
+    if constexpr (W == 32) tmem_st16(taddr, r);
+    else tmem_st8(taddr, r);
+}
+
 template <int HD> struct Cfg;
 template <> struct Cfg<256> {
-    static constexpr int NK = 32, NSP = 4, KST = 4, VST = 2, NQI = 4;
+    static constexpr int NK = 64, VK = 32, NSP = 2, KST = 2, VST = 2, NQI = 1;
     static constexpr bool QL_TMEM = false;
     static constexpr int O_COL = 0, QH_COL = 256, QL_COL = 0, SP_COL = 384;
 };
 template <> struct Cfg<128> {
-    static constexpr int NK = 64, NSP = 4, KST = 4, VST = 4, NQI = 4;
+    static constexpr int NK = 64, VK = 64, NSP = 4, KST = 4, VST = 4, NQI = 2;
     static constexpr bool QL_TMEM = true;
     static constexpr int O_COL = 0, QH_COL = 128, QL_COL = 192, SP_COL = 256;
 };
 template <> struct Cfg<64> {
-    static constexpr int NK = 128, NSP = 3, KST = 3, VST = 3, NQI = 3;
+    static constexpr int NK = 128, VK = 128, NSP = 3, KST = 3, VST = 3, NQI = 1;
     static constexpr bool QL_TMEM = true;
     static constexpr int O_COL = 0, QH_COL = 64, QL_COL = 96, SP_COL = 128;
 };
@@ -62,7 +79,7 @@ template <int HD> struct Layout {
     static constexpr int QL_BYTES = C::QL_TMEM ? 0 : kTileM * HD * 2;
     static constexpr int KPANEL_BYTES = C::NK * 128;
     static constexpr int KSTAGE_BYTES = 2 * KPANELS * KPANEL_BYTES;   // hi + lo
-    static constexpr int VPANEL_BYTES = C::NK * 128;       // NK key rows of 64 hd values
+    static constexpr int VPANEL_BYTES = C::VK * 128;       // VK key rows of 64 hd values
     static constexpr int VSTAGE_BYTES = VPANELS * VPANEL_BYTES;
     static constexpr int K_OFF = QL_BYTES;
     static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
@@ -82,6 +99,7 @@ template <int HD> struct Layout {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(C::SP_COL + C::NSP * C::NK <= 512, "TMEM budget");
     static_assert(C::NSP % C::NQI == 0 && C::KST % C::NQI == 0, "issuer-owned buffers and slots");
+    static_assert(C::NK % C::VK == 0 && C::VK % 16 == 0, "V stages tile a score tile");
 };
 
 // log2 units: P stays <= 2^15 between rescales, inside the fp16 range (65504).  A rescale of O
@@ -91,6 +109,52 @@ template <int HD> struct Layout {
 // the subnormal range (2^-6 or less of the largest) are off by at most 2^-25 each.
 constexpr float kRescaleThreshold = 15.0f;
 constexpr float kHeadroom = 8.0f;
+
+// Rows [r0, r0 + nr) of the in-cluster merge of P partitions: out = sum_p w_p O_p with the
+// per-row weights w (already divided by the merged denominator).  The staged O rows are read
+// through distributed shared memory, whose latency is long: each thread takes U float4 columns
+// (of different rows) at once, so U * P loads are in flight per thread.
+template <int P, int HD, int THREADS, int PITCH>
+__device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int r0, int nr,
+                                                   const float *wgt, float *const *dst)
+{
+    constexpr int V4 = HD / 4;
+    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1);
+    uint32_t peer[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) peer[q] = dsmem_map(smem_base, q);
+    const int n = nr * V4;
+    for (int base = threadIdx.x; base < n; base += U * THREADS) {
+        float4 v[U][P];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int item = base + u * THREADS;
+            if (item < n) {
+                const uint32_t off = (uint32_t)(((r0 + item / V4) * PITCH + 4 * (item % V4)) * 4);
+#pragma unroll
+                for (int q = 0; q < P; ++q) v[u][q] = dsmem_ld_f4(peer[q] + off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int item = base + u * THREADS;
+            if (item >= n) continue;
+            const int i = item / V4;
+            float *d = dst[i];
+            if (!d) continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const float w = wgt[i * kMaxClusterSplits + q];
+                acc.x = fmaf(w, v[u][q].x, acc.x);
+                acc.y = fmaf(w, v[u][q].y, acc.y);
+                acc.z = fmaf(w, v[u][q].z, acc.z);
+                acc.w = fmaf(w, v[u][q].w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(d + 4 * (item % V4)) = acc;
+        }
+    }
+}
 
 template <int HD>
 __global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
@@ -198,14 +262,15 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             int issued[VST] = {};
-            for (int it = 0; it < n_local; ++it) {
+            // VK-key stages, NK/VK of them per score tile
+            for (int it = 0; it < n_local * (NK / C::VK); ++it) {
                 const int s = it % VST;
                 if (it >= VST && !mbar_wait_bounded(&v_empty[s], ((it / VST) - 1) & 1, limit)) {
                     ok = false;
                     break;
                 }
                 uint8_t *vst = smem + Lay::V_OFF + s * Lay::VSTAGE_BYTES;
-                const int key0 = (tile0 + it) * NK;
+                const int key0 = tile0 * NK + it * C::VK;
                 mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::VPANELS; ++pn)
                     tma_load_3d_hint(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64,
@@ -219,76 +284,91 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         __syncwarp();
     } else if (warp == 1 || warp == 3 || warp >= 8) {
         // ---------------------------------------------------------------- MMA issuers
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
-            constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, kTileM, HD);   // fp16, B MN-major
-            const uint32_t t_o = tbase + C::O_COL;
-            const uint32_t t_qh = tbase + C::QH_COL;
-            const uint32_t t_ql = tbase + C::QL_COL;
-            const uint32_t t_sp = tbase + C::SP_COL;
-            // Descriptors are built once; per stage / k-step only the start address moves
-            // (the 14-bit address field cannot carry: shared addresses are < 256 KiB).
-            const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + Lay::K_OFF), 16, 1024);
-            // V is MN-major: 64-wide hd panels NK rows apart (leading offset), 8-key groups 1 KiB
-            // apart (stride offset)
-            const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + Lay::V_OFF), Lay::VPANEL_BYTES, 1024);
-            const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
-            const int me = warp == 1 ? 0 : 1 + (warp == 3 ? 0 : warp - 7);   // drain slot
-            bool ok = true;
-            if (warp == 1) {
-                // P.V, in tile order: O += P_i V_i
-                for (int i = 0; ok && i < n_local; ++i) {
-                    const int b = i % NSP, vs = i % VST;
-                    if (!mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit)) { ok = false; break; }
-                    if (!mbar_wait_bounded(&v_full[vs], (i / VST) & 1, limit)) { ok = false; break; }
+        // The whole warp runs the issue loop, so tile indices and descriptors are warp-uniform
+        // values; the lane chosen by elect.sync issues every tcgen05 instruction (the same lane
+        // each time, so its commits track all of its MMAs).
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
+        constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, kTileM, HD);   // fp16, B MN-major
+        const uint32_t t_o = tbase + C::O_COL;
+        const uint32_t t_qh = tbase + C::QH_COL;
+        const uint32_t t_ql = tbase + C::QL_COL;
+        const uint32_t t_sp = tbase + C::SP_COL;
+        // Descriptors are built once; per stage / k-step only the start address moves
+        // (the 14-bit address field cannot carry: shared addresses are < 256 KiB).
+        const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + Lay::K_OFF), 16, 1024);
+        // V is MN-major: 64-wide hd panels VK rows apart (leading offset), 8-key groups 1 KiB
+        // apart (stride offset)
+        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + Lay::V_OFF), Lay::VPANEL_BYTES, 1024);
+        const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+        const int me = warp == 1 ? 0 : 1 + (warp == 3 ? 0 : warp - 7);   // drain slot
+        bool ok = true;
+        if (warp == 1) {
+            // P.V, in tile order: O += P_i V_i
+            constexpr int VPT = NK / C::VK;                 // V stages per score tile
+            for (int i = 0; ok && i < n_local; ++i) {
+                const int b = i % NSP;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit));
+                for (int h = 0; ok && h < VPT; ++h) {
+                    const int c = i * VPT + h, vs = c % VST;
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&v_full[vs], (c / VST) & 1, limit));
+                    if (!ok) break;
                     tc_fence_after();
                     const uint64_t vd = vdesc0 + (uint64_t)((vs * Lay::VSTAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < NK / 16; ++ks) {
-                        // keys 16ks..16ks+15: two 8-row groups, 2 KiB into every hd panel
+                    for (int ks = 0; ks < C::VK / 16; ++ks) {
+                        // keys 16ks..16ks+15 of the stage: two 8-row groups, 2 KiB into every
+                        // hd panel; the P columns of key 16k start at 8k
                         const uint64_t bdesc = vd + (uint64_t)((ks * 16 * 128) >> 4);
-                        mma_bf16_ts(t_o, t_sp + b * NK + ks * 8, bdesc, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+                        const int kk = h * (C::VK / 16) + ks;
+                        mma_bf16_ts_by(leader, t_o, t_sp + b * NK + kk * 8, bdesc, idesc_pv,
+                                       (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&v_empty[vs]);
-                    mma_commit(&sp_free[b]);
+                    mma_commit_by(leader, &v_empty[vs]);
                 }
-                if (ok) mma_commit(o_final);
-            } else {
-                // Q.K^T of the tiles j = q (mod NQI): S_j = qh.kh + qh.kl + ql.kh
-                const int q = warp == 3 ? 0 : warp - 7;
-                ok = mbar_wait_bounded(q_ready, 0, limit);
-                if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
-                tc_fence_after();
-                for (int j = q; ok && j < n_local; j += NQI) {
-                    const int b = j % NSP, s = j % KST;
-                    if (j >= NSP && !mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit)) { ok = false; break; }
-                    if (!mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t kd = kdesc0 + (uint64_t)((s * Lay::KSTAGE_BYTES) >> 4);
-                    const uint32_t d = t_sp + b * NK;
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const int pn = kk >> 2, sub = kk & 3;
-                        const uint64_t bh = kd + (uint64_t)((pn * Lay::KPANEL_BYTES + sub * 32) >> 4);
-                        const uint64_t bl = kd + (uint64_t)(((Lay::KPANELS + pn) * Lay::KPANEL_BYTES + sub * 32) >> 4);
-                        mma_bf16_ts(d, t_qh + kk * 8, bh, idesc_qk, kk > 0 ? 1u : 0u);
-                        mma_bf16_ts(d, t_qh + kk * 8, bl, idesc_qk, 1u);
-                        if constexpr (C::QL_TMEM) {
-                            mma_bf16_ts(d, t_ql + kk * 8, bh, idesc_qk, 1u);
-                        } else {
-                            const uint64_t ad = qdesc0 + (uint64_t)((pn * (kTileM * 128) + sub * 32) >> 4);
-                            mma_bf16_ss(d, ad, bh, idesc_qk, 1u);
-                        }
-                    }
-                    mma_commit(&k_empty[s]);
-                    mma_commit(&s_full[b]);
-                }
+                if (!ok) break;
+                mma_commit_by(leader, &sp_free[b]);
             }
-            if (!ok) atomicOr(p.status, kErrWaitMma);
-            // no tcgen05 operation of this thread may still run when TMEM is released
-            mma_commit(&drain[me]);
-            if (!mbar_wait_bounded(&drain[me], 0, limit)) atomicOr(p.status, kErrWaitDrain);
+            if (ok) mma_commit_by(leader, o_final);
+        } else {
+            // Q.K^T of the tiles j = q (mod NQI): S_j = qh.kh + qh.kl + ql.kh
+            const int q = warp == 3 ? 0 : warp - 7;
+            ok = mbar_wait_bounded(q_ready, 0, limit);
+            if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            for (int j = q; ok && j < n_local; j += NQI) {
+                const int b = j % NSP, s = j % KST;
+                if (j >= NSP) ok = mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit);
+                if (ok) ok = mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t kd = kdesc0 + (uint64_t)((s * Lay::KSTAGE_BYTES) >> 4);
+                const uint32_t d = t_sp + b * NK;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const int pn = kk >> 2, sub = kk & 3;
+                    const uint64_t bh = kd + (uint64_t)((pn * Lay::KPANEL_BYTES + sub * 32) >> 4);
+                    const uint64_t bl = kd + (uint64_t)(((Lay::KPANELS + pn) * Lay::KPANEL_BYTES + sub * 32) >> 4);
+                    mma_bf16_ts_by(leader, d, t_qh + kk * 8, bh, idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_bf16_ts_by(leader, d, t_qh + kk * 8, bl, idesc_qk, 1u);
+                    if constexpr (C::QL_TMEM) {
+                        mma_bf16_ts_by(leader, d, t_ql + kk * 8, bh, idesc_qk, 1u);
+                    } else {
+                        const uint64_t ad = qdesc0 + (uint64_t)((pn * (kTileM * 128) + sub * 32) >> 4);
+                        mma_bf16_ss_by(leader, d, ad, bh, idesc_qk, 1u);
+                    }
+                }
+                mma_commit_by(leader, &k_empty[s]);
+                mma_commit_by(leader, &s_full[b]);
+            }
         }
+        if (!ok && leader) atomicOr(p.status, kErrWaitMma);
+        // no tcgen05 operation of this warp may still run when TMEM is released
+        mma_commit_by(leader, &drain[me]);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&drain[me], 0, limit)) && leader)
+            atomicOr(p.status, kErrWaitDrain);
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
         // ---------------------------------------------------------------- softmax / epilogue
@@ -346,14 +426,15 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 const int valid = p.S - (tile0 + t) * NK;
+                constexpr int CW = NK % 32 == 0 ? 32 : 16;
 #pragma unroll 1
-                for (int c = 0; c < NK / 32; ++c) {
-                    uint32_t sr[32];
-                    tmem_ld32(tbase + lane_off + C::SP_COL + t * NK + 32 * c, sr);
+                for (int c = 0; c < NK / CW; ++c) {
+                    uint32_t sr[CW];
+                    tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + t * NK + CW * c, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
+                    for (int i = 0; i < CW; ++i)
+                        if (CW * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
                 }
             }
             if (ok && nw > 0) m_used = m0 + kHeadroom;
@@ -366,28 +447,29 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
             // NK <= 64: the whole score row stays in registers; NK = 128: the maximum is taken in
             // a first pass and the scores are read again (register budget of 320 threads)
-            constexpr int RC = NK <= 64 ? NK / 32 : 1;
-            uint32_t sr[RC][32];
+            constexpr int CW = NK % 32 == 0 ? 32 : 16;            // columns per score chunk
+            constexpr int RC = NK <= 64 ? NK / CW : 1;
+            uint32_t sr[RC][CW];
             // keys of this tile below S; only the last tile of the key range is partial, so the
             // masking branch is warp-uniform and almost never taken
             const int valid = p.S - (tile0 + it) * NK;
             float mx;
             if constexpr (NK <= 64) {
 #pragma unroll
-                for (int c = 0; c < RC; ++c) tmem_ld32(tsp + 32 * c, sr[c]);
+                for (int c = 0; c < RC; ++c) tmem_ld_chunk<CW>(tsp + CW * c, sr[c]);
                 tmem_wait_ld();
                 if (valid < NK) {
 #pragma unroll
                     for (int c = 0; c < RC; ++c)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+                        for (int i = 0; i < CW; ++i)
+                            if (CW * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
                 }
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < RC; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2)
+                    for (int i = 0; i < CW; i += 2)
                         m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[c][i]),
                                                  __uint_as_float(sr[c][i + 1]));
                 mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
@@ -458,9 +540,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             if constexpr (NK <= 64) {
 #pragma unroll
                 for (int c = 0; c < RC; ++c) {
-                    uint32_t pw[16];
+                    uint32_t pw[CW / 2];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < CW / 2; ++i) {
                         const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[c][2 * i]),
                                                                __uint_as_float(sr[c][2 * i + 1])), mm);
                         const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
@@ -468,7 +550,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         const __half2 h = __floats2half2_rn(pp.x, pp.y);
                         pw[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
-                    tmem_st16(tsp + 16 * c, pw);
+                    tmem_st_half_chunk<CW>(tsp + (CW / 2) * c, pw);
                 }
             } else {
 #pragma unroll 1
@@ -613,28 +695,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                                  : nullptr;
         }
         __syncthreads();
-        uint32_t peer[kMaxClusterSplits];
-#pragma unroll
-        for (int q = 0; q < kMaxClusterSplits; ++q) peer[q] = q < P ? dsmem_map(smem_u32(smem), q) : 0u;
-        constexpr int V4 = HD / 4;
-        for (int item = threadIdx.x; item < nr * V4; item += Lay::THREADS) {
-            const int i = item / V4, c4 = item % V4;
-            float *d = dst[i];
-            if (!d) continue;
-            const uint32_t off = (uint32_t)(((r0 + i) * Lay::STG_PITCH + 4 * c4) * 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < kMaxClusterSplits; ++q) {
-                if (q < P) {
-                    const float4 v = dsmem_ld_f4(peer[q] + off);
-                    const float w = wgt[i * kMaxClusterSplits + q];
-                    acc.x = fmaf(w, v.x, acc.x);
-                    acc.y = fmaf(w, v.y, acc.y);
-                    acc.z = fmaf(w, v.z, acc.z);
-                    acc.w = fmaf(w, v.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(d + 4 * c4) = acc;
+        const uint32_t sb = smem_u32(smem);
+        constexpr int TH = Lay::THREADS, PI = Lay::STG_PITCH;
+        switch (P) {
+        case 2: cluster_merge_rows<2, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 3: cluster_merge_rows<3, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 4: cluster_merge_rows<4, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 5: cluster_merge_rows<5, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 6: cluster_merge_rows<6, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 7: cluster_merge_rows<7, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        default: cluster_merge_rows<8, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
         }
         // no CTA leaves (or frees its shared memory) while a peer may still read it
         cluster_sync_all();
@@ -701,9 +771,9 @@ cudaError_t prepare_hd()
 TcGeom tc_geometry(int hd)
 {
     switch (hd) {
-    case 64: return {Cfg<64>::NK, Cfg<64>::QL_TMEM};
-    case 128: return {Cfg<128>::NK, Cfg<128>::QL_TMEM};
-    case 256: return {Cfg<256>::NK, Cfg<256>::QL_TMEM};
+    case 64: return {Cfg<64>::NK, Cfg<64>::VK, Cfg<64>::QL_TMEM};
+    case 128: return {Cfg<128>::NK, Cfg<128>::VK, Cfg<128>::QL_TMEM};
+    case 256: return {Cfg<256>::NK, Cfg<256>::VK, Cfg<256>::QL_TMEM};
     default: return {0, 0};
     }
 }

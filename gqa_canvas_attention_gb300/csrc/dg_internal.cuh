@@ -169,7 +169,8 @@ struct TcMaps {
 
 // Tile geometry of the tensor-core kernel for a head dimension.
 struct TcGeom {
-    int nk;        // keys per tile
+    int nk;        // keys per score tile
+    int vk;        // keys per V ring stage (divides nk)
     int ql_in_tmem;
 };
 TcGeom tc_geometry(int hd);

@@ -199,20 +199,23 @@ __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, ui
     return ok;
 }
 
-// MMA issuer (one thread): accumulates into tacc, signals acc_full; drains before returning.
-// Returns a DG status bit, or 0.
+// MMA issuer (a whole warp: warp-uniform loop and descriptors, one elected lane issues the
+// tcgen05 instructions): accumulates into tacc, signals acc_full; drains before returning.
+// Returns a DG status bit, or 0 (the same in every lane).
 template <int N = 128>
 __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
                                                   uint64_t *acc_full, uint64_t *drain,
                                                   uint32_t tacc, int nk, uint64_t limit)
 {
     constexpr uint32_t idesc = make_idesc(1, 0, 0, kTileM, N);
+    const uint32_t leader = elect_one_sync();
     const uint64_t d0 = smem_desc_sw64(smem_u32(smem));
     uint32_t err = 0;
     bool ok = true;
     for (int it = 0; ok && it < nk; ++it) {
         const int s = it % kProjStages;
-        if (!mbar_wait_bounded(&full[s], (it / kProjStages) & 1, limit)) { ok = false; break; }
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (it / kProjStages) & 1, limit));
+        if (!ok) break;
         tc_fence_after();
         const uint64_t base = d0 + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
@@ -221,16 +224,16 @@ __device__ __forceinline__ uint32_t gemm_mma_loop(uint8_t *smem, uint64_t *full,
             const uint64_t al = base + (uint64_t)((kPanelBytes + sub * 32) >> 4);
             const uint64_t bh = base + (uint64_t)((2 * kPanelBytes + sub * 32) >> 4);
             const uint64_t bl = base + (uint64_t)((3 * kPanelBytes + sub * 32) >> 4);
-            mma_bf16_ss(tacc, ah, bh, idesc, (it > 0 || sub > 0) ? 1u : 0u);
-            mma_bf16_ss(tacc, ah, bl, idesc, 1u);
-            mma_bf16_ss(tacc, al, bh, idesc, 1u);
+            mma_bf16_ss_by(leader, tacc, ah, bh, idesc, (it > 0 || sub > 0) ? 1u : 0u);
+            mma_bf16_ss_by(leader, tacc, ah, bl, idesc, 1u);
+            mma_bf16_ss_by(leader, tacc, al, bh, idesc, 1u);
         }
-        mma_commit(&empty[s]);
+        mma_commit_by(leader, &empty[s]);
     }
-    if (ok) mma_commit(acc_full);
+    if (ok) mma_commit_by(leader, acc_full);
     else err |= kErrWaitMma;
-    mma_commit(drain);      // no tcgen05 operation of this thread may still run when TMEM goes
-    if (!mbar_wait_bounded(drain, 0, limit)) err |= kErrWaitDrain;
+    mma_commit_by(leader, drain);   // no tcgen05 operation of this warp may still run when TMEM goes
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(drain, 0, limit))) err |= kErrWaitDrain;
     return err;
 }
 
@@ -293,10 +296,8 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             atomicOr(p.status, kErrWaitProducer);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t e = gemm_mma_loop(smem, full, empty, acc_full, drain, tacc, nk, limit);
-            if (e) atomicOr(p.status, e);
-        }
+        const uint32_t e = gemm_mma_loop(smem, full, empty, acc_full, drain, tacc, nk, limit);
+        if (e && lane == 0) atomicOr(p.status, e);
         __syncwarp();
     } else {
         // part 1: accumulator columns into registers, input-norm scale, partial sum of squares
@@ -482,10 +483,8 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
             atomicOr(p.status, kErrWaitProducer);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t e = gemm_mma_loop<N>(smem, full, empty, acc_full, drain, tacc, nk, limit);
-            if (e) atomicOr(p.status, e);
-        }
+        const uint32_t e = gemm_mma_loop<N>(smem, full, empty, acc_full, drain, tacc, nk, limit);
+        if (e && lane == 0) atomicOr(p.status, e);
         __syncwarp();
     } else {
         const int quarter = warp & 3;
