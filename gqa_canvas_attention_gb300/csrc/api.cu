@@ -176,8 +176,9 @@ int qtiles_for(const dg_attn_plan *p)
 
 // Key-range partitions: minimise (waves of CTAs) x (tiles per CTA + the fixed start-up and drain
 // cost of a CTA) + the combine kernel's cost, all in units of one key tile's time.  The
-// tensor-core figures were measured on the GB300 at hd = 256: ~0.9 us per 32-key tile and
-// ~8 us of start-up plus epilogue per CTA; the combine reads the partitions' rows once.
+// tensor-core constants (0.9 us per tile, 8 us of start-up plus epilogue per CTA) were fitted on
+// the GB300; sweeps of the partition count on the hd = 256, 128 and 64 workloads found the same
+// counts as this model.  The combine reads the partitions' rows once.
 // The tensor-core path merges 2..8 partitions inside the kernel (one cluster per query tile)
 // when such clusters fit on the GPU; other partition counts go through the combine kernel.
 bool cluster_combine(const dg_attn_plan *p, int splits)
