@@ -29,7 +29,7 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio of th
 # DRAM bytes (read + write) per launch of the tensor-core attention kernel on the bench workload,
 # from one ncu capture (profiles/attn_tc_kernel_denoise48_ctx8k.md), valid only for the kernel
 # source it was taken on: the bench reports null once attn_tc.cu has changed.
-ATTN_TRAFFIC = {"source_sha1_prefix": "405d1d758f30", "bytes": 59.77e6}
+ATTN_TRAFFIC = {"source_sha1_prefix": "56d04d207e63", "bytes": 59.96e6}
 
 
 def attn_traffic():
@@ -382,9 +382,10 @@ def main():
 
     # ---------------------------------------------------------------- end to end from host memory
     # Each forward's canvas goes host -> device and its output device -> host through pinned
-    # buffers, every step, the cache once per step.  The copies run on two copy streams and the
-    # forwards on the compute stream, double-buffered and ordered by events, so the transfers of
-    # forward i+1 and i-1 overlap the kernels of forward i (as a serving loop would run them).
+    # buffers, every step, the cache once per step.  The copies run on copy streams and the
+    # forwards on the compute stream, four buffers deep and ordered by events, so the transfers of
+    # the next and previous forwards overlap the kernels of forward i (as a serving loop would run them); the
+    # next step's cache is copied on a stream of its own while this step's forwards run.
     e2e = None
     if args.e2e_steps > 0 and not args.hidden:
         pin = lambda t: None if t is None else t.cpu().pin_memory()
@@ -392,35 +393,43 @@ def main():
         h_canv = [{k: pin(v) for k, v in c.items()} for c in canv]
         h_out = [torch.empty((w.T, w.nh * w.hd), dtype=torch.float32).pin_memory()
                  for _ in range(n_fwd)]
+        # four device buffers of canvas inputs and outputs: the link (pinned copies at ~200 GB/s
+        # one way, ~140 GB/s each way when both directions run) is nearly as busy as the GPU, so
+        # the copies get slack to absorb their jitter
+        NB = 4
         d_in = [{k: torch.empty_like(v) if v is not None else None for k, v in canv[0].items()}
-                for _ in range(2)]
-        d_out = [torch.empty_like(out) for _ in range(2)]
+                for _ in range(NB)]
+        d_out = [torch.empty_like(out) for _ in range(NB)]
         d_kc = [torch.empty_like(kc) if kc is not None else None for _ in range(2)]
         d_vc = [torch.empty_like(vc) if vc is not None else None for _ in range(2)]
         h2d = (0 if kc is None else (kc.numel() + vc.numel()) * 4)
         h2d += sum(v.numel() * 4 for v in canv[0].values() if v is not None) * n_fwd
         d2h = out.numel() * 4 * n_fwd
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_in, s_out, s_cache = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()
         ev_cache, ev_cache_free = [ev(), ev()], [ev(), ev()]
-        ev_in, ev_in_free = [ev(), ev()], [ev(), ev()]
-        ev_done, ev_out_free = [ev(), ev()], [ev(), ev()]
+        ev_in, ev_in_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
+        ev_done, ev_out_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
         counter = {"step": 0, "fwd": 0}
+
+        def cache_copy(cb):
+            # the cache of a coming step into buffer cb, once that buffer's previous prepare is done
+            with torch.cuda.stream(s_cache):
+                s_cache.wait_event(ev_cache_free[cb])
+                d_kc[cb].copy_(h_kc, non_blocking=True)
+                d_vc[cb].copy_(h_vc, non_blocking=True)
+                ev_cache[cb].record(s_cache)
 
         def e2e_step():
             cb = counter["step"] % 2
             counter["step"] += 1
             if kc is not None:
-                with torch.cuda.stream(s_in):
-                    s_in.wait_event(ev_cache_free[cb])
-                    d_kc[cb].copy_(h_kc, non_blocking=True)
-                    d_vc[cb].copy_(h_vc, non_blocking=True)
-                    ev_cache[cb].record(s_in)
                 stream.wait_event(ev_cache[cb])
                 plan.cache_prepare(d_kc[cb], d_vc[cb])
                 ev_cache_free[cb].record(stream)
+                cache_copy(cb ^ 1)                  # the next step's cache
             for i, hc in enumerate(h_canv):
-                b = counter["fwd"] % 2
+                b = counter["fwd"] % NB
                 counter["fwd"] += 1
                 with torch.cuda.stream(s_in):
                     s_in.wait_event(ev_in_free[b])
@@ -439,6 +448,8 @@ def main():
                     h_out[i].copy_(d_out[b], non_blocking=True)
                     ev_out_free[b].record(s_out)
 
+        if kc is not None:
+            cache_copy(0)
         e2e_step()
         torch.cuda.synchronize()
         if world > 1:
@@ -447,10 +458,13 @@ def main():
         e0.record(stream)
         s_in.wait_event(e0)
         s_out.wait_event(e0)
+        h0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
+        host_ms = (time.perf_counter() - h0) * 1e3 / args.e2e_steps
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
+        stream.wait_stream(s_cache)
         e1.record(stream)
         torch.cuda.synchronize()
         if plan.sync_status() != B.DG_OK:
@@ -459,8 +473,10 @@ def main():
                                             dev if world > 1 else None)
         e2e = {"value": replicas.throughput(ems, e2e_flops) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": ems / args.e2e_steps,
-               "overlap": "copies on two streams, double-buffered against the forwards"}
+               "ms_per_step": ems / args.e2e_steps, "host_enqueue_ms_per_step": host_ms,
+               "overlap": "canvas copies on two streams, four buffers deep against the "
+                          "forwards; the next step's cache copied on a third stream during this "
+                          "step"}
 
     launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (plan.get(B.DG_INFO_LAUNCHES)
                                                            + (1 if args.hidden else 0)
