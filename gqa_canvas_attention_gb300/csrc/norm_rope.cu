@@ -5,7 +5,7 @@
 //
 // One warp per (canvas token, chunk of up to 512/hd of its nh + 2*nkv heads): the warp requests
 // every row of its chunk, its norm weights and its cos/sin row before any arithmetic, then
-// normalises, rotates and stores the rows one by one.  The cos/sin rows come from a table (the
+// normalises, rotates and stores the rows, 256/hd rows per instruction.  The cos/sin rows come from a table (the
 // caller's, or the plan's, built once per set of positions by rope_table_kernel); without one each
 // lane computes those of its own elements.  Either way the angle
 // (pos0 + t) * theta^(-2i/hd) is formed in double-float (the frequency arrives as an fp64 value
@@ -14,9 +14,9 @@
 // and the leftover low part folded in with the second-order angle-addition formula around
 // CUDA's sincosf.  fp32 angles would be off by up to ~1e-3 rad at positions near 8192.
 //
-// Each lane holds hd/32 elements (float, float2, float4 or two float4); the RMS is a warp
-// shuffle reduction and the rotate-half partner of element i (i +- hd/2) is either in the same
-// lane or in lane ^ 16.
+// A row is held by hd/8 lanes, 8 elements each (elements 4l..4l+3 and hd/2+4l..hd/2+4l+3 of
+// sub-lane l), so a warp instruction covers 256/hd rows; the RMS is a shuffle reduction over the
+// row's lanes and the rotate-half partner of element i (i +- hd/2) is in the same lane.
 //
 // For the tensor-core layouts q-hat (times log2 e) and k-hat are written as bf16 hi/lo pairs and
 // v-hat as fp16, next to the cache rows of the same kv head.
@@ -26,101 +26,63 @@
 namespace dg {
 namespace {
 
+// A row of hd values is held by hd/8 consecutive lanes ("sub-lanes"), 8 values each: sub-lane l
+// holds elements 4l..4l+3 (slots 0-3) and hd/2+4l..hd/2+4l+3 (slots 4-7), so the rotate-half
+// partner of slot e is slot e^4 of the same lane, and a warp instruction covers 32/(hd/8) rows.
 template <int HD>
-struct Lane {
-    static constexpr int EPL = HD / 32;
-    // element index held in slot e of lane l
+struct Rows {
+    static constexpr int LPR = HD / 8;         // lanes per row
+    static constexpr int RPI = 32 / LPR;       // rows per warp instruction
+    static constexpr int HALF = HD / 2;
     __device__ static __forceinline__ int idx(int l, int e)
     {
-        if constexpr (HD <= 128) return l * EPL + e;
-        else return (e < 4) ? 4 * l + e : 128 + 4 * l + (e - 4);
+        return e < 4 ? 4 * l + e : HALF + 4 * l + (e - 4);
     }
-    // is slot e of lane l in the first half (i < hd/2)?
-    __device__ static __forceinline__ bool first_half(int l, int e)
+    __device__ static __forceinline__ void load(const float *row, int l, float (&x)[8])
     {
-        if constexpr (HD <= 128) return l < 16;
-        else return e < 4;
+        const float4 a = reinterpret_cast<const float4 *>(row)[l];
+        const float4 b = reinterpret_cast<const float4 *>(row + HALF)[l];
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
-    __device__ static __forceinline__ void load(const float *row, int l, float (&x)[EPL])
+    __device__ static __forceinline__ void store(float *row, int l, const float (&x)[8])
     {
-        if constexpr (HD == 32) {
-            x[0] = row[l];
-        } else if constexpr (HD == 64) {
-            float2 a = reinterpret_cast<const float2 *>(row)[l];
-            x[0] = a.x; x[1] = a.y;
-        } else if constexpr (HD == 128) {
-            float4 a = reinterpret_cast<const float4 *>(row)[l];
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        } else {
-            float4 a = reinterpret_cast<const float4 *>(row)[l];
-            float4 b = reinterpret_cast<const float4 *>(row)[32 + l];
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-        }
+        reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4 *>(row + HALF)[l] = make_float4(x[4], x[5], x[6], x[7]);
     }
-    __device__ static __forceinline__ void store(float *row, int l, const float (&x)[EPL])
-    {
-        if constexpr (HD == 32) {
-            row[l] = x[0];
-        } else if constexpr (HD == 64) {
-            reinterpret_cast<float2 *>(row)[l] = make_float2(x[0], x[1]);
-        } else if constexpr (HD == 128) {
-            reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
-        } else {
-            reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
-            reinterpret_cast<float4 *>(row)[32 + l] = make_float4(x[4], x[5], x[6], x[7]);
-        }
-    }
-    // 16-bit stores of EPL elements per lane (HD >= 64 in the tensor-core layouts)
+    // 16-bit values: 8 bytes per half row
     template <typename H, typename H2>
-    __device__ static __forceinline__ void store_16(H *row, int l, const H (&x)[EPL])
+    __device__ static __forceinline__ void store_16(H *row, int l, const H (&x)[8])
     {
-        static_assert(HD >= 64, "tensor-core layouts need hd >= 64");
-        if constexpr (HD == 64) {
-            H2 v; v.x = x[0]; v.y = x[1];
-            reinterpret_cast<H2 *>(row)[l] = v;
-        } else if constexpr (HD == 128) {
-            H2 a, b; a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
-            uint2 u; u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
-            reinterpret_cast<uint2 *>(row)[l] = u;
-        } else {
-            H2 a, b, c, d;
-            a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
-            c.x = x[4]; c.y = x[5]; d.x = x[6]; d.y = x[7];
-            uint2 u, w;
-            u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
-            w.x = *reinterpret_cast<uint32_t *>(&c); w.y = *reinterpret_cast<uint32_t *>(&d);
-            reinterpret_cast<uint2 *>(row)[l] = u;
-            reinterpret_cast<uint2 *>(row)[32 + l] = w;
-        }
+        uint2 u, w;
+        H2 a, b;
+        a.x = x[0]; a.y = x[1]; b.x = x[2]; b.y = x[3];
+        u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
+        a.x = x[4]; a.y = x[5]; b.x = x[6]; b.y = x[7];
+        w.x = *reinterpret_cast<uint32_t *>(&a); w.y = *reinterpret_cast<uint32_t *>(&b);
+        reinterpret_cast<uint2 *>(row)[l] = u;
+        reinterpret_cast<uint2 *>(row + HALF)[l] = w;
     }
 };
 
 // Q operand rows for the tensor-core kernel, "row-interleaved": 16-byte unit u (8 values) of row r
 // of 128-row tile T sits at unit index (T * (HD/8) + u) * 128 + r, so that 32 threads each
 // loading their own row read 512 contiguous bytes per instruction.  `tile` points at unit 0 of
-// the tile; lane `l` holds the elements Lane<HD>::idx(l, e).
+// the tile; sub-lane `l` holds the elements Rows<HD>::idx(l, e): two runs of 4, each half a unit.
 template <int HD>
 __device__ __forceinline__ void store_q_interleaved(__nv_bfloat16 *tile, int r, int l,
-                                                    const __nv_bfloat16 (&x)[HD / 32])
+                                                    const __nv_bfloat16 (&x)[8])
 {
-    constexpr int EPL = HD / 32;
     char *base = reinterpret_cast<char *>(tile);
-    if constexpr (HD == 64) {
-        const int i = 2 * l;                                   // elements 2l, 2l+1
-        __nv_bfloat162 v; v.x = x[0]; v.y = x[1];
-        *reinterpret_cast<__nv_bfloat162 *>(base + ((size_t)(i / 8) * 128 + r) * 16 + (i % 8) * 2) = v;
-    } else {
 #pragma unroll
-        for (int g4 = 0; g4 < EPL / 4; ++g4) {                 // runs of 4 contiguous elements
-            const int i = Lane<HD>::idx(l, 4 * g4);
-            __nv_bfloat162 a, b;
-            a.x = x[4 * g4]; a.y = x[4 * g4 + 1]; b.x = x[4 * g4 + 2]; b.y = x[4 * g4 + 3];
-            uint2 u;
-            u.x = *reinterpret_cast<uint32_t *>(&a);
-            u.y = *reinterpret_cast<uint32_t *>(&b);
-            *reinterpret_cast<uint2 *>(base + ((size_t)(i / 8) * 128 + r) * 16 + (i % 8) * 2) = u;
-        }
+    for (int g4 = 0; g4 < 2; ++g4) {
+        const int i = Rows<HD>::idx(l, 4 * g4);
+        __nv_bfloat162 a, b;
+        a.x = x[4 * g4]; a.y = x[4 * g4 + 1]; b.x = x[4 * g4 + 2]; b.y = x[4 * g4 + 3];
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a);
+        u.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(base + ((size_t)(i / 8) * 128 + r) * 16 + (i % 8) * 2) = u;
     }
 }
 
@@ -145,31 +107,30 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
     s = sd + cd * e - sd * h;
 }
 
-// Rows (heads) of one token that one warp takes: 16 elements per lane in registers (more warps,
-// each with a shorter chain of dependent instructions, measured faster than 32 or 64).
-template <int HD> constexpr int kChunkRows = 512 / HD > 0 ? 512 / HD : 1;
+// Rows (heads) of one token that one warp takes: 16 values per lane in registers, two rows per
+// lane (more warps, each with a shorter chain of dependent instructions, measured faster than 32
+// or 64 values per lane).
+template <int HD> constexpr int kChunkRows = 2 * Rows<HD>::RPI;
 
 template <int HD, int MODE>
 __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int chunks)
 {
-    using L = Lane<HD>;
-    constexpr int EPL = L::EPL;
-    constexpr int HALF = HD / 2;
-    constexpr int CH = kChunkRows<HD>;
-    // distinct frequencies per lane: with hd = 256 slots e and e + 4 share one
-    constexpr int NU = HD == 256 ? 4 : EPL;
+    using R = Rows<HD>;
+    constexpr int LPR = R::LPR, RPI = R::RPI;
+    constexpr int RG = 2;                         // rows per lane
     // The inputs may come from the kernel before this one in the stream: wait for it first,
     // unless the caller has declared them resident (then only the stores below wait, and the
     // loads and arithmetic overlap the end of the previous forward's attention kernel).
     pdl_launch_dependents();
     if (!p.inputs_resident) pdl_wait();
     const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR, rsub = lane / LPR;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int t = gw / chunks;
     if (t >= p.T) return;
     const int jobs = p.nh + 2 * p.nkv;
-    const int j0 = (gw % chunks) * CH;
-    const int nj = min(CH, jobs - j0);
+    const int j0 = (gw % chunks) * kChunkRows<HD>;
+    const int nj = min(kChunkRows<HD>, jobs - j0);
     const int G = p.nh / p.nkv;
     auto src_row = [&](int job) -> const float * {
         if (job < p.nh) return p.q + ((size_t)t * p.nh + job) * HD;
@@ -177,75 +138,75 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
         return p.v + ((size_t)t * p.nkv + (job - p.nh - p.nkv)) * HD;
     };
 
-    // every row of the chunk is requested before any arithmetic
-    float x[CH][EPL];
+    // every row of the chunk is requested before any arithmetic; lanes past the chunk's last row
+    // hold zeros (they join the shuffles, store nothing)
+    float x[RG][8];
 #pragma unroll
-    for (int r = 0; r < CH; ++r)
-        if (r < nj) L::load(src_row(j0 + r), lane, x[r]);
+    for (int g = 0; g < RG; ++g) {
+        const int r = g * RPI + rsub;
+        if (r < nj) {
+            R::load(src_row(j0 + r), sub, x[g]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[g][e] = 0.f;
+        }
+    }
 
     // the norm weights of the kinds present in the chunk (vector loads, once per warp)
-    float wq[EPL], wk[EPL];
+    float wq[8], wk[8];
     const bool has_q = j0 < p.nh, has_k = j0 < p.nh + p.nkv && j0 + nj > p.nh;
-    if (p.do_norm && p.wq && has_q) L::load(p.wq, lane, wq);
-    if (p.do_norm && p.wk && has_k) L::load(p.wk, lane, wk);
+    if (p.do_norm && p.wq && has_q) R::load(p.wq, sub, wq);
+    if (p.do_norm && p.wk && has_k) R::load(p.wk, sub, wk);
 
     // cos and sin of this lane's elements at position pos0 + t; the sine carries the sign of the
     // rotate-half partner (-x[i + hd/2] in the first half), so the rotation is two FMAs
-    float cs[EPL], sn[EPL];
+    float cs[8], sn[8];
     if (p.do_rope && (has_q || has_k)) {
         if (p.cos_sin) {
             const float *row = p.cos_sin + (size_t)t * 2 * HD;
-            L::load(row, lane, cs);
-            L::load(row + HD, lane, sn);
+            R::load(row, sub, cs);
+            R::load(row + HD, sub, sn);
         } else {
+            // slots e and e + 4 share the frequency of element 4 * sub + e
             const float pf = (float)(p.pos0 + t);
 #pragma unroll
-            for (int e = 0; e < NU; ++e)
-                rope_angle_cos_sin(pf, p.inv_freq[L::idx(lane, e) % HALF], cs[e], sn[e]);
-#pragma unroll
-            for (int e = NU; e < EPL; ++e) {
-                cs[e] = cs[e - NU];
-                sn[e] = sn[e - NU];
+            for (int e = 0; e < 4; ++e) {
+                rope_angle_cos_sin(pf, p.inv_freq[4 * sub + e], cs[e], sn[e]);
+                cs[e + 4] = cs[e];
+                sn[e + 4] = sn[e];
             }
         }
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            if (L::first_half(lane, e)) sn[e] = -sn[e];
+        for (int e = 0; e < 4; ++e) sn[e] = -sn[e];
     }
 
 #pragma unroll
-    for (int r = 0; r < CH; ++r) {
-        if (r >= nj) break;
-        const int job = j0 + r;
+    for (int g = 0; g < RG; ++g) {
+        const int job = j0 + g * RPI + rsub;
         const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
-        float *xr = x[r];
+        float *xr = x[g];
         if (p.do_norm) {
             float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) ss = fmaf(xr[e], xr[e], ss);
+            for (int e = 0; e < 8; ++e) ss = fmaf(xr[e], xr[e], ss);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             const float rn = rsqrtf(ss * (1.0f / (float)HD) + p.eps);
-            const float *w = (kind == 0 && p.wq) ? wq : (kind == 1 && p.wk) ? wk : nullptr;
-            if (w) {
+            const bool use_q = kind == 0 && p.wq, use_k = kind == 1 && p.wk;
+            if (use_q || use_k) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) xr[e] = (xr[e] * rn) * w[e];
+                for (int e = 0; e < 8; ++e) xr[e] = (xr[e] * rn) * (use_q ? wq[e] : wk[e]);
             } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) xr[e] *= rn;
+                for (int e = 0; e < 8; ++e) xr[e] *= rn;
             }
         }
         if (p.do_rope && kind != 2) {
-            float part[EPL];
-            if constexpr (HD <= 128) {
+            float part[8];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[e] = __shfl_xor_sync(0xffffffffu, xr[e], 16);
-            } else {
+            for (int e = 0; e < 8; ++e) part[e] = xr[e ^ 4];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[e] = xr[e ^ 4];
-            }
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) xr[e] = fmaf(xr[e], cs[e], part[e] * sn[e]);
+            for (int e = 0; e < 8; ++e) xr[e] = fmaf(xr[e], cs[e], part[e] * sn[e]);
         }
     }
 
@@ -253,38 +214,37 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     if (p.inputs_resident) pdl_wait();
 
 #pragma unroll
-    for (int r = 0; r < CH; ++r) {
-        if (r >= nj) break;
+    for (int g = 0; g < RG; ++g) {
+        const int r = g * RPI + rsub;
+        if (r >= nj) continue;
         const int job = j0 + r;
         const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
         const int head = kind == 0 ? job : kind == 1 ? job - p.nh : job - p.nh - p.nkv;
-        const float *xr = x[r];
+        const float *xr = x[g];
         if constexpr (MODE == kOutFp32) {
             float *dst = kind == 0 ? p.q_out + ((size_t)t * p.nh + head) * HD
                        : kind == 1 ? p.k_out + ((size_t)t * p.nkv + head) * HD
                                    : p.v_out + ((size_t)t * p.nkv + head) * HD;
-            L::store(dst, lane, x[r]);
+            R::store(dst, sub, x[g]);
         } else {
             if (kind == 2) {
-                __half v[EPL];
+                __half v[8];
 #pragma unroll
-                for (int e = 0; e + 1 < EPL; e += 2) {
+                for (int e = 0; e < 8; e += 2) {
                     const __half2 h = __floats2half2_rn(xr[e], xr[e + 1]);
                     v[e] = h.x;
                     v[e + 1] = h.y;
                 }
-                if constexpr (EPL % 2) v[EPL - 1] = __float2half_rn(xr[EPL - 1]);
-                if constexpr (HD >= 64)
-                    L::template store_16<__half, __half2>(p.vh + ((size_t)head * p.S + p.ctx + t) * HD,
-                                                          lane, v);
+                R::template store_16<__half, __half2>(p.vh + ((size_t)head * p.S + p.ctx + t) * HD,
+                                                      sub, v);
             } else {
                 // q-hat is scaled by log2(e) (one fp32 rounding) so that the tensor-core kernel
                 // gets its scores in the log2 units of its exponentials
                 const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;
                 // hi = bf16(y), lo = bf16(y - hi), two elements per conversion
-                __nv_bfloat16 hi[EPL], lo[EPL];
+                __nv_bfloat16 hi[8], lo[8];
 #pragma unroll
-                for (int e = 0; e + 1 < EPL; e += 2) {
+                for (int e = 0; e < 8; e += 2) {
                     const float y0 = xr[e] * sc, y1 = xr[e + 1] * sc;
                     const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                     const float2 hf = __bfloat1622float2(h);
@@ -292,28 +252,21 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
                     hi[e] = h.x; hi[e + 1] = h.y;
                     lo[e] = l.x; lo[e + 1] = l.y;
                 }
-                if constexpr (EPL % 2) {
-                    const float y = xr[EPL - 1] * sc;
-                    hi[EPL - 1] = __float2bfloat16_rn(y);
-                    lo[EPL - 1] = __float2bfloat16_rn(y - __bfloat162float(hi[EPL - 1]));
-                }
-                if constexpr (HD >= 64) {
-                    if (kind == 0) {
-                        // Q hi row-interleaved (the attention kernel's threads load it into
-                        // TMEM); Q lo likewise when it goes to TMEM, else row-major for TMA
-                        const int g = head / G, R = t * G + head % G;
-                        const size_t tile = ((size_t)g * (p.rows_pad / 128) + R / 128) * HD * 128;
-                        store_q_interleaved<HD>(p.qh + tile, R % 128, lane, hi);
-                        if (p.ql_interleaved)
-                            store_q_interleaved<HD>(p.ql + tile, R % 128, lane, lo);
-                        else
-                            L::template store_16<__nv_bfloat16, __nv_bfloat162>(
-                                p.ql + ((size_t)g * p.rows_pad + R) * HD, lane, lo);
-                    } else {
-                        const size_t off = ((size_t)head * p.S + p.ctx + t) * HD;
-                        L::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kh + off, lane, hi);
-                        L::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kl + off, lane, lo);
-                    }
+                if (kind == 0) {
+                    // Q hi row-interleaved (the attention kernel's threads load it into TMEM);
+                    // Q lo likewise when it goes to TMEM, else row-major for TMA
+                    const int gk = head / G, Rw = t * G + head % G;
+                    const size_t tile = ((size_t)gk * (p.rows_pad / 128) + Rw / 128) * HD * 128;
+                    store_q_interleaved<HD>(p.qh + tile, Rw % 128, sub, hi);
+                    if (p.ql_interleaved)
+                        store_q_interleaved<HD>(p.ql + tile, Rw % 128, sub, lo);
+                    else
+                        R::template store_16<__nv_bfloat16, __nv_bfloat162>(
+                            p.ql + ((size_t)gk * p.rows_pad + Rw) * HD, sub, lo);
+                } else {
+                    const size_t off = ((size_t)head * p.S + p.ctx + t) * HD;
+                    R::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kh + off, sub, hi);
+                    R::template store_16<__nv_bfloat16, __nv_bfloat162>(p.kl + off, sub, lo);
                 }
             }
         }
