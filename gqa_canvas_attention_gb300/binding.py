@@ -18,8 +18,11 @@ DG_PATH_TC, DG_PATH_FP32 = 0, 1
 DG_OPT_PATH, DG_OPT_POS0, DG_OPT_SPLITS, DG_OPT_WAIT_LIMIT_MS, DG_OPT_PROFILE = 1, 2, 3, 4, 5
 DG_OPT_INJECT_STALL = 6
 DG_OPT_INPUTS_RESIDENT = 7
+DG_OPT_SCHEDULE = 8
+DG_SCHEDULE_AUTO, DG_SCHEDULE_SPLIT, DG_SCHEDULE_STREAM_K = 0, 1, 2
 DG_DTYPE_F32, DG_DTYPE_F16, DG_DTYPE_BF16 = 0, 1, 2
 DG_INFO_SPLITS_USED, DG_INFO_SCRATCH_BYTES, DG_INFO_CACHE_READY, DG_INFO_LAUNCHES = 16, 17, 18, 19
+DG_INFO_SCHEDULE_USED = 20
 DG_STAGE_NORM_ROPE, DG_STAGE_ATTENTION, DG_STAGE_COMBINE, DG_STAGE_CACHE = 0, 1, 2, 3
 DG_STAGE_PROJECTION = 4
 DG_STAGE_OPROJ = 5

@@ -83,6 +83,7 @@ struct dg_attn_plan {
     long long pos0;
     int path;
     int splits_opt;
+    int schedule_opt;            // DG_SCHEDULE_AUTO / _SPLIT / _STREAM_K
     long long wait_limit_ms;
     int profile;
     int inject_stall;
@@ -187,7 +188,8 @@ bool cluster_combine(const dg_attn_plan *p, int splits)
            p->max_clusters[splits] > 0;
 }
 
-int auto_splits(const dg_attn_plan *p)
+// Cost of s partitions, or 1e300 when s is not a partition count that leaves none empty.
+double split_cost(const dg_attn_plan *p, int s)
 {
     const int nt = n_tiles_for(p);
     const int qt = qtiles_for(p);
@@ -197,29 +199,99 @@ int auto_splits(const dg_attn_plan *p)
     const double tile_us = tc ? 0.9 : 2.0;
     const double startup = tc ? 8.0 / tile_us : 1.0;
     const double rows = (double)qt * (tc ? dg::kTileM : dg::kFp32TileM);
+    if (s < 1 || s > nt) return 1e300;
+    const int tps = (nt + s - 1) / s;
+    const int s_eff = (nt + tps - 1) / tps;
+    if (s_eff != s) return 1e300;
+    const bool cl = cluster_combine(p, s);
+    // co-resident CTAs: whole clusters only (they are placed within one GPC each)
+    const int slots_s = cl ? std::min(slots, p->max_clusters[s] * s) : slots;
+    if (slots_s < 1) return 1e300;
+    const int waves = (qt * s + slots_s - 1) / slots_s;
+    double cost = waves * (tps + startup);
+    if (s > 1 && cl) {
+        cost += 1.5 / tile_us;                     // in-kernel merge through shared memory
+    } else if (s > 1) {
+        const double bytes = rows * p->hd * 4.0 * (s + 1);
+        cost += (3.0 + bytes / 3.0e6) / tile_us;   // launch + traffic at ~3 TB/s (bytes/us)
+    }
+    return cost;
+}
+
+int auto_splits(const dg_attn_plan *p)
+{
+    const int nt = n_tiles_for(p);
     int best = 1;
     double best_cost = 1e300;
     for (int s = 1; s <= nt && s <= 64; ++s) {
-        const int tps = (nt + s - 1) / s;
-        const int s_eff = (nt + tps - 1) / tps;
-        if (s_eff != s) continue;
-        const bool cl = cluster_combine(p, s);
-        // co-resident CTAs: whole clusters only (they are placed within one GPC each)
-        const int slots_s = cl ? std::min(slots, p->max_clusters[s] * s) : slots;
-        const int waves = (qt * s + slots_s - 1) / slots_s;
-        double cost = waves * (tps + startup);
-        if (s > 1 && cl) {
-            cost += 1.5 / tile_us;                     // in-kernel merge through shared memory
-        } else if (s > 1) {
-            const double bytes = rows * p->hd * 4.0 * (s + 1);
-            cost += (3.0 + bytes / 3.0e6) / tile_us;   // launch + traffic at ~3 TB/s (bytes/us)
-        }
+        const double cost = split_cost(p, s);
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best = s;
         }
     }
     return best;
+}
+
+// Stream-K layout of the tensor-core kernel: one CTA per SM (fewer when there are fewer key
+// tiles), at least one per (query tile, kv group) pair so that a CTA's run of key tiles covers at
+// most two pairs; kmax = the most pieces any pair is cut into (the partial slots needed).
+struct SkLayout {
+    int ctas = 0, kmax = 0;
+    long long units = 0;
+};
+
+bool sk_layout(const dg_attn_plan *p, SkLayout &L)
+{
+    if (p->path != DG_PATH_TC) return false;
+    const int nt = n_tiles_for(p);
+    const int pairs = qtiles_for(p);
+    const long long U = (long long)pairs * nt;
+    long long C = p->num_sms;
+    if (C > U) C = U;
+    // no pair in more pieces than the combine merges: fewer CTAs when the pairs are few
+    if (C > (long long)pairs * (dg::kMaxStreamKPieces - 1)) C = (long long)pairs * (dg::kMaxStreamKPieces - 1);
+    if (C < pairs) return false;
+    int kmax = 0;
+    for (;;) {
+        kmax = 0;
+        for (int pr = 0; pr < pairs; ++pr) {
+            const int k = dg::sk_cta_of((long long)(pr + 1) * nt - 1, U, (int)C) -
+                          dg::sk_cta_of((long long)pr * nt, U, (int)C) + 1;
+            if (k > kmax) kmax = k;
+        }
+        if (kmax <= dg::kMaxStreamKPieces || C <= pairs) break;
+        --C;
+    }
+    if (kmax > dg::kMaxStreamKPieces) return false;
+    L.ctas = (int)C;
+    L.units = U;
+    L.kmax = kmax;
+    return true;
+}
+
+// Cost of the stream-K schedule in the units of auto_splits (one key tile's time): the longest
+// run, the CTA's start-up, the switch between two pieces (Q reload, O written out) and the
+// combine kernel, which reads every piece once from L2.  Measured on the GB300 (hd = 256, 48-step
+// workload): the kernel 57.4 us against 62.5 us for four clustered partitions, but the combine
+// ~8 us of a forward, so the clustered split stays ahead on the workloads measured.
+double sk_cost(const dg_attn_plan *p, const SkLayout &L)
+{
+    const double tile_us = 0.9, startup = 8.0 / tile_us;
+    const double run = (double)((L.units + L.ctas - 1) / L.ctas);
+    const double pieces = (double)L.ctas + qtiles_for(p);
+    const double bytes = pieces * dg::kTileM * p->hd * 4.0 + (double)p->rows * p->nkv * p->hd * 4.0;
+    return run + startup + 2.0 + (8.0 + bytes / 8.0e6) / tile_us;   // L2 at ~8 TB/s (bytes/us)
+}
+
+// The schedule the next forward uses.
+bool use_stream_k(const dg_attn_plan *p, SkLayout &L)
+{
+    if (p->path != DG_PATH_TC || p->schedule_opt == DG_SCHEDULE_SPLIT) return false;
+    if (!sk_layout(p, L)) return false;
+    if (p->schedule_opt == DG_SCHEDULE_STREAM_K) return true;
+    if (p->splits_opt > 0) return false;           // an explicit partition count asks for splits
+    return sk_cost(p, L) < split_cost(p, auto_splits(p));
 }
 
 // Partitions actually used: the option (clamped so that none is empty) or the automatic choice.
@@ -234,9 +306,15 @@ void split_layout(const dg_attn_plan *p, int &splits, int &tiles_per_split, int 
     splits = (n_tiles + tiles_per_split - 1) / tiles_per_split;
 }
 
-int ensure_partials(dg_attn_plan *p, int splits)
+// Partial-result slots per (query tile, kv group): the split schedule needs one per partition
+// when it has two or more (a single partition writes the output itself); the stream-K schedule
+// needs kmax of them, even 1 (every piece goes through the combine).
+int split_slots(int splits) { return splits > 1 ? splits : 0; }
+
+int ensure_partials(dg_attn_plan *p, int slots)
 {
-    if (splits <= 1 || splits <= p->part_capacity) return DG_OK;
+    const int splits = slots;
+    if (splits <= 0 || splits <= p->part_capacity) return DG_OK;
     if (p->part_o) cudaFree(p->part_o);
     if (p->part_ml) cudaFree(p->part_ml);
     p->part_o = nullptr;
@@ -318,6 +396,17 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
 {
     int splits, tps, nt;
     split_layout(p, splits, tps, nt);
+    SkLayout sk;
+    const bool stream_k = use_stream_k(p, sk);
+    if (stream_k) {
+        splits = sk.kmax;           // partial slots per pair
+        tps = nt;
+        if (int rc = ensure_partials(p, sk.kmax)) return rc;
+        if (!p->part_o || !p->part_ml || p->part_capacity < sk.kmax) {
+            set_error("stream-K schedule without room for its partial results");
+            return DG_ERR_STATE;
+        }
+    }
     int rc = record_event(p, DG_STAGE_ATTENTION, s);
     if (rc) return rc;
     cudaError_t err;
@@ -329,8 +418,13 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.S = p->S; a.G = p->G;
         a.rows = p->rows; a.rows_pad = p->rows_pad;
         a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
-        a.cluster_combine = cluster_combine(p, splits) ? 1 : 0;
+        a.cluster_combine = !stream_k && cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
+        if (stream_k) {
+            a.sk_ctas = sk.ctas;
+            a.sk_units = sk.units;
+            a.qtiles = p->rows_pad / dg::kTileM;
+        }
         err = dg::launch_attn_tc(a, p->maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
     } else {
@@ -346,12 +440,18 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
     }
     rc = record_event(p, DG_STAGE_ATTENTION, s);
     if (rc) return rc;
-    if (splits > 1 && !cluster_combine(p, splits)) {
+    if (stream_k || (splits > 1 && !cluster_combine(p, splits))) {
         dg::CombineParams c{};
         c.part_o = p->part_o; c.part_ml = p->part_ml; c.out = out;
         c.T = p->T; c.nh = p->nh; c.nkv = p->nkv; c.G = p->G; c.rows = p->rows;
         c.rows_pad = p->rows_pad; c.splits = splits; c.hd = p->hd;
         c.log2_domain = p->path == DG_PATH_TC ? 1 : 0;
+        if (stream_k) {
+            c.sk_ctas = sk.ctas;
+            c.sk_units = sk.units;
+            c.qtiles = p->rows_pad / dg::kTileM;
+            c.n_tiles = nt;
+        }
         if ((rc = record_event(p, DG_STAGE_COMBINE, s))) return rc;
         err = dg::launch_combine(c, s);
         if (err != cudaSuccess) return cuda_fail(err, "combine launch");
@@ -476,6 +576,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     p->tc_ok = (hd == 64 || hd == 128 || hd == 256);
     p->path = p->tc_ok ? DG_PATH_TC : DG_PATH_FP32;
     p->splits_opt = 0;
+    p->schedule_opt = DG_SCHEDULE_AUTO;
     p->wait_limit_ms = 2000;
     p->device = dev;
     p->num_sms = prop.multiProcessorCount;
@@ -519,12 +620,14 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     if (rc == DG_OK) {
         // room for the partitions both paths would pick
         const int saved = p->path;
-        int need = 1;
+        int need = 0;
         for (int path : {DG_PATH_TC, DG_PATH_FP32}) {
             if (path == DG_PATH_TC && !p->tc_ok) continue;
             p->path = path;
-            const int s = auto_splits(p);
+            const int s = split_slots(auto_splits(p));
             if (s > need) need = s;
+            SkLayout L;
+            if (use_stream_k(p, L) && L.kmax > need) need = L.kmax;
         }
         p->path = saved;
         rc = ensure_partials(p, need);
@@ -579,7 +682,16 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
         p->part_capacity = 1 << 30;   // size the request before clamping to the buffers
         split_layout(p, s, tps, nt);
         p->part_capacity = cap;
-        return ensure_partials(p, s);
+        return ensure_partials(p, split_slots(s));
+    }
+    case DG_OPT_SCHEDULE: {
+        if (value != DG_SCHEDULE_AUTO && value != DG_SCHEDULE_SPLIT && value != DG_SCHEDULE_STREAM_K) {
+            set_error("schedule must be DG_SCHEDULE_AUTO, _SPLIT or _STREAM_K");
+            return DG_ERR_ARG;
+        }
+        p->schedule_opt = (int)value;
+        SkLayout L;
+        return use_stream_k(p, L) ? ensure_partials(p, L.kmax) : DG_OK;
     }
     case DG_OPT_WAIT_LIMIT_MS:
         if (value < 1 || value > 600000) {
@@ -620,16 +732,31 @@ int dg_attn_get_option(const dg_attn_plan *p, int key, long long *value)
     case DG_OPT_PROFILE: *value = p->profile; return DG_OK;
     case DG_OPT_INJECT_STALL: *value = p->inject_stall; return DG_OK;
     case DG_OPT_INPUTS_RESIDENT: *value = p->inputs_resident; return DG_OK;
-    case DG_INFO_SPLITS_USED:
+    case DG_OPT_SCHEDULE: *value = p->schedule_opt; return DG_OK;
+    case DG_INFO_SPLITS_USED: {
+        SkLayout L;
+        if (use_stream_k(p, L)) {
+            *value = L.kmax;        // the most pieces of one pair
+            return DG_OK;
+        }
         split_layout(p, s, tps, nt);
         *value = s;
         return DG_OK;
+    }
+    case DG_INFO_SCHEDULE_USED: {
+        SkLayout L;
+        *value = use_stream_k(p, L) ? DG_SCHEDULE_STREAM_K : DG_SCHEDULE_SPLIT;
+        return DG_OK;
+    }
     case DG_INFO_SCRATCH_BYTES: *value = (long long)p->scratch_bytes; return DG_OK;
     case DG_INFO_CACHE_READY: *value = p->cache_ready ? 1 : 0; return DG_OK;
-    case DG_INFO_LAUNCHES:
+    case DG_INFO_LAUNCHES: {
         split_layout(p, s, tps, nt);
-        *value = 2 + (s > 1 && !cluster_combine(p, s) ? 1 : 0) + (p->rope_dirty ? 1 : 0);
+        SkLayout L;
+        const bool combine = use_stream_k(p, L) || (s > 1 && !cluster_combine(p, s));
+        *value = 2 + (combine ? 1 : 0) + (p->rope_dirty ? 1 : 0);
         return DG_OK;
+    }
     default:
         set_error("unknown option %d", key);
         return DG_ERR_ARG;

@@ -84,7 +84,7 @@ template <int HD> struct Layout {
     static constexpr int K_OFF = QL_BYTES;
     static constexpr int V_OFF = K_OFF + C::KST * KSTAGE_BYTES;
     static constexpr int BAR_OFF = V_OFF + C::VST * VSTAGE_BYTES;
-    static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 3 + (C::NQI + 1);
+    static constexpr int NBARS = 2 * C::KST + 2 * C::VST + 3 * C::NSP + 5 + (C::NQI + 1);
     static constexpr int THREADS = 32 * (7 + C::NQI);
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + TMEM slot + alignment
     // In-cluster combine, once every MMA has completed (operand rings free): O of the tile
@@ -156,7 +156,9 @@ __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int r0, i
     }
 }
 
-template <int HD>
+// SK: the stream-K schedule (a CTA may hold two pieces); its bookkeeping is compiled only into
+// that instantiation (it costs the split schedule ~2% at hd = 256 otherwise).
+template <int HD, bool SK>
 __global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
 {
@@ -178,17 +180,58 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     uint64_t *o_final = sp_free + NSP;
     uint64_t *q_full = o_final + 1;
     uint64_t *q_ready = q_full + 1;
-    uint64_t *drain = q_ready + 1;          // [NQI + 1]: one per MMA-issuing thread
+    uint64_t *qk_done = q_ready + 1;        // every Q.K^T of the first piece has completed
+    uint64_t *o_free = qk_done + 1;         // O of the first piece has been read out of TMEM
+    uint64_t *drain = o_free + 1;           // [NQI + 1]: one per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + NQI + 1);
 
     // the next kernel of the stream may be scheduled now; it waits for this one to finish
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
-    const int tile0 = split * p.tiles_per_split;
-    const int n_local = min(p.n_tiles, tile0 + p.tiles_per_split) - tile0;
     const uint64_t limit = p.wait_limit_ns;
+
+    // The pieces of work of this CTA, each (query tile qt, kv group g, key tiles [t0, t0 + n)):
+    // one with the split schedule; one or two with the stream-K schedule (the end of a pair's
+    // key tiles and the start of the next pair's).  All roles walk the same sequence of
+    // n_all = n[0] + n[1] tiles; ring slots and barrier phases run on across the two pieces.
+    int pq[2] = {0, 0}, pg[2] = {0, 0}, pt0[2] = {0, 0}, pn[2] = {0, 0}, pslot[2] = {0, 0};
+    int nseg = 1;
+    if constexpr (!SK) {
+        pq[0] = blockIdx.x;
+        pg[0] = blockIdx.y;
+        pslot[0] = blockIdx.z;
+        pt0[0] = blockIdx.z * p.tiles_per_split;
+        pn[0] = min(p.n_tiles, pt0[0] + p.tiles_per_split) - pt0[0];
+    } else {
+        const long long U = p.sk_units;
+        long long u = sk_begin(blockIdx.x, U, p.sk_ctas);
+        const long long u1 = sk_begin(blockIdx.x + 1, U, p.sk_ctas);
+        nseg = 0;
+        while (u < u1 && nseg < 2) {
+            const int pr = (int)(u / p.n_tiles);
+            const int t0 = (int)(u - (long long)pr * p.n_tiles);
+            const int n = (int)min((long long)(p.n_tiles - t0), u1 - u);
+            pq[nseg] = pr % p.qtiles;
+            pg[nseg] = pr / p.qtiles;
+            pt0[nseg] = t0;
+            pn[nseg] = n;
+            pslot[nseg] = (int)blockIdx.x - sk_cta_of((long long)pr * p.n_tiles, U, p.sk_ctas);
+            ++nseg;
+            u += n;
+        }
+        if (u < u1 && threadIdx.x == 0) atomicOr(p.status, kErrSchedule);
+    }
+    const int n_all = SK ? pn[0] + pn[1] : pn[0];
+    // piece of tile `it` of the sequence, and the tile's index within its pair's key range
+    auto piece_of = [&](int it) -> int {
+        if constexpr (SK) return it < pn[0] ? 0 : 1;
+        else return 0;
+    };
+    auto key_tile = [&](int it) -> int {
+        if constexpr (SK) return it < pn[0] ? pt0[0] + it : pt0[1] + (it - pn[0]);
+        else return pt0[0] + it;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < KST; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
@@ -201,6 +244,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         mbar_init(o_final, 1);
         mbar_init(q_full, 1);
         mbar_init(q_ready, 128);
+        mbar_init(qk_done, NQI);
+        mbar_init(o_free, 128);
         for (int i = 0; i <= NQI; ++i) mbar_init(&drain[i], 1);
         fence_mbar_init();
         prefetch_tmap(&maps.kh);
@@ -225,21 +270,30 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             int issued[KST] = {};
-            if (!C::QL_TMEM) {
-                uint8_t *qls = smem;
-                mbar_arrive_expect_tx(q_full, Lay::QL_BYTES);
-                for (int pn = 0; pn < Lay::KPANELS; ++pn)
-                    tma_load_3d(qls + pn * (kTileM * 128), &maps.ql, q_full, pn * 64,
-                                qt * kTileM, g);
-            }
-            for (int it = 0; it < n_local; ++it) {
+            int cur = -1, q_loads = 0;
+            for (int it = 0; it < n_all; ++it) {
+                const int sg = piece_of(it), g = pg[sg];
+                if (sg != cur) {
+                    cur = sg;
+                    if (!C::QL_TMEM) {
+                        // the Q lo tile of the piece's pair; the second replaces the first once
+                        // every Q.K^T of the first piece has completed
+                        if (sg > 0 && !mbar_wait_bounded(qk_done, 0, limit)) { ok = false; break; }
+                        uint8_t *qls = smem;
+                        mbar_arrive_expect_tx(q_full, Lay::QL_BYTES);
+                        for (int pn = 0; pn < Lay::KPANELS; ++pn)
+                            tma_load_3d(qls + pn * (kTileM * 128), &maps.ql, q_full, pn * 64,
+                                        pq[sg] * kTileM, g);
+                        ++q_loads;
+                    }
+                }
                 const int s = it % KST;
                 if (it >= KST && !mbar_wait_bounded(&k_empty[s], ((it / KST) - 1) & 1, limit)) {
                     ok = false;
                     break;
                 }
                 uint8_t *kst = smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES;
-                const int key0 = (tile0 + it) * NK;
+                const int key0 = key_tile(it) * NK;
                 mbar_arrive_expect_tx(&k_full[s], Lay::KSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::KPANELS; ++pn) {
                     tma_load_3d_hint(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64,
@@ -253,7 +307,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             // let every load issued by this thread land before the CTA can exit
             for (int s = 0; s < KST; ++s)
                 if (issued[s] > 0) mbar_wait_bounded(&k_full[s], (issued[s] - 1) & 1, limit);
-            if (!C::QL_TMEM) mbar_wait_bounded(q_full, 0, limit);
+            if (q_loads > 0) mbar_wait_bounded(q_full, (q_loads - 1) & 1, limit);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -263,14 +317,17 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             bool ok = true;
             int issued[VST] = {};
             // VK-key stages, NK/VK of them per score tile
-            for (int it = 0; it < n_local * (NK / C::VK); ++it) {
+            constexpr int VPT = NK / C::VK;
+            for (int it = 0; it < n_all * VPT; ++it) {
                 const int s = it % VST;
                 if (it >= VST && !mbar_wait_bounded(&v_empty[s], ((it / VST) - 1) & 1, limit)) {
                     ok = false;
                     break;
                 }
                 uint8_t *vst = smem + Lay::V_OFF + s * Lay::VSTAGE_BYTES;
-                const int key0 = tile0 * NK + it * C::VK;
+                const int tile = it / VPT;
+                const int key0 = key_tile(tile) * NK + (it % VPT) * C::VK;
+                const int g = pg[piece_of(tile)];
                 mbar_arrive_expect_tx(&v_full[s], Lay::VSTAGE_BYTES);
                 for (int pn = 0; pn < Lay::VPANELS; ++pn)
                     tma_load_3d_hint(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64,
@@ -306,8 +363,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         if (warp == 1) {
             // P.V, in tile order: O += P_i V_i
             constexpr int VPT = NK / C::VK;                 // V stages per score tile
-            for (int i = 0; ok && i < n_local; ++i) {
+            for (int i = 0; ok && i < n_all; ++i) {
                 const int b = i % NSP;
+                const int sg = piece_of(i), first = sg == 0 ? 0 : pn[0];
+                if (sg > 0 && i == first) {
+                    // the second piece accumulates into O afresh once the first piece's O has
+                    // been read out
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_free, 0, limit));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(&p_full[b], (i / NSP) & 1, limit));
                 for (int h = 0; ok && h < VPT; ++h) {
                     const int c = i * VPT + h, vs = c % VST;
@@ -322,22 +387,38 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         const uint64_t bdesc = vd + (uint64_t)((ks * 16 * 128) >> 4);
                         const int kk = h * (C::VK / 16) + ks;
                         mma_bf16_ts_by(leader, t_o, t_sp + b * NK + kk * 8, bdesc, idesc_pv,
-                                       (i > 0 || kk > 0) ? 1u : 0u);
+                                       (i > first || kk > 0) ? 1u : 0u);
                     }
                     mma_commit_by(leader, &v_empty[vs]);
                 }
                 if (!ok) break;
                 mma_commit_by(leader, &sp_free[b]);
+                // O of a piece is complete after its last tile (o_final completes once per piece)
+                if (i == first + pn[sg] - 1) mma_commit_by(leader, o_final);
             }
-            if (ok) mma_commit_by(leader, o_final);
         } else {
             // Q.K^T of the tiles j = q (mod NQI): S_j = qh.kh + qh.kl + ql.kh
             const int q = warp == 3 ? 0 : warp - 7;
-            ok = mbar_wait_bounded(q_ready, 0, limit);
-            if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, 0, limit);
-            ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
-            for (int j = q; ok && j < n_local; j += NQI) {
+            int next_q = 0;                     // next phase of q_ready / q_full to wait for
+            bool done0 = false;                 // qk_done committed
+            for (int j = q; ok && j < n_all; j += NQI) {
+                const int sg = piece_of(j);
+                // Q of the piece's pair (hi, and lo when it lives in TMEM, in TMEM; lo in shared
+                // memory otherwise).  Phases are waited for in order: a parity wait for phase 1
+                // would pass while phase 0 is still open.  Before the second piece, every
+                // Q.K^T of the first issued here is committed to qk_done (Q may be replaced once
+                // they complete).
+                for (; ok && next_q <= sg; ++next_q) {
+                    if (next_q > 0 && !done0) {
+                        mma_commit_by(leader, qk_done);
+                        done0 = true;
+                    }
+                    ok = mbar_wait_bounded(q_ready, next_q & 1, limit);
+                    if (ok && !C::QL_TMEM) ok = mbar_wait_bounded(q_full, next_q & 1, limit);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                }
+                if (!ok) break;
                 const int b = j % NSP, s = j % KST;
                 if (j >= NSP) ok = mbar_wait_bounded(&sp_free[b], ((j / NSP) - 1) & 1, limit);
                 if (ok) ok = mbar_wait_bounded(&k_full[s], (j / KST) & 1, limit);
@@ -363,6 +444,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 mma_commit_by(leader, &k_empty[s]);
                 mma_commit_by(leader, &s_full[b]);
             }
+            if (ok && nseg > 1 && !done0) mma_commit_by(leader, qk_done);
         }
         if (!ok && leader) atomicOr(p.status, kErrWaitMma);
         // no tcgen05 operation of this warp may still run when TMEM is released
@@ -375,8 +457,44 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                  // tile row == TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int Rg = qt * kTileM + r;                     // packed row in the group
         bool ok = true;
+        // Scores arrive in log2 units: the first stage scaled q-hat by log2(e) before its
+        // hi/lo split, so P = 2^(s - m) needs no multiply here.
+        float m_used = -INFINITY;
+        float2 l2 = make_float2(0.f, 0.f);   // running denominator, two partial sums
+
+        // A stream-K piece's result (O unnormalised, once o_final of the piece has completed):
+        // its (m, l) per row, and its O rows row-interleaved per 128-row tile (16-byte unit u of
+        // row r at u * 128 + r), so every store instruction of a warp writes 512 contiguous
+        // bytes straight from the TMEM registers (no shared memory: the rings may be busy with
+        // the next piece).
+        auto write_piece = [&](int sg, float m, float l) {
+            const size_t prow = ((size_t)pslot[sg] * p.nkv + pg[sg]) * p.rows_pad;
+            p.part_ml[prow + (size_t)pq[sg] * kTileM + r] = make_float2(m, l);
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + (prow + (size_t)pq[sg] * kTileM) * HD) + r;
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, orr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[(size_t)(8 * c + v) * kTileM] =
+                        make_float4(__uint_as_float(orr[4 * v]), __uint_as_float(orr[4 * v + 1]),
+                                    __uint_as_float(orr[4 * v + 2]), __uint_as_float(orr[4 * v + 3]));
+            }
+        };
+
+        for (int sg = 0; ok && sg < nseg; ++sg) {
+        const int qt = pq[sg], g = pg[sg];
+        const int base = sg == 0 ? 0 : pn[0];               // first tile of the piece in the CTA
+        const int nloc = pn[sg], tile0 = pt0[sg];
+        if (sg > 0) {
+            // Q of the second pair replaces the first once every Q.K^T of the first piece is done
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(qk_done, 0, limit));
+            if (!ok) break;
+            tc_fence_after();
+        }
 
         // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.  Every load of the
         // row is issued before the first TMEM store (one memory round trip, not one per chunk).
@@ -409,20 +527,28 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             tc_fence_before();
             mbar_arrive(q_ready);
         }
-
-        // Scores arrive in log2 units: the first stage scaled q-hat by log2(e) before its
-        // hi/lo split, so P = 2^(s - m) needs no multiply here.
-        float m_used = -INFINITY;
-        float2 l2 = make_float2(0.f, 0.f);   // running denominator, two partial sums
+        if (sg > 0) {
+            // the first piece's O goes out while the tensor pipe starts on the second piece's
+            // scores; then the second piece's P.V may overwrite O
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, limit));
+            if (!ok) break;
+            tc_fence_after();
+            write_piece(0, m_used, l2.x + l2.y);
+            tc_fence_before();
+            mbar_arrive(o_free);
+        }
+        m_used = -INFINITY;
+        l2 = make_float2(0.f, 0.f);
         {
             // Start the reference from the maximum over the first NSP score tiles (they are
             // computed at once by the NSP issuers), not the first tile alone: the running
             // maximum then grows less, and O is rescaled less often.  A buffer's first phase is
             // waited for again in the loop below; that wait returns at once.
-            const int nw = min(NSP, n_local);
+            const int nw = min(NSP, nloc);
             float m0 = -INFINITY;
             for (int t = 0; t < nw; ++t) {
-                ok = mbar_wait_bounded(&s_full[t], 0, limit);
+                const int bt = (base + t) % NSP;
+                ok = mbar_wait_bounded(&s_full[bt], ((base + t) / NSP) & 1, limit);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 const int valid = p.S - (tile0 + t) * NK;
@@ -430,7 +556,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
 #pragma unroll 1
                 for (int c = 0; c < NK / CW; ++c) {
                     uint32_t sr[CW];
-                    tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + t * NK + CW * c, sr);
+                    tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + bt * NK + CW * c, sr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < CW; ++i)
@@ -439,7 +565,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             }
             if (ok && nw > 0) m_used = m0 + kHeadroom;
         }
-        for (int it = 0; ok && it < n_local; ++it) {
+        for (int it = base; ok && it < base + nloc; ++it) {
             const int b = it % NSP;
             ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
@@ -452,7 +578,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             uint32_t sr[RC][CW];
             // keys of this tile below S; only the last tile of the key range is partial, so the
             // masking branch is warp-uniform and almost never taken
-            const int valid = p.S - (tile0 + it) * NK;
+            const int valid = p.S - (tile0 + (it - base)) * NK;
             float mx;
             if constexpr (NK <= 64) {
 #pragma unroll
@@ -495,7 +621,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             if (__any_sync(0xffffffffu, need)) {
                 const float m_new = fmaxf(m_used, mx + kHeadroom);
                 const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
-                if (it > 0) {
+                if (it > base) {
                     // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
                     // has landed
                     const int pb = (it - 1) % NSP;
@@ -579,13 +705,19 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             tc_fence_before();
             if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
         }
+        }   // pieces
         const float l_run = l2.x + l2.y;
-        if (ok && !mbar_wait_bounded(o_final, 0, limit)) ok = false;
+        if (ok && !mbar_wait_bounded(o_final, (nseg - 1) & 1, limit)) ok = false;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) atomicOr(p.status, kErrWaitSoftmax);
+        } else if (SK) {
+            tc_fence_after();
+            write_piece(nseg - 1, m_used, l_run);
         } else {
             tc_fence_after();
+            const int qt = pq[0], g = pg[0], split = pslot[0];
+            const int Rg = qt * kTileM + r;                 // packed row in the group
             // Every MMA has completed, so the K ring is free: each warp stages its 32 rows x 32
             // columns of O in a shared-memory tile (row pitch 36 floats, conflict-free for float4)
             // and writes it back row-contiguous: a store instruction covers 128 bytes of each of
@@ -690,8 +822,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplits; ++q)
                 if (q < P) wgt[i * kMaxClusterSplits + q] = m[q] * inv;
-            const int Rg = qt * kTileM + r;
-            dst[i] = Rg < p.rows ? p.out + ((size_t)(Rg / p.G) * p.nh + g * p.G + Rg % p.G) * HD
+            const int Rg = pq[0] * kTileM + r;
+            dst[i] = Rg < p.rows ? p.out + ((size_t)(Rg / p.G) * p.nh + pg[0] * p.G + Rg % p.G) * HD
                                  : nullptr;
         }
         __syncthreads();
@@ -722,7 +854,7 @@ template <int HD>
 cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
+    cfg.gridDim = p.sk_ctas ? dim3(p.sk_ctas) : dim3((p.rows + kTileM - 1) / kTileM, p.nkv, p.splits);
     cfg.blockDim = dim3(Layout<HD>::THREADS);
     cfg.dynamicSmemBytes = Layout<HD>::SMEM_BYTES;
     cfg.stream = s;
@@ -734,7 +866,8 @@ cudaError_t launch_hd(const AttnTcParams &p, const TcMaps &maps, cudaStream_t s)
     attr[1].val.clusterDim.z = p.splits;
     cfg.attrs = attr;
     cfg.numAttrs = p.cluster_combine ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, p);
+    if (p.sk_ctas) return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, true>, maps, p);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, false>, maps, p);
 }
 
 template <int HD>
@@ -752,7 +885,7 @@ int max_clusters_hd(int splits, int qtiles, int nkv)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD, false>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -762,7 +895,11 @@ int max_clusters_hd(int splits, int qtiles, int nkv)
 template <int HD>
 cudaError_t prepare_hd()
 {
-    return cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<HD>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_tc_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Layout<HD>::SMEM_BYTES);
 }
 

@@ -142,6 +142,99 @@ __global__ void __launch_bounds__(32 * kCombineRowsPerCta) combine_kernel(Combin
                                          acc[v].w * inv);
 }
 
+// Stream-K pieces: one CTA per (128-row query tile, kv group, 32 columns), one thread per row
+// (blockIdx.z picks the columns: the merge of a tile is spread over hd/32 CTAs).  The pair's
+// pieces are those of CTAs sk_cta_of(p * n_tiles) .. sk_cta_of((p + 1) * n_tiles - 1) of the
+// attention kernel, in that order (deterministic).  A piece's O rows are row-interleaved, so each
+// load instruction of a warp reads 512 contiguous bytes; the merged rows go out through a
+// shared-memory transpose, 128 contiguous bytes of 4 rows per store instruction.
+//   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k.
+template <int HD>
+__global__ void __launch_bounds__(kTileM) combine_sk_kernel(CombineParams p)
+{
+    pdl_launch_dependents();
+    pdl_wait();   // the pieces come from the attention kernel just before
+    __shared__ float stage[kTileM / 32][32 * 36];
+    const int qt = blockIdx.x, g = blockIdx.y, c = blockIdx.z;
+    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    const int pr = g * p.qtiles + qt;
+    const long long U = p.sk_units;
+    const int c0 = sk_cta_of((long long)pr * p.n_tiles, U, p.sk_ctas);
+    const int np = sk_cta_of((long long)(pr + 1) * p.n_tiles - 1, U, p.sk_ctas) - c0 + 1;
+    const int R = qt * kTileM + r;
+    const size_t stride = (size_t)p.nkv * p.rows_pad;           // rows between slots
+    const size_t row = (size_t)g * p.rows_pad + R;
+    float w[kMaxStreamKPieces];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxStreamKPieces; ++k) {
+        w[k] = -INFINITY;
+        if (k < np) {
+            const float2 ml = p.part_ml[k * stride + row];
+            w[k] = ml.x;
+            M = fmaxf(M, ml.x);
+        }
+    }
+    float den = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxStreamKPieces; ++k) {
+        if (k < np) {
+            const float e = exp2f(w[k] - M);
+            den = fmaf(e, p.part_ml[k * stride + row].y, den);
+            w[k] = e;
+        } else {
+            w[k] = 0.f;
+        }
+    }
+    const float inv = 1.0f / den;
+    float *mydst = R < p.rows ? p.out + ((size_t)(R / p.G) * p.nh + g * p.G + R % p.G) * HD
+                              : nullptr;
+    // float4 units of this tile in slot k: (slot tile base + u) * 128 + r
+    const float4 *src = reinterpret_cast<const float4 *>(p.part_o) +
+                        ((size_t)g * p.rows_pad + (size_t)qt * kTileM) * (HD / 4) + r;
+    const size_t slot_stride = stride * (HD / 4);
+    float *stg = stage[warp];
+    const int sub = lane & 7, rsub = lane >> 3;
+    // the pieces four at a time, all 32 loads of a batch in flight before any arithmetic
+    float4 acc[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k0 = 0; k0 < kMaxStreamKPieces; k0 += 4) {
+        if (k0 >= np) break;
+        float4 o[4][8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                o[k][v] = k0 + k < np ? src[(k0 + k) * slot_stride + (size_t)(8 * c + v) * kTileM]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float wk = k0 + k < np ? w[k0 + k] * inv : 0.f;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                acc[v].x = fmaf(wk, o[k][v].x, acc[v].x);
+                acc[v].y = fmaf(wk, o[k][v].y, acc[v].y);
+                acc[v].z = fmaf(wk, o[k][v].z, acc[v].z);
+                acc[v].w = fmaf(wk, o[k][v].w, acc[v].w);
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<float4 *>(stg + lane * 36 + 4 * v) = acc[v];
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int j = 4 * k + rsub;
+        float *d = reinterpret_cast<float *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mydst), j));
+        if (d)
+            *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) =
+                *reinterpret_cast<const float4 *>(stg + j * 36 + 4 * sub);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
@@ -161,6 +254,21 @@ cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s)
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
+    if (p.sk_ctas > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.qtiles, p.nkv, p.hd / 32);
+        cfg.blockDim = dim3(kTileM);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1] = {pdl_attribute()};
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        switch (p.hd) {
+        case 64: return cudaLaunchKernelEx(&cfg, combine_sk_kernel<64>, p);
+        case 128: return cudaLaunchKernelEx(&cfg, combine_sk_kernel<128>, p);
+        case 256: return cudaLaunchKernelEx(&cfg, combine_sk_kernel<256>, p);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (p.splits > kMaxCombineSplits) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta, p.nkv);

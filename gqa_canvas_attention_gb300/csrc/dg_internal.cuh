@@ -16,6 +16,7 @@ enum : uint32_t {
     kErrWaitMma = 2u,
     kErrWaitSoftmax = 4u,
     kErrWaitDrain = 8u,
+    kErrSchedule = 16u,            // a stream-K run covered more than two pairs (host error)
 };
 
 // Rows of the tensor-core query tile: the G = nh/nkv query heads of one kv group are packed
@@ -90,7 +91,26 @@ struct AttnTcParams {
     int cluster_combine;           // 1: the splits CTAs of a query tile form a cluster and merge
                                    // their partial results through distributed shared memory
     int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
+    // stream-K schedule (sk_ctas > 0): CTA c takes key-tile units [sk_begin(c), sk_begin(c + 1))
+    // of the qtiles * nkv pairs in order p = g * qtiles + qt, n_tiles units each; its pieces go
+    // to part_o / part_ml at slot = its rank among the CTAs of that pair
+    int sk_ctas, qtiles;
+    long long sk_units;
 };
+
+// Stream-K schedule: U key-tile units over C CTAs, CTA c taking [sk_begin(c), sk_begin(c + 1)).
+__host__ __device__ inline long long sk_begin(int c, long long U, int C)
+{
+    return (long long)c * U / C;
+}
+// The CTA whose run holds unit u.
+__host__ __device__ inline int sk_cta_of(long long u, long long U, int C)
+{
+    int c = (int)((u * C) / U);
+    while (c + 1 < C && sk_begin(c + 1, U, C) <= u) ++c;
+    while (c > 0 && sk_begin(c, U, C) > u) --c;
+    return c;
+}
 
 struct CombineParams {
     const float *part_o;
@@ -98,6 +118,11 @@ struct CombineParams {
     float *out;
     int T, nh, nkv, G, rows, rows_pad, splits, hd;
     int log2_domain;               // 1: weights are 2^(s - m) (tensor-core path), 0: e^(s - m)
+    // stream-K pieces (sk_ctas > 0): pair (qt, g) has the pieces of CTAs sk_cta_of(p * n_tiles)
+    // .. sk_cta_of((p + 1) * n_tiles - 1), p = g * qtiles + qt; part_o holds them row-interleaved
+    // per 128-row tile (16-byte unit u of tile row r at u * 128 + r)
+    int sk_ctas, qtiles, n_tiles;
+    long long sk_units;
 };
 
 // ---- the projection step before the block (proj_tc.cu) ----
@@ -199,6 +224,7 @@ cudaError_t attn_tc_prepare(int hd);   // one-time function attributes (smem opt
 // Clusters of `splits` CTAs the GPU can hold at once (0: that cluster launch cannot run).
 int attn_tc_max_clusters(int hd, int splits, int qtiles, int nkv);
 constexpr int kMaxClusterSplits = 8;   // portable cluster size
+constexpr int kMaxStreamKPieces = 16;  // pieces of one pair the stream-K combine merges
 size_t attn_tc_smem_bytes(int hd);
 
 }  // namespace dg

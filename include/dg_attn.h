@@ -75,12 +75,26 @@ typedef struct dg_attn_plan dg_attn_plan;
                                    reads them while the previous call's attention kernel is still
                                    running.  Default 0: the first stage waits for the preceding
                                    kernel before reading anything */
+#define DG_OPT_SCHEDULE      8  /* how the tensor-core kernel deals key tiles to CTAs: one of
+                                   DG_SCHEDULE_AUTO (default), DG_SCHEDULE_SPLIT,
+                                   DG_SCHEDULE_STREAM_K */
+#define DG_SCHEDULE_AUTO     0  /* the cheaper of the two for the plan's geometry (a cost model) */
+#define DG_SCHEDULE_SPLIT    1  /* one CTA per (query tile, kv group, key partition), partitions
+                                   set by DG_OPT_SPLITS; 2..8 partitions merge inside the kernel,
+                                   more through the combine kernel */
+#define DG_SCHEDULE_STREAM_K 2  /* one CTA per SM: the (query tile, kv group) pairs, in order, are
+                                   cut into key tiles and every CTA takes an equal run of them
+                                   (a run may cover the end of one pair and the start of the
+                                   next); the combine kernel merges each pair's pieces.  Ignores
+                                   DG_OPT_SPLITS */
 /* Read-only (dg_attn_get_option): */
 #define DG_INFO_SPLITS_USED  16 /* partitions the next forward will use */
 #define DG_INFO_SCRATCH_BYTES 17 /* device bytes the plan holds */
 #define DG_INFO_CACHE_READY  18 /* 1 when dg_attn_cache_prepare has filled the plan's cache copy */
 #define DG_INFO_LAUNCHES     19 /* kernels the next dg_attn_forward enqueues with the current options
                                    (without a caller's cos_sin table) */
+#define DG_INFO_SCHEDULE_USED 20 /* DG_SCHEDULE_SPLIT or DG_SCHEDULE_STREAM_K: what the next forward
+                                   uses (DG_SCHEDULE_SPLIT on the fp32 path) */
 
 /* Create a plan for one geometry on the current device.  Requires nh % nkv == 0, nh, nkv, T >= 1,
  * ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in {64, 128, 256}),

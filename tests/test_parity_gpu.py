@@ -194,6 +194,76 @@ def test_forced_partitions(case, path):
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], f"splits={splits}")
 
 
+# The stream-K schedule (one CTA per SM, each an equal run of key tiles over the (query tile,
+# kv group) pairs in order; most runs cover the end of one pair and the start of the next).
+STREAM_K_SHAPES = [
+    # T, ctx, nh, nkv, hd
+    (512, 8192, 8, 4, 256),  # the 48-step workload's geometry: 32 pairs x 136 tiles on 152 CTAs
+    (50, 1000, 4, 2, 256),   # S = 1050: the last key tile of every pair is ragged
+    (65, 300, 8, 1, 256),    # G = 8: 520 packed rows, the last query tile nearly empty
+    (130, 1500, 8, 4, 256),  # 3 query tiles per kv group
+    (256, 4096, 16, 8, 128), # two Q.K^T issuers per CTA
+    (40, 2000, 4, 2, 128),
+    (512, 0, 16, 16, 64),    # ctx = 0, 64 pairs
+    (3, 5, 2, 1, 64),        # one pair, fewer key tiles than SMs
+]
+
+
+@pytest.mark.parametrize("shape", STREAM_K_SHAPES, ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d" % s)
+def test_stream_k_schedule(shape):
+    T, ctx, nh, nkv, hd = shape
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=300 + T + hd, weighted=True)
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_SCHEDULE, B.DG_SCHEDULE_STREAM_K)
+    assert plan.get(B.DG_INFO_SCHEDULE_USED) == B.DG_SCHEDULE_STREAM_K
+    out = run_forward(plan, dd)
+    again = run_forward(plan, dd)
+    assert torch.equal(out, again), "the stream-K merge order is fixed: results repeat bit for bit"
+    ranges = row_ranges(T)
+    ref = np.zeros((T, nh * hd))
+    for a, b in ranges:
+        ref[a:b] = oracle_out(d, nh, nkv, hd, rows=(a, b))[a:b]
+    check(out, ref, B.DG_PATH_TC, ranges, "stream-K %s" % (shape,))
+    # the split schedule on the same inputs agrees within the same bound
+    plan.set(B.DG_OPT_SCHEDULE, B.DG_SCHEDULE_SPLIT)
+    assert plan.get(B.DG_INFO_SCHEDULE_USED) == B.DG_SCHEDULE_SPLIT
+    split = run_forward(plan, dd)
+    check(split, ref, B.DG_PATH_TC, ranges, "split %s" % (shape,))
+
+
+def test_stream_k_under_a_cuda_graph_with_resident_inputs():
+    """The bench's configuration: graph replay, resident inputs, several forwards back to back."""
+    w = WORKLOADS["denoise48_ctx8k"]
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_SCHEDULE, B.DG_SCHEDULE_STREAM_K).set(B.DG_OPT_INPUTS_RESIDENT, 1)
+    d0 = workload_inputs(w, step=0)
+    plan.cache_prepare(d0["k_cache"].cuda(), d0["v_cache"].cuda())
+    steps = (0, 1, 2)
+    ins = []
+    for st in steps:
+        d = workload_inputs(w, step=st)
+        d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]
+        ins.append((d, to_dev(d)))
+    outs = [torch.empty(w.T, w.nh * w.hd, device="cuda") for _ in steps]
+    fwd = lambda: [plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None,
+                                dd["q_norm_w"], dd["k_norm_w"], None, o)
+                   for (_, dd), o in zip(ins, outs)]
+    fwd()                                   # builds the cos/sin table outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd()
+    for o in outs:
+        o.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert plan.sync_status() == B.DG_OK
+    for (d, _), o in zip(ins, outs):
+        ranges = [(w.T - 4, w.T)]
+        check(o, oracle_out(d, w.nh, w.nkv, w.hd, rows=ranges[0]), B.DG_PATH_TC, ranges, "graph")
+
+
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
 def test_k_and_v_canvas_may_alias(path):
     """Models whose V is the raw K projection pass the same buffer twice."""
