@@ -486,225 +486,225 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         };
 
         for (int sg = 0; ok && sg < nseg; ++sg) {
-        const int qt = pq[sg], g = pg[sg];
-        const int base = sg == 0 ? 0 : pn[0];               // first tile of the piece in the CTA
-        const int nloc = pn[sg], tile0 = pt0[sg];
-        if (sg > 0) {
-            // Q of the second pair replaces the first once every Q.K^T of the first piece is done
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(qk_done, 0, limit));
-            if (!ok) break;
-            tc_fence_after();
-        }
-
-        // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.  Every load of the
-        // row is issued before the first TMEM store (one memory round trip, not one per chunk).
-        {
-            // the operand is row-interleaved: 16-byte unit u of tile row r at (tile*HD/8 + u)*128
-            // + r, so each load instruction of a warp reads 512 contiguous bytes
-            constexpr int NCH = (HD / 64) * (C::QL_TMEM ? 2 : 1);   // 32-column chunks
-            const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + qt) * (HD / 8) * kTileM;
-            const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh) + tile + r;
-            const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql) + tile + r;
-            uint4 w[NCH][8];
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    w[c][v] = c < HD / 64 ? src_h[(c * 8 + v) * kTileM]
-                                          : src_l[((c - HD / 64) * 8 + v) * kTileM];
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                uint32_t u[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    u[4 * v] = w[c][v].x; u[4 * v + 1] = w[c][v].y;
-                    u[4 * v + 2] = w[c][v].z; u[4 * v + 3] = w[c][v].w;
-                }
-                const int col = c < HD / 64 ? C::QH_COL + 32 * c : C::QL_COL + 32 * (c - HD / 64);
-                tmem_st32(tbase + lane_off + col, u);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(q_ready);
-        }
-        if (sg > 0) {
-            // the first piece's O goes out while the tensor pipe starts on the second piece's
-            // scores; then the second piece's P.V may overwrite O
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, limit));
-            if (!ok) break;
-            tc_fence_after();
-            write_piece(0, m_used, l2.x + l2.y);
-            tc_fence_before();
-            mbar_arrive(o_free);
-        }
-        m_used = -INFINITY;
-        l2 = make_float2(0.f, 0.f);
-        {
-            // Start the reference from the maximum over the first NSP score tiles (they are
-            // computed at once by the NSP issuers), not the first tile alone: the running
-            // maximum then grows less, and O is rescaled less often.  A buffer's first phase is
-            // waited for again in the loop below; that wait returns at once.
-            const int nw = min(NSP, nloc);
-            float m0 = -INFINITY;
-            for (int t = 0; t < nw; ++t) {
-                const int bt = (base + t) % NSP;
-                ok = mbar_wait_bounded(&s_full[bt], ((base + t) / NSP) & 1, limit);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const int qt = pq[sg], g = pg[sg];
+            const int base = sg == 0 ? 0 : pn[0];               // first tile of the piece in the CTA
+            const int nloc = pn[sg], tile0 = pt0[sg];
+            if (sg > 0) {
+                // Q of the second pair replaces the first once every Q.K^T of the first piece is done
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(qk_done, 0, limit));
+                if (!ok) break;
                 tc_fence_after();
-                const int valid = p.S - (tile0 + t) * NK;
-                constexpr int CW = NK % 32 == 0 ? 32 : 16;
-#pragma unroll 1
-                for (int c = 0; c < NK / CW; ++c) {
-                    uint32_t sr[CW];
-                    tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + bt * NK + CW * c, sr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < CW; ++i)
-                        if (CW * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
-                }
             }
-            if (ok && nw > 0) m_used = m0 + kHeadroom;
-        }
-        for (int it = base; ok && it < base + nloc; ++it) {
-            const int b = it % NSP;
-            ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
-            tc_fence_after();
-            const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
-            // NK <= 64: the whole score row stays in registers; NK = 128: the maximum is taken in
-            // a first pass and the scores are read again (register budget of 320 threads)
-            constexpr int CW = NK % 32 == 0 ? 32 : 16;            // columns per score chunk
-            constexpr int RC = NK <= 64 ? NK / CW : 1;
-            uint32_t sr[RC][CW];
-            // keys of this tile below S; only the last tile of the key range is partial, so the
-            // masking branch is warp-uniform and almost never taken
-            const int valid = p.S - (tile0 + (it - base)) * NK;
-            float mx;
-            if constexpr (NK <= 64) {
+
+            // Q hi (and Q lo) rows into TMEM: HD bf16 = HD/2 32-bit columns each.  Every load of the
+            // row is issued before the first TMEM store (one memory round trip, not one per chunk).
+            {
+                // the operand is row-interleaved: 16-byte unit u of tile row r at (tile*HD/8 + u)*128
+                // + r, so each load instruction of a warp reads 512 contiguous bytes
+                constexpr int NCH = (HD / 64) * (C::QL_TMEM ? 2 : 1);   // 32-column chunks
+                const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + qt) * (HD / 8) * kTileM;
+                const uint4 *src_h = reinterpret_cast<const uint4 *>(p.qh) + tile + r;
+                const uint4 *src_l = reinterpret_cast<const uint4 *>(p.ql) + tile + r;
+                uint4 w[NCH][8];
 #pragma unroll
-                for (int c = 0; c < RC; ++c) tmem_ld_chunk<CW>(tsp + CW * c, sr[c]);
-                tmem_wait_ld();
-                if (valid < NK) {
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        w[c][v] = c < HD / 64 ? src_h[(c * 8 + v) * kTileM]
+                                              : src_l[((c - HD / 64) * 8 + v) * kTileM];
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t u[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        u[4 * v] = w[c][v].x; u[4 * v + 1] = w[c][v].y;
+                        u[4 * v + 2] = w[c][v].z; u[4 * v + 3] = w[c][v].w;
+                    }
+                    const int col = c < HD / 64 ? C::QH_COL + 32 * c : C::QL_COL + 32 * (c - HD / 64);
+                    tmem_st32(tbase + lane_off + col, u);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(q_ready);
+            }
+            if (sg > 0) {
+                // the first piece's O goes out while the tensor pipe starts on the second piece's
+                // scores; then the second piece's P.V may overwrite O
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, limit));
+                if (!ok) break;
+                tc_fence_after();
+                write_piece(0, m_used, l2.x + l2.y);
+                tc_fence_before();
+                mbar_arrive(o_free);
+            }
+            m_used = -INFINITY;
+            l2 = make_float2(0.f, 0.f);
+            {
+                // Start the reference from the maximum over the first NSP score tiles (they are
+                // computed at once by the NSP issuers), not the first tile alone: the running
+                // maximum then grows less, and O is rescaled less often.  A buffer's first phase is
+                // waited for again in the loop below; that wait returns at once.
+                const int nw = min(NSP, nloc);
+                float m0 = -INFINITY;
+                for (int t = 0; t < nw; ++t) {
+                    const int bt = (base + t) % NSP;
+                    ok = mbar_wait_bounded(&s_full[bt], ((base + t) / NSP) & 1, limit);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    const int valid = p.S - (tile0 + t) * NK;
+                    constexpr int CW = NK % 32 == 0 ? 32 : 16;
+#pragma unroll 1
+                    for (int c = 0; c < NK / CW; ++c) {
+                        uint32_t sr[CW];
+                        tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + bt * NK + CW * c, sr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < CW; ++i)
+                            if (CW * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
+                    }
+                }
+                if (ok && nw > 0) m_used = m0 + kHeadroom;
+            }
+            for (int it = base; ok && it < base + nloc; ++it) {
+                const int b = it % NSP;
+                ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
+                tc_fence_after();
+                const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
+                // NK <= 64: the whole score row stays in registers; NK = 128: the maximum is taken in
+                // a first pass and the scores are read again (register budget of 320 threads)
+                constexpr int CW = NK % 32 == 0 ? 32 : 16;            // columns per score chunk
+                constexpr int RC = NK <= 64 ? NK / CW : 1;
+                uint32_t sr[RC][CW];
+                // keys of this tile below S; only the last tile of the key range is partial, so the
+                // masking branch is warp-uniform and almost never taken
+                const int valid = p.S - (tile0 + (it - base)) * NK;
+                float mx;
+                if constexpr (NK <= 64) {
+#pragma unroll
+                    for (int c = 0; c < RC; ++c) tmem_ld_chunk<CW>(tsp + CW * c, sr[c]);
+                    tmem_wait_ld();
+                    if (valid < NK) {
+#pragma unroll
+                        for (int c = 0; c < RC; ++c)
+#pragma unroll
+                            for (int i = 0; i < CW; ++i)
+                                if (CW * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+                    }
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int c = 0; c < RC; ++c)
 #pragma unroll
-                        for (int i = 0; i < CW; ++i)
-                            if (CW * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
-                }
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int c = 0; c < RC; ++c)
-#pragma unroll
-                    for (int i = 0; i < CW; i += 2)
-                        m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[c][i]),
-                                                 __uint_as_float(sr[c][i + 1]));
-                mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-            } else {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        for (int i = 0; i < CW; i += 2)
+                            m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[c][i]),
+                                                     __uint_as_float(sr[c][i + 1]));
+                    mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+                } else {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-                for (int c = 0; c < NK / 32; ++c) {
-                    tmem_ld32(tsp + 32 * c, sr[0]);
-                    tmem_wait_ld();
-                    if (32 * c + 32 > valid) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[0][i]),
-                                                 __uint_as_float(sr[0][i + 1]));
-                }
-                mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-            }
-            const bool need = mx > m_used + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float m_new = fmaxf(m_used, mx + kHeadroom);
-                const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
-                if (it > base) {
-                    // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
-                    // has landed
-                    const int pb = (it - 1) % NSP;
-                    if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    tc_fence_after();
-                    const float2 a2 = make_float2(alpha, alpha);
-                    // two 32-column chunks per round trip to TMEM (one when the score row
-                    // already holds 64 registers)
-                    constexpr int RW = NK <= 32 ? 2 : 1;
-#pragma unroll 1
-                    for (int c = 0; c < HD / 32; c += RW) {
-                        uint32_t o0[32], o1[32];
-                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, o0);
-                        if constexpr (RW == 2) tmem_ld32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
+                    for (int c = 0; c < NK / 32; ++c) {
+                        tmem_ld32(tsp + 32 * c, sr[0]);
                         tmem_wait_ld();
+                        if (32 * c + 32 > valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const float2 x0 = mul_f32x2(
-                                make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
-                            o0[i] = __float_as_uint(x0.x);
-                            o0[i + 1] = __float_as_uint(x0.y);
-                            if constexpr (RW == 2) {
-                                const float2 x1 = mul_f32x2(
-                                    make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
-                                o1[i] = __float_as_uint(x1.x);
-                                o1[i + 1] = __float_as_uint(x1.y);
-                            }
+                            for (int i = 0; i < 32; ++i)
+                                if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
                         }
-                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c, o0);
-                        if constexpr (RW == 2) tmem_st32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
-                    }
-                    tmem_wait_st();
-                }
-                l2 = mul_f32x2(l2, make_float2(alpha, alpha));
-                m_used = m_new;
-            }
-            // P in fp16, two keys per 32-bit column, written over the start of the score buffer
-            // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
-            // sums the fp32 values; their fp16 roundings differ by at most 2^-11 relative each.
-            const float2 mm = make_float2(m_used, m_used);
-            if constexpr (NK <= 64) {
 #pragma unroll
-                for (int c = 0; c < RC; ++c) {
-                    uint32_t pw[CW / 2];
-#pragma unroll
-                    for (int i = 0; i < CW / 2; ++i) {
-                        const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[c][2 * i]),
-                                                               __uint_as_float(sr[c][2 * i + 1])), mm);
-                        const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-                        l2 = add_f32x2(l2, pp);
-                        const __half2 h = __floats2half2_rn(pp.x, pp.y);
-                        pw[i] = *reinterpret_cast<const uint32_t *>(&h);
+                        for (int i = 0; i < 32; i += 2)
+                            m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[0][i]),
+                                                     __uint_as_float(sr[0][i + 1]));
                     }
-                    tmem_st_half_chunk<CW>(tsp + (CW / 2) * c, pw);
+                    mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
                 }
-            } else {
+                const bool need = mx > m_used + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = fmaxf(m_used, mx + kHeadroom);
+                    const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
+                    if (it > base) {
+                        // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
+                        // has landed
+                        const int pb = (it - 1) % NSP;
+                        if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        const float2 a2 = make_float2(alpha, alpha);
+                        // two 32-column chunks per round trip to TMEM (one when the score row
+                        // already holds 64 registers)
+                        constexpr int RW = NK <= 32 ? 2 : 1;
 #pragma unroll 1
-                for (int c = 0; c < NK / 32; ++c) {
-                    tmem_ld32(tsp + 32 * c, sr[0]);
-                    tmem_wait_ld();
-                    if (32 * c + 32 > valid) {
+                        for (int c = 0; c < HD / 32; c += RW) {
+                            uint32_t o0[32], o1[32];
+                            tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                            if constexpr (RW == 2) tmem_ld32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 x0 = mul_f32x2(
+                                    make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
+                                o0[i] = __float_as_uint(x0.x);
+                                o0[i + 1] = __float_as_uint(x0.y);
+                                if constexpr (RW == 2) {
+                                    const float2 x1 = mul_f32x2(
+                                        make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
+                                    o1[i] = __float_as_uint(x1.x);
+                                    o1[i + 1] = __float_as_uint(x1.y);
+                                }
+                            }
+                            tmem_st32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                            if constexpr (RW == 2) tmem_st32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
+                        }
+                        tmem_wait_st();
                     }
-                    uint32_t pw[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[0][2 * i]),
-                                                               __uint_as_float(sr[0][2 * i + 1])), mm);
-                        const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-                        l2 = add_f32x2(l2, pp);
-                        const __half2 h = __floats2half2_rn(pp.x, pp.y);
-                        pw[i] = *reinterpret_cast<const uint32_t *>(&h);
-                    }
-                    tmem_st16(tsp + 16 * c, pw);
+                    l2 = mul_f32x2(l2, make_float2(alpha, alpha));
+                    m_used = m_new;
                 }
+                // P in fp16, two keys per 32-bit column, written over the start of the score buffer
+                // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
+                // sums the fp32 values; their fp16 roundings differ by at most 2^-11 relative each.
+                const float2 mm = make_float2(m_used, m_used);
+                if constexpr (NK <= 64) {
+#pragma unroll
+                    for (int c = 0; c < RC; ++c) {
+                        uint32_t pw[CW / 2];
+#pragma unroll
+                        for (int i = 0; i < CW / 2; ++i) {
+                            const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[c][2 * i]),
+                                                                   __uint_as_float(sr[c][2 * i + 1])), mm);
+                            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+                            l2 = add_f32x2(l2, pp);
+                            const __half2 h = __floats2half2_rn(pp.x, pp.y);
+                            pw[i] = *reinterpret_cast<const uint32_t *>(&h);
+                        }
+                        tmem_st_half_chunk<CW>(tsp + (CW / 2) * c, pw);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < NK / 32; ++c) {
+                        tmem_ld32(tsp + 32 * c, sr[0]);
+                        tmem_wait_ld();
+                        if (32 * c + 32 > valid) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (32 * c + i >= valid) sr[0][i] = __float_as_uint(-INFINITY);
+                        }
+                        uint32_t pw[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[0][2 * i]),
+                                                                   __uint_as_float(sr[0][2 * i + 1])), mm);
+                            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+                            l2 = add_f32x2(l2, pp);
+                            const __half2 h = __floats2half2_rn(pp.x, pp.y);
+                            pw[i] = *reinterpret_cast<const uint32_t *>(&h);
+                        }
+                        tmem_st16(tsp + 16 * c, pw);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
-        }
         }   // pieces
         const float l_run = l2.x + l2.y;
         if (ok && !mbar_wait_bounded(o_final, (nseg - 1) & 1, limit)) ok = false;
