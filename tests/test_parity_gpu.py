@@ -354,14 +354,21 @@ def test_errors_are_reported_not_raised_on_device():
     assert plan.sync_status() == B.DG_OK
 
 
-def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable():
+@pytest.mark.parametrize("schedule", [B.DG_SCHEDULE_SPLIT, B.DG_SCHEDULE_STREAM_K],
+                         ids=["split", "stream_k"])
+def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable(schedule):
     """Failure detection without a fault: the softmax withholds one P-ready signal (a flag that
     nothing else sets), every wait behind it runs out after the short limit, the kernel unwinds
-    (TMEM freed, loads drained) and the host reads DG_ERR_TIMEOUT; the next forward is exact."""
-    T, ctx, nh, nkv, hd = 40, 300, 4, 2, 256
+    (TMEM freed, loads drained) and the host reads DG_ERR_TIMEOUT; the next forward is exact.
+    With the stream-K schedule most CTAs hold two pieces, so the waits between them (Q reload,
+    O hand-over) run out too."""
+    T, ctx, nh, nkv, hd = (40, 300, 4, 2, 256) if schedule == B.DG_SCHEDULE_SPLIT else \
+                          (130, 1500, 8, 4, 256)
     d = make_inputs(T, ctx, nh, nkv, hd, seed=31)
     dd = to_dev(d)
     plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_SCHEDULE, schedule)
+    assert plan.get(B.DG_INFO_SCHEDULE_USED) == schedule
     plan.set(B.DG_OPT_WAIT_LIMIT_MS, 100).set(B.DG_OPT_INJECT_STALL, 1)
     plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["k_cache"], dd["v_cache"],
                  dd["q_norm_w"], dd["k_norm_w"])
@@ -369,7 +376,11 @@ def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable():
     assert plan.sync_status() == B.DG_OK          # read-and-clear
     plan.set(B.DG_OPT_INJECT_STALL, 0)
     out = run_forward(plan, dd)
-    check(out, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, [(0, T)], "after-timeout")
+    ranges = row_ranges(T)
+    ref = np.zeros((T, nh * hd))
+    for a, b in ranges:
+        ref[a:b] = oracle_out(d, nh, nkv, hd, rows=(a, b))[a:b]
+    check(out, ref, B.DG_PATH_TC, ranges, "after-timeout")
 
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
