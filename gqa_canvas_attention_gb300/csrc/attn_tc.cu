@@ -2,9 +2,13 @@
 // src/diffusion_gemma_gpu.rs", item DG_ATTN: GQA bidirectional attention, scaling 1.0, no mask,
 // keys = [cache | canvas] of kv head g = h / (nh/nkv)), written for sm_103a.
 //
-// Work unit: one CTA per (128-row query tile, kv group, key-range partition).  The G query heads
-// of a kv group are packed into the MMA M dimension (row R = t*G + h mod G), so each K/V tile is
-// staged once for all of them.
+// Work unit: one CTA per (128-row query tile, kv group, key-range partition) with the split
+// schedule (2..8 partitions of a query tile form a thread-block cluster and merge in the kernel);
+// with the stream-K schedule one CTA per SM, each an equal run of key tiles over the (query tile,
+// kv group) pairs in order, so a CTA may hold the end of one pair and the start of the next (two
+// "pieces", merged afterwards by the combine kernel).  The G query heads of a kv group are packed
+// into the MMA M dimension (row R = t*G + h mod G), so each K/V tile is staged once for all of
+// them.
 //
 // Precision (scores reach |s| ~ 90 because of scaling 1.0, so one TF32 rounding of q or k moves
 // outputs by ~1e-2): Q.K^T is computed as  qh.kh + qh.kl + ql.kh  with bf16 hi/lo splits of both
