@@ -142,20 +142,25 @@ __global__ void __launch_bounds__(32 * kCombineRowsPerCta) combine_kernel(Combin
                                          acc[v].w * inv);
 }
 
-// Stream-K pieces: one CTA per (128-row query tile, kv group, 32 columns), one thread per row
-// (blockIdx.z picks the columns: the merge of a tile is spread over hd/32 CTAs).  The pair's
-// pieces are those of CTAs sk_cta_of(p * n_tiles) .. sk_cta_of((p + 1) * n_tiles - 1) of the
-// attention kernel, in that order (deterministic).  A piece's O rows are row-interleaved, so each
-// load instruction of a warp reads 512 contiguous bytes; the merged rows go out through a
-// shared-memory transpose, 128 contiguous bytes of 4 rows per store instruction.
+// Stream-K pieces: one CTA per (128-row query tile, kv group, 8 columns), one thread per row.
+// The pair's pieces are those of CTAs sk_cta_of(p * n_tiles) .. sk_cta_of((p + 1) * n_tiles - 1)
+// of the attention kernel, merged in that order (deterministic):
 //   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k.
+// Every load of a thread (the (m, l) and the 2 float4 of its columns of up to 8 pieces) is in
+// flight at once: one round trip to memory and a store.  A piece's O rows are row-interleaved,
+// so each load instruction of a warp reads 512 contiguous bytes; the merged rows go out through a
+// shared-memory transpose, 32 contiguous bytes of 16 rows per store instruction.  (Tried on the
+// GB300, 48-step workload: 32 columns per thread in 4-piece batches, 16 columns per thread, and a
+// one-CTA-per-SM loop over the units; this layout was the fastest, ~8 us of a forward.)
+constexpr int kSkBatch = 8;
+
 template <int HD>
 __global__ void __launch_bounds__(kTileM) combine_sk_kernel(CombineParams p)
 {
     pdl_launch_dependents();
     pdl_wait();   // the pieces come from the attention kernel just before
-    __shared__ float stage[kTileM / 32][32 * 36];
-    const int qt = blockIdx.x, g = blockIdx.y, c = blockIdx.z;
+    __shared__ float stage[kTileM / 32][32 * 12];
+    const int qt = blockIdx.x, g = blockIdx.y, c8 = blockIdx.z;    // columns 8*c8 ..
     const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
     const int pr = g * p.qtiles + qt;
     const long long U = p.sk_units;
@@ -164,74 +169,68 @@ __global__ void __launch_bounds__(kTileM) combine_sk_kernel(CombineParams p)
     const int R = qt * kTileM + r;
     const size_t stride = (size_t)p.nkv * p.rows_pad;           // rows between slots
     const size_t row = (size_t)g * p.rows_pad + R;
-    float w[kMaxStreamKPieces];
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kMaxStreamKPieces; ++k) {
-        w[k] = -INFINITY;
-        if (k < np) {
-            const float2 ml = p.part_ml[k * stride + row];
-            w[k] = ml.x;
-            M = fmaxf(M, ml.x);
-        }
-    }
-    float den = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxStreamKPieces; ++k) {
-        if (k < np) {
-            const float e = exp2f(w[k] - M);
-            den = fmaf(e, p.part_ml[k * stride + row].y, den);
-            w[k] = e;
-        } else {
-            w[k] = 0.f;
-        }
-    }
-    const float inv = 1.0f / den;
-    float *mydst = R < p.rows ? p.out + ((size_t)(R / p.G) * p.nh + g * p.G + R % p.G) * HD
-                              : nullptr;
     // float4 units of this tile in slot k: (slot tile base + u) * 128 + r
     const float4 *src = reinterpret_cast<const float4 *>(p.part_o) +
                         ((size_t)g * p.rows_pad + (size_t)qt * kTileM) * (HD / 4) + r;
     const size_t slot_stride = stride * (HD / 4);
-    float *stg = stage[warp];
-    const int sub = lane & 7, rsub = lane >> 3;
-    // the pieces four at a time, all 32 loads of a batch in flight before any arithmetic
-    float4 acc[8];
+    float M = -INFINITY, den = 0.f;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k0 = 0; k0 < np; k0 += kSkBatch) {
+        float2 ml[kSkBatch];
+        float4 o[kSkBatch][2];
 #pragma unroll
-    for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < kSkBatch; ++k) {
+            ml[k] = make_float2(-INFINITY, 0.f);
+            o[k][0] = o[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k0 + k < np) {
+                ml[k] = p.part_ml[(k0 + k) * stride + row];
 #pragma unroll
-    for (int k0 = 0; k0 < kMaxStreamKPieces; k0 += 4) {
-        if (k0 >= np) break;
-        float4 o[4][8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                o[k][v] = k0 + k < np ? src[(k0 + k) * slot_stride + (size_t)(8 * c + v) * kTileM]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float wk = k0 + k < np ? w[k0 + k] * inv : 0.f;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                acc[v].x = fmaf(wk, o[k][v].x, acc[v].x);
-                acc[v].y = fmaf(wk, o[k][v].y, acc[v].y);
-                acc[v].z = fmaf(wk, o[k][v].z, acc[v].z);
-                acc[v].w = fmaf(wk, o[k][v].w, acc[v].w);
+                for (int v = 0; v < 2; ++v)
+                    o[k][v] = src[(k0 + k) * slot_stride + (size_t)(2 * c8 + v) * kTileM];
             }
         }
+        // fold the batch in with a running reference (the first batch sets it)
+        float Mb = M;
+#pragma unroll
+        for (int k = 0; k < kSkBatch; ++k) Mb = fmaxf(Mb, ml[k].x);
+        const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mb);
+        den *= rescale;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            acc[v].x *= rescale; acc[v].y *= rescale; acc[v].z *= rescale; acc[v].w *= rescale;
+        }
+#pragma unroll
+        for (int k = 0; k < kSkBatch; ++k) {
+            const float w = k0 + k < np ? exp2f(ml[k].x - Mb) : 0.f;
+            den = fmaf(w, ml[k].y, den);
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                acc[v].x = fmaf(w, o[k][v].x, acc[v].x);
+                acc[v].y = fmaf(w, o[k][v].y, acc[v].y);
+                acc[v].z = fmaf(w, o[k][v].z, acc[v].z);
+                acc[v].w = fmaf(w, o[k][v].w, acc[v].w);
+            }
+        }
+        M = Mb;
     }
+    const float inv = 1.0f / den;
+    float *mydst = R < p.rows ? p.out + ((size_t)(R / p.G) * p.nh + g * p.G + R % p.G) * HD
+                              : nullptr;
+    float *stg = stage[warp];
 #pragma unroll
-    for (int v = 0; v < 8; ++v) *reinterpret_cast<float4 *>(stg + lane * 36 + 4 * v) = acc[v];
+    for (int v = 0; v < 2; ++v)
+        *reinterpret_cast<float4 *>(stg + lane * 12 + 4 * v) =
+            make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
     __syncwarp();
+    const int sub = lane & 1, rsub = lane >> 1;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int j = 4 * k + rsub;
+    for (int k = 0; k < 2; ++k) {
+        const int j = 16 * k + rsub;
         float *d = reinterpret_cast<float *>(
             __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mydst), j));
         if (d)
-            *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) =
-                *reinterpret_cast<const float4 *>(stg + j * 36 + 4 * sub);
+            *reinterpret_cast<float4 *>(d + 8 * c8 + 4 * sub) =
+                *reinterpret_cast<const float4 *>(stg + j * 12 + 4 * sub);
     }
 }
 
@@ -256,7 +255,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
     if (p.sk_ctas > 0) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(p.qtiles, p.nkv, p.hd / 32);
+        cfg.gridDim = dim3(p.qtiles, p.nkv, p.hd / 8);
         cfg.blockDim = dim3(kTileM);
         cfg.stream = s;
         cudaLaunchAttribute attr[1] = {pdl_attribute()};
