@@ -34,7 +34,7 @@ EXPORTED = [
     "dg_attn_norm_rope",
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
-    "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error",
+    "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error", "dg_attn_schedule_info",
 ]
 
 _lib = None
@@ -96,8 +96,27 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_forward_noalloc.restype = I
     lib.dg_attn_noalloc_last_error.argtypes = []
     lib.dg_attn_noalloc_last_error.restype = ctypes.c_char_p
+    lib.dg_attn_schedule_info.argtypes = [I, I, I, I, I, I, P, I, P]
+    lib.dg_attn_schedule_info.restype = I
     _lib = lib
     return lib
+
+
+def dg_attn_schedule_info(nh, nkv, hd, ctx, T, num_sms, max_clusters=None,
+                          schedule=DG_SCHEDULE_AUTO):
+    """The tensor-core schedule a plan of this geometry would use (host arithmetic, no GPU):
+    (schedule, partitions or most pieces of a pair, CTAs, key tiles of the longest run)."""
+    lib = _lib or load()
+    out = (ctypes.c_longlong * 4)()
+    mc = None
+    if max_clusters is not None:
+        mc = (ctypes.c_int * len(max_clusters))(*max_clusters)
+    rc = lib.dg_attn_schedule_info(nh, nkv, hd, ctx, T, num_sms,
+                                   ctypes.cast(mc, ctypes.c_void_p) if mc is not None else None,
+                                   schedule, out)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_attn_schedule_info")
+    return tuple(int(v) for v in out)
 
 
 def status_string(status: int) -> str:

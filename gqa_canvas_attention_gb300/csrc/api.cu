@@ -640,6 +640,46 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     return p;
 }
 
+int dg_attn_schedule_info(int nh, int nkv, int hd, int ctx, int T, int num_sms,
+                          const int *max_clusters, int schedule, long long *out)
+{
+    if (!out || nh < 1 || nkv < 1 || T < 1 || ctx < 0 || nh % nkv != 0 || num_sms < 1 ||
+        (hd != 64 && hd != 128 && hd != 256) ||
+        (schedule != DG_SCHEDULE_AUTO && schedule != DG_SCHEDULE_SPLIT &&
+         schedule != DG_SCHEDULE_STREAM_K)) {
+        set_error("dg_attn_schedule_info: bad arguments");
+        return DG_ERR_ARG;
+    }
+    // the plan fields the schedule choice reads, as dg_attn_plan_create sets them
+    dg_attn_plan p{};
+    p.nh = nh; p.nkv = nkv; p.hd = hd; p.ctx = ctx; p.T = T;
+    p.G = nh / nkv; p.S = ctx + T; p.rows = T * p.G;
+    p.rows_pad = ((p.rows + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
+    p.tc_ok = true;
+    p.path = DG_PATH_TC;
+    p.splits_opt = 0;
+    p.schedule_opt = schedule;
+    p.num_sms = num_sms;
+    p.part_capacity = 1 << 30;   // no clamp by buffers
+    for (int s = 0; s <= dg::kMaxClusterSplits; ++s)
+        p.max_clusters[s] = s < 2 ? 0 : (max_clusters ? max_clusters[s] : num_sms / s);
+    SkLayout L;
+    if (use_stream_k(&p, L)) {
+        out[0] = DG_SCHEDULE_STREAM_K;
+        out[1] = L.kmax;
+        out[2] = L.ctas;
+        out[3] = (L.units + L.ctas - 1) / L.ctas;
+    } else {
+        int s, tps, nt;
+        split_layout(&p, s, tps, nt);
+        out[0] = DG_SCHEDULE_SPLIT;
+        out[1] = s;
+        out[2] = (long long)qtiles_for(&p) * s;
+        out[3] = tps;
+    }
+    return DG_OK;
+}
+
 void dg_attn_plan_destroy(dg_attn_plan *p)
 {
     if (!p) return;

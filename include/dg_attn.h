@@ -103,6 +103,19 @@ typedef struct dg_attn_plan dg_attn_plan;
 dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float eps,
                                   float rope_theta);
 
+/* The schedule of the tensor-core attention kernel that a plan of this geometry would use, on a
+ * device with `num_sms` SMs on which max_clusters[s] thread-block clusters of s CTAs (s = 2..8;
+ * entries 0 and 1 unused) fit at once, or num_sms / s of each when max_clusters is NULL; with
+ * DG_OPT_SPLITS left at 0.  schedule: DG_SCHEDULE_AUTO, _SPLIT or _STREAM_K, as for
+ * DG_OPT_SCHEDULE (a stream-K request the geometry cannot take falls back to the split schedule,
+ * as a forward would).  Host arithmetic only: touches no device and needs no GPU.
+ * out[4]: [0] DG_SCHEDULE_SPLIT or DG_SCHEDULE_STREAM_K; [1] key partitions per query tile
+ * (split) or the most pieces any (query tile, kv group) pair is cut into (stream-K); [2] CTAs of
+ * the attention kernel; [3] key tiles in the longest CTA's run.  hd must be 64, 128 or 256.
+ * Returns DG_ERR_ARG (with dg_attn_last_error()) for a bad geometry or a NULL out. */
+int dg_attn_schedule_info(int nh, int nkv, int hd, int ctx, int T, int num_sms,
+                          const int *max_clusters, int schedule, long long *out);
+
 /* The whole block: norms + RoPE, attention, output.  k_cache and v_cache are [nkv, ctx, hd];
  * with ctx == 0 they must be NULL.  With ctx > 0 and both NULL the plan uses the cache copy made
  * by the last dg_attn_cache_prepare (DG_ERR_STATE if there is none).  v_canvas may alias
