@@ -578,16 +578,20 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }   // TMEM access is warp-wide
                 tc_fence_after();
                 const uint32_t tsp = tbase + lane_off + C::SP_COL + b * NK;
-                // NK <= 64: the whole score row stays in registers; NK = 128: the maximum is taken in
-                // a first pass and the scores are read again (register budget of 320 threads)
+                // The whole score row stays in registers (one pass over TMEM) when the register
+                // budget allows: always at NK <= 64, and at NK = 128 with 256 threads (~194
+                // registers; at hd = 64 this single pass took the kernel from 137.7 to 109.3 us
+                // on the 4-canvas workload).  Otherwise the maximum is taken in a first pass and
+                // the scores are read again.
+                constexpr bool ROW_REGS = NK <= 64 || Lay::THREADS <= 256;
                 constexpr int CW = NK % 32 == 0 ? 32 : 16;            // columns per score chunk
-                constexpr int RC = NK <= 64 ? NK / CW : 1;
+                constexpr int RC = ROW_REGS ? NK / CW : 1;
                 uint32_t sr[RC][CW];
                 // keys of this tile below S; only the last tile of the key range is partial, so the
                 // masking branch is warp-uniform and almost never taken
                 const int valid = p.S - (tile0 + (it - base)) * NK;
                 float mx;
-                if constexpr (NK <= 64) {
+                if constexpr (ROW_REGS) {
 #pragma unroll
                     for (int c = 0; c < RC; ++c) tmem_ld_chunk<CW>(tsp + CW * c, sr[c]);
                     tmem_wait_ld();
@@ -670,7 +674,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
                 // sums the fp32 values; their fp16 roundings differ by at most 2^-11 relative each.
                 const float2 mm = make_float2(m_used, m_used);
-                if constexpr (NK <= 64) {
+                if constexpr (ROW_REGS) {
 #pragma unroll
                     for (int c = 0; c < RC; ++c) {
                         uint32_t pw[CW / 2];
