@@ -34,13 +34,18 @@ def weights(H, nh, nkv, hd, seed, with_v=True):
                                    (256, 1024, 8, 4, 256, 1024)],
                          ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d_H%d" % s)
 @pytest.mark.parametrize("with_v", [True, False], ids=["wv", "k_eq_v"])
-def test_hidden_to_output_parity(shape, with_v):
+@pytest.mark.parametrize("schedule", [B.DG_SCHEDULE_AUTO, B.DG_SCHEDULE_STREAM_K],
+                         ids=["auto", "stream_k"])
+def test_hidden_to_output_parity(shape, with_v, schedule):
     T, ctx, nh, nkv, hd, H = shape
     d = make_inputs(T, ctx, nh, nkv, hd, seed=71)
     x = torch.randn(T, H, generator=torch.Generator().manual_seed(72), dtype=torch.float32)
     ln, wq, wk, wv = weights(H, nh, nkv, hd, 73, with_v)
     cu = lambda t: None if t is None else t.cuda()
     plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_SCHEDULE, schedule)
+    if schedule == B.DG_SCHEDULE_STREAM_K:
+        assert plan.get(B.DG_INFO_SCHEDULE_USED) == B.DG_SCHEDULE_STREAM_K
     plan.proj_prepare(H, cu(ln), cu(wq), cu(wk), cu(wv))
     out = plan.forward_hidden(cu(x), cu(d["k_cache"]), cu(d["v_cache"]), cu(d["q_norm_w"]),
                               cu(d["k_norm_w"]))
