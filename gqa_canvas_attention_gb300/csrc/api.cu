@@ -1191,6 +1191,11 @@ int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
     err = cudaMemcpy(&st, p->status, sizeof(st), cudaMemcpyDeviceToHost);
     if (err == cudaSuccess) err = cudaMemset(p->status, 0, sizeof(uint32_t));
     if (err != cudaSuccess) return cuda_fail(err, "reading the status word");
+    if (st & dg::kErrSchedule) {
+        set_error("a stream-K run covered more than two (query tile, kv group) pairs (status 0x%x)",
+                  st);
+        return DG_ERR_STATE;
+    }
     if (st) {
         set_error("a device wait ran out (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 drain)",
                   st);

@@ -164,8 +164,10 @@ int dg_attn_attend(dg_attn_plan *plan, const float *q_hat, const float *k_hat,
 int dg_attn_set_option(dg_attn_plan *plan, int key, long long value);
 int dg_attn_get_option(const dg_attn_plan *plan, int key, long long *value);
 
-/* Synchronise `stream`, then read and clear the plan's device status word: DG_OK, or
- * DG_ERR_TIMEOUT when a kernel gave up on a bounded wait since the last call. */
+/* Synchronise `stream`, then read and clear the plan's device status word: DG_OK;
+ * DG_ERR_TIMEOUT when a kernel gave up on a bounded wait since the last call; DG_ERR_STATE when a
+ * stream-K CTA was handed a run it cannot hold (more than two pairs; the host layout rules this
+ * out). */
 int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 
 /* Stages for dg_attn_profile_read. */
