@@ -250,7 +250,8 @@ bool sk_layout(const dg_attn_plan *p, SkLayout &L)
     long long C = p->num_sms;
     if (C > U) C = U;
     // no pair in more pieces than the combine merges: fewer CTAs when the pairs are few
-    if (C > (long long)pairs * (dg::kMaxStreamKPieces - 1)) C = (long long)pairs * (dg::kMaxStreamKPieces - 1);
+    const long long c_cap = (long long)pairs * (dg::kMaxStreamKPieces - 1);
+    if (C > c_cap) C = c_cap;
     if (C < pairs) return false;
     int kmax = 0;
     for (;;) {
