@@ -544,13 +544,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             m_used = -INFINITY;
             l2 = make_float2(0.f, 0.f);
             {
-                // Start the reference from the maximum over the piece's first 128 keys (the
-                // first NW score tiles, computed back to back), not the first tile alone: the
-                // running maximum then grows less, and O is rescaled less often.  Waiting for
-                // more tiles delayed the first softmax (all NSP tiles: 1.3% slower at hd = 64).
-                // A buffer's first phase is waited for again in the loop below; that wait
-                // returns at once.
-                constexpr int NW = NK >= 128 ? 1 : (128 / NK < NSP ? 128 / NK : NSP);
+                // Start the reference from the maximum over the piece's first score tile (plus
+                // the headroom, which keeps later rescales rare).  Waiting for more tiles to
+                // take a wider maximum delayed the first softmax, and with it the first P.V and
+                // the refill of that buffer: two tiles at hd = 256 were 2.4% slower, all three
+                // buffers at hd = 64 1.3%.  A buffer's first phase is waited for again in the
+                // loop below; that wait returns at once.
+                constexpr int NW = 1;
                 const int nw = min(NW, nloc);
                 float m0 = -INFINITY;
                 for (int t = 0; t < nw; ++t) {
