@@ -29,7 +29,7 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio of th
 # DRAM bytes (read + write) per launch of the tensor-core attention kernel on the bench workload,
 # from one ncu capture (profiles/attn_tc_kernel_denoise48_ctx8k.md), valid only for the kernel
 # source it was taken on: the bench reports null once attn_tc.cu has changed.
-ATTN_TRAFFIC = {"source_sha1_prefix": "3b59494f6536", "bytes": 59.77e6}
+ATTN_TRAFFIC = {"source_sha1_prefix": "ff27378fde19", "bytes": 59.92e6}
 
 
 def attn_traffic():
