@@ -33,9 +33,9 @@
 //            that hand-over, not the tensor pipe, set the pace of the loop;
 //   warps 4-7 softmax: thread = one query row = one TMEM lane.  They put Q into TMEM, turn each
 //            score tile S (TMEM) into P = 2^(s*log2e - m) rounded to fp16, packed two per column
-//            over the start of S, keep the fp32 running max m and denominator l, rescale O in TMEM when the max
-//            has grown by more than 15 (log2 units; so P <= 2^15 in between), and write the
-//            output.
+//            over the start of S, keep the fp32 running max m and the denominator l (the sum of
+//            those fp16 values), rescale O in TMEM when the max has grown by more than 15 (log2
+//            units; so P <= 2^15 in between), and write the output.
 // TMEM: O [128 x hd] fp32, Q hi (bf16 pairs), Q lo (hd <= 128), NSP score/probability buffers.
 // hd = 256 uses 64-key score tiles in two buffers (TMEM holds 128 columns for them): the product
 // ql.kh takes its Q lo operand from shared memory (4 KiB per k-step), so wider tiles read it
@@ -106,13 +106,14 @@ template <int HD> struct Layout {
     static_assert(C::NK % C::VK == 0 && C::VK % 16 == 0, "V stages tile a score tile");
 };
 
-// log2 units: P stays <= 2^15 between rescales, inside the fp16 range (65504).  A rescale of O
-// (which every row of a warp takes when any one row needs it) sets the reference kHeadroom above
-// the row maximum, so the maximum may grow by 15 + 8 before the next one; the largest P of a row
-// stays >= 2^-8, a normal fp16 number with its full 11-bit precision, and the keys that fall into
-// the subnormal range (2^-6 or less of the largest) are off by at most 2^-25 each.
+// log2 units.  Each row's reference m is the row maximum seen at the last rescale (or over the
+// first score tile), so it never exceeds the row's running maximum: the largest P of a row is
+// >= 1, and every key within 14 of the row maximum gets a normal fp16 P with its full 11-bit
+// precision.  Keys further below fall into the fp16 subnormal range, each off by at most 2^-25
+// against a denominator >= 1, so even S = 8704 such keys move the weights by at most 2.6e-4
+// relative.  O is rescaled when a row's maximum exceeds m + 15, so P <= 2^15 (inside the fp16
+// range, 65504) in between.
 constexpr float kRescaleThreshold = 15.0f;
-constexpr float kHeadroom = 8.0f;
 
 // Rows [r0, r0 + nr) of the in-cluster merge of P partitions: out = sum_p w_p O_p with the
 // per-row weights w (already divided by the merged denominator).  The staged O rows are read
@@ -544,12 +545,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             m_used = -INFINITY;
             l2 = make_float2(0.f, 0.f);
             {
-                // Start the reference from the maximum over the piece's first score tile (plus
-                // the headroom, which keeps later rescales rare).  Waiting for more tiles to
-                // take a wider maximum delayed the first softmax, and with it the first P.V and
-                // the refill of that buffer: two tiles at hd = 256 were 2.4% slower, all three
-                // buffers at hd = 64 1.3%.  A buffer's first phase is waited for again in the
-                // loop below; that wait returns at once.
+                // Start the reference from the maximum over the piece's first score tile.
+                // Waiting for more tiles to take a wider maximum delayed the first softmax, and
+                // with it the first P.V and the refill of that buffer: two tiles at hd = 256 were
+                // 2.4% slower, all three buffers at hd = 64 1.3%.  A buffer's first phase is
+                // waited for again in the loop below; that wait returns at once.
                 constexpr int NW = 1;
                 const int nw = min(NW, nloc);
                 float m0 = -INFINITY;
@@ -570,7 +570,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                             if (CW * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
                     }
                 }
-                if (ok && nw > 0) m_used = m0 + kHeadroom;
+                if (ok && nw > 0) m_used = m0;
             }
             for (int it = base; ok && it < base + nloc; ++it) {
                 const int b = it % NSP;
@@ -630,7 +630,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 }
                 const bool need = mx > m_used + kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = fmaxf(m_used, mx + kHeadroom);
+                    const float m_new = fmaxf(m_used, mx);
                     const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
                     if (it > base) {
                         // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
@@ -672,7 +672,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                 }
                 // P in fp16, two keys per 32-bit column, written over the start of the score buffer
                 // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
-                // sums the fp32 values; their fp16 roundings differ by at most 2^-11 relative each.
+                // sums the same fp16 values that P.V multiplies (widened exactly), so numerator and
+                // denominator carry one set of roundings: a single dominant key returns its V.
                 const float2 mm = make_float2(m_used, m_used);
                 if constexpr (ROW_REGS) {
 #pragma unroll
@@ -682,10 +683,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         for (int i = 0; i < CW / 2; ++i) {
                             const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[c][2 * i]),
                                                                    __uint_as_float(sr[c][2 * i + 1])), mm);
-                            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-                            l2 = add_f32x2(l2, pp);
-                            const __half2 h = __floats2half2_rn(pp.x, pp.y);
+                            const __half2 h = __floats2half2_rn(ex2_approx(d.x), ex2_approx(d.y));
                             pw[i] = *reinterpret_cast<const uint32_t *>(&h);
+                            add_f16x2_to_f32x2(l2, pw[i]);
                         }
                         tmem_st_half_chunk<CW>(tsp + (CW / 2) * c, pw);
                     }
@@ -704,10 +704,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         for (int i = 0; i < 16; ++i) {
                             const float2 d = sub_f32x2(make_float2(__uint_as_float(sr[0][2 * i]),
                                                                    __uint_as_float(sr[0][2 * i + 1])), mm);
-                            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-                            l2 = add_f32x2(l2, pp);
-                            const __half2 h = __floats2half2_rn(pp.x, pp.y);
+                            const __half2 h = __floats2half2_rn(ex2_approx(d.x), ex2_approx(d.y));
                             pw[i] = *reinterpret_cast<const uint32_t *>(&h);
+                            add_f16x2_to_f32x2(l2, pw[i]);
                         }
                         tmem_st16(tsp + 16 * c, pw);
                     }

@@ -13,13 +13,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
@@ -169,13 +162,6 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t caddr)
     return v;
 }
 
-__device__ __forceinline__ void dsmem_st_f4(uint32_t caddr, float4 v)
-{
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t caddr)
 {
     float v;
@@ -256,53 +242,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, uint32_t a_mn
            | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]   (A from tensor memory)
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued before has completed.
-__device__ __forceinline__ void mma_commit(uint64_t *bar)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
 // ------------------------------------------------------------------ warp-uniform MMA issue
 
 // 1 in the one lane of a converged warp that elect.sync picks (the lowest active lane), else 0.
@@ -314,8 +253,10 @@ __device__ __forceinline__ uint32_t elect_one_sync()
     return r;
 }
 
-// The MMAs and commit above, called by every lane of a warp; only the lane with `issue` set
-// executes the instruction (a guard predicate, no branch).
+// kind::f16 MMAs (D[tmem] (+)= A * B, A from tensor memory (_ts) or shared memory (_ss), B from
+// shared memory) and the commit that arrives on an mbarrier once every tcgen05 operation the
+// thread issued before has completed.  Called by every lane of a warp; only the lane with `issue`
+// set executes the instruction (a guard predicate, no branch).
 __device__ __forceinline__ void mma_bf16_ts_by(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem,
                                                uint64_t b_desc, uint32_t idesc, uint32_t accumulate)
 {
@@ -405,14 +346,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------------------ number formats
 
-// fp32 -> tf32 with round-to-nearest, ties away from zero (low 13 bits cleared).
-__device__ __forceinline__ uint32_t f32_to_tf32_rna(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
 // 2^x on the special-function unit (hardware approximation, a single instruction).
 __device__ __forceinline__ float ex2_approx(float x)
 {
@@ -458,6 +391,15 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
         "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// l += the two fp16 values packed in h2 (low half into l.x, high half into l.y), each widened
+// exactly and added in fp32 with one rounding: the mixed-precision add of sm_100 and later.
+__device__ __forceinline__ void add_f16x2_to_f32x2(float2 &l, uint32_t h2)
+{
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(l.x), "+f"(l.y) : "r"(h2));
 }
 
 }  // namespace dg
