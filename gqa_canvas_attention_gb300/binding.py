@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_PKG, "libdgattn.so")
 
 # status codes and option keys (mirrors include/dg_attn.h)
 DG_OK, DG_ERR_ARG, DG_ERR_ALIGN, DG_ERR_CUDA, DG_ERR_TIMEOUT, DG_ERR_UNSUPPORTED, DG_ERR_STATE = range(7)
+DG_ERR_RANGE = 7
 DG_PATH_TC, DG_PATH_FP32 = 0, 1
 DG_OPT_PATH, DG_OPT_POS0, DG_OPT_SPLITS, DG_OPT_WAIT_LIMIT_MS, DG_OPT_PROFILE = 1, 2, 3, 4, 5
 DG_OPT_INJECT_STALL = 6
@@ -35,6 +36,7 @@ EXPORTED = [
     "dg_attn_attend", "dg_attn_set_option", "dg_attn_get_option", "dg_attn_sync_status",
     "dg_attn_profile_read", "dg_attn_plan_destroy", "dg_attn_status_string", "dg_attn_last_error",
     "dg_attn_forward_noalloc", "dg_attn_noalloc_last_error", "dg_attn_schedule_info",
+    "dg_attn_build_id",
 ]
 
 _lib = None
@@ -98,6 +100,8 @@ def load(path: str = LIB_PATH):
     lib.dg_attn_noalloc_last_error.restype = ctypes.c_char_p
     lib.dg_attn_schedule_info.argtypes = [I, I, I, I, I, I, P, I, P]
     lib.dg_attn_schedule_info.restype = I
+    lib.dg_attn_build_id.argtypes = []
+    lib.dg_attn_build_id.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -119,6 +123,11 @@ def dg_attn_schedule_info(nh, nkv, hd, ctx, T, num_sms, max_clusters=None,
     return tuple(int(v) for v in out)
 
 
+def build_id() -> str:
+    """The loaded library's build identity ("sha1:<hex>" of its sources)."""
+    return load().dg_attn_build_id().decode()
+
+
 def status_string(status: int) -> str:
     return load().dg_attn_status_string(int(status)).decode()
 
@@ -128,12 +137,42 @@ def last_error() -> str:
 
 
 def _ptr(t):
-    """Device (or host) address of a tensor, or None."""
+    """Address of a tensor (or a raw integer address), or None.  A tensor must be contiguous:
+    the library reads dense row-major buffers."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("the library reads dense row-major buffers: pass a contiguous tensor")
     return t.data_ptr()
+
+
+def _check_tensors(device, *specs):
+    """Reject, before any library call, a tensor the library would misread.  Each spec is
+    (tensor or None, name, element count[, dtypes]); every tensor is first checked for its type,
+    dtype (float32 unless given), contiguity and element count, then all of them for living on
+    the plan's CUDA device."""
+    import torch
+    for spec in specs:
+        t, name, numel = spec[:3]
+        dtypes = spec[3] if len(spec) > 3 else (torch.float32,)
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+        if t.dtype not in dtypes:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous (dense row-major)")
+        if t.numel() != numel:
+            raise ValueError(f"{name}: {t.numel()} elements ({tuple(t.shape)}), expected {numel}")
+    for spec in specs:
+        t, name = spec[:2]
+        if t is not None and (t.device.type != "cuda" or
+                              (device is not None and t.device.index != device)):
+            raise ValueError(f"{name}: must live on cuda:{device} (the plan's device), not "
+                             f"{t.device}")
 
 
 def _stream(stream):
@@ -244,9 +283,9 @@ def dg_attn_get_option(plan, key) -> int:
 
 
 def dg_attn_sync_status(plan, stream=None) -> int:
-    """Returns the status (DG_OK or DG_ERR_TIMEOUT) instead of raising on a device timeout."""
+    """Returns the device status (DG_OK, DG_ERR_TIMEOUT or DG_ERR_RANGE) instead of raising."""
     rc = load().dg_attn_sync_status(plan, _stream(stream))
-    if rc not in (DG_OK, DG_ERR_TIMEOUT):
+    if rc not in (DG_OK, DG_ERR_TIMEOUT, DG_ERR_RANGE):
         raise DgAttnError(rc, "dg_attn_sync_status")
     return rc
 
@@ -263,8 +302,29 @@ class Plan:
     """Owning handle around a dg_attn_plan (created on the current CUDA device)."""
 
     def __init__(self, nh, nkv, hd, ctx, T, eps=1e-6, rope_theta=10000.0):
+        import torch
         self.nh, self.nkv, self.hd, self.ctx, self.T = nh, nkv, hd, ctx, T
+        self.H = self.oH = None
+        self.device = torch.cuda.current_device()
         self.handle = dg_attn_plan_create(nh, nkv, hd, ctx, T, eps, rope_theta)
+
+    # element counts of the buffers of this geometry
+    def _nq(self):
+        return self.T * self.nh * self.hd
+
+    def _nk(self):
+        return self.T * self.nkv * self.hd
+
+    def _nc(self):
+        return self.nkv * self.ctx * self.hd
+
+    def _check_canvas(self, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                      out, q_name="q", k_name="k_canvas", v_name="v_canvas"):
+        _check_tensors(self.device, (q, q_name, self._nq()), (k_canvas, k_name, self._nk()),
+                       (v_canvas, v_name, self._nk()), (k_cache, "k_cache", self._nc()),
+                       (v_cache, "v_cache", self._nc()), (q_norm_w, "q_norm_w", self.hd),
+                       (k_norm_w, "k_norm_w", self.hd), (cos_sin, "cos_sin", 2 * self.T * self.hd),
+                       (out, "out", self._nq()))
 
     def close(self):
         if self.handle:
@@ -289,30 +349,46 @@ class Plan:
         import torch
         if out is None:
             out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=q.device)
+        self._check_canvas(q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                           out)
         dg_attn_forward(self.handle, q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w,
                         cos_sin, out, stream)
         return out
 
     def proj_prepare(self, H, ln_in_w, wq, wk, wv=None, stream=None):
+        _check_tensors(self.device, (ln_in_w, "ln_in_w", H), (wq, "wq", self.nh * self.hd * H),
+                       (wk, "wk", self.nkv * self.hd * H), (wv, "wv", self.nkv * self.hd * H))
         dg_attn_proj_prepare(self.handle, H, ln_in_w, wq, wk, wv, stream)
+        self.H = H
 
     def forward_hidden(self, x, k_cache=None, v_cache=None, q_norm_w=None, k_norm_w=None,
                        cos_sin=None, out=None, stream=None):
         import torch
         if out is None:
             out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=x.device)
+        if self.H is not None:
+            _check_tensors(self.device, (x, "x", self.T * self.H))
+        self._check_canvas(out, None, None, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, None,
+                           q_name="out")
         dg_attn_forward_hidden(self.handle, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out,
                                stream)
         return out
 
     def oproj_prepare(self, H, wo, ln_post_w=None, stream=None):
+        _check_tensors(self.device, (wo, "wo", H * self.nh * self.hd), (ln_post_w, "ln_post_w", H))
         dg_attn_oproj_prepare(self.handle, H, wo, ln_post_w, stream)
+        self.oH = H
 
     def oproj_residual(self, attn_out, resid, stream=None):
+        _check_tensors(self.device, (attn_out, "attn_out", self._nq()),
+                       (resid, "resid", self.T * self.oH if self.oH is not None else resid.numel()))
         dg_attn_oproj_residual(self.handle, attn_out, resid, stream)
 
     def forward_layer(self, resid, k_cache=None, v_cache=None, q_norm_w=None, k_norm_w=None,
                       cos_sin=None, stream=None):
+        if self.H is not None:
+            _check_tensors(self.device, (resid, "resid", self.T * self.H))
+        self._check_canvas(None, None, None, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, None)
         dg_attn_forward_layer(self.handle, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
                               stream)
         return resid
@@ -324,11 +400,14 @@ class Plan:
                  torch.bfloat16: DG_DTYPE_BF16}
         if k_cache.dtype not in types or v_cache.dtype != k_cache.dtype:
             raise ValueError("cache tensors must both be float32, float16 or bfloat16")
+        _check_tensors(self.device, (k_cache, "k_cache", self._nc(), (k_cache.dtype,)),
+                       (v_cache, "v_cache", self._nc(), (k_cache.dtype,)))
         dg_attn_cache_prepare_typed(self.handle, k_cache, v_cache, types[k_cache.dtype], stream)
 
     def norm_rope(self, q, k_canvas, v_canvas, q_norm_w=None, k_norm_w=None, cos_sin=None,
                   stream=None):
         import torch
+        self._check_canvas(q, k_canvas, v_canvas, None, None, q_norm_w, k_norm_w, cos_sin, None)
         qh = torch.empty_like(q)
         kh = torch.empty_like(k_canvas)
         vh = torch.empty_like(v_canvas)
@@ -340,6 +419,8 @@ class Plan:
         import torch
         if out is None:
             out = torch.empty((self.T, self.nh * self.hd), dtype=torch.float32, device=q_hat.device)
+        self._check_canvas(q_hat, k_hat, v_hat, k_cache, v_cache, None, None, None, out,
+                           "q_hat", "k_hat", "v_hat")
         dg_attn_attend(self.handle, q_hat, k_hat, v_hat, k_cache, v_cache, out, stream)
         return out
 

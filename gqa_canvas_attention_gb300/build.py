@@ -26,9 +26,39 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+ATTN_KERNEL_SOURCES = ["attn_tc.cu", "sm103_ptx.cuh", "dg_internal.cuh", "api.cu"]
+
+
+def attn_kernel_source_id() -> str:
+    """sha1 over the files that fix the tensor-core attention kernel and its launch (the kernel,
+    its PTX wrappers, the shared parameter blocks, the launch and schedule code): DRAM counters
+    taken from an ncu capture stand for the kernel only while this id is unchanged."""
+    import hashlib
+    h = hashlib.sha1()
+    for name in ATTN_KERNEL_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(fh.read())
+    return "sha1:" + h.hexdigest()
+
+
+def source_id() -> str:
+    """sha1 over the CUDA sources and the C header the library is built from (file names and
+    contents, in name order): the string libdgattn.so reports through dg_attn_build_id()."""
+    import hashlib
+    h = hashlib.sha1()
+    files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    for name, path in [(f, os.path.join(CSRC, f)) for f in files] + \
+            [("dg_attn.h", os.path.join(INCLUDE, "dg_attn.h"))]:
+        h.update(name.encode())
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return "sha1:" + h.hexdigest()
+
+
 def _flags(verbose_ptxas: bool) -> list:
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                "--expt-relaxed-constexpr"]
+                "--expt-relaxed-constexpr", f'-DDG_BUILD_ID="{source_id()}"']
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f
@@ -41,11 +71,25 @@ def _stale(outputs: str, inputs: list) -> bool:
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
+def _built_id():
+    """The build id of the library on disk, read without loading it into this process (the
+    binding caches the first library it loads), or None."""
+    if not os.path.exists(LIB):
+        return None
+    with open(LIB, "rb") as f:
+        data = f.read()
+    i = data.find(b"sha1:")
+    if i < 0:
+        return None
+    j = data.find(b"\0", i)
+    return data[i:j].decode(errors="replace")
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     """Compile every .cu under csrc/ and link libdgattn.so next to this file; returns its path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "dg_attn.h")]
-    if not force and not verbose_ptxas and not _stale(LIB, deps):
+    if not force and not verbose_ptxas and not _stale(LIB, deps) and _built_id() == source_id():
         return LIB
     nvcc = _nvcc()
     flags = _flags(verbose_ptxas)

@@ -20,12 +20,15 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <new>
 #include <vector>
 
 namespace {
 
 thread_local char g_last_error[512] = "";
+// devices on which the projection kernels' shared-memory opt-in has been made
+std::atomic<unsigned long long> g_proj_attrs{0};
 
 void set_error(const char *fmt, ...)
 {
@@ -42,6 +45,37 @@ int cuda_fail(cudaError_t e, const char *what)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A buffer as the byte range [p, p + bytes) (p may be NULL: no range).
+struct Range {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlap(Range a, Range b)
+{
+    if (!a.p || !b.p || !a.bytes || !b.bytes) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a.p), y = reinterpret_cast<uintptr_t>(b.p);
+    return x < y + b.bytes && y < x + a.bytes;
+}
+
+// DG_ERR_ARG when an output range overlaps an input range or another output.
+int check_no_overlap(std::initializer_list<Range> outs, std::initializer_list<Range> ins)
+{
+    for (auto o = outs.begin(); o != outs.end(); ++o) {
+        for (const Range &i : ins)
+            if (overlap(*o, i)) {
+                set_error("an output buffer overlaps an input buffer");
+                return DG_ERR_ARG;
+            }
+        for (auto o2 = o + 1; o2 != outs.end(); ++o2)
+            if (overlap(*o, *o2)) {
+                set_error("two output buffers overlap");
+                return DG_ERR_ARG;
+            }
+    }
+    return DG_OK;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 {
@@ -494,7 +528,7 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
         // the per-call conversion overwrites the plan's cache copy
         p->cache_ready = false;
         dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
-                              p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32};
+                              p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32, p->status};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);
@@ -833,7 +867,7 @@ int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void
     const int type = dtype == DG_DTYPE_F16 ? dg::kCacheF16
                    : dtype == DG_DTYPE_BF16 ? dg::kCacheBf16 : dg::kCacheF32;
     dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
-                          p->nkv, p->ctx, p->S, p->S_pad, p->hd, type};
+                          p->nkv, p->ctx, p->S, p->S_pad, p->hd, type, p->status};
     if (p->path == DG_PATH_FP32) {
         if (dtype == DG_DTYPE_F32) {
             p->prep_k = static_cast<const float *>(k_cache);
@@ -891,6 +925,12 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
     if (int rc = check_canvas_args(p, q, k_canvas, v_canvas, q_norm_w, k_norm_w, cos_sin, out,
                                    nullptr, nullptr))
         return rc;
+    const size_t qb = (size_t)p->T * p->nh * p->hd * 4, kb = (size_t)p->T * p->nkv * p->hd * 4;
+    const size_t cb = (size_t)p->nkv * p->ctx * p->hd * 4, wb = (size_t)p->hd * 4;
+    if (int rc = check_no_overlap({{out, qb}}, {{q, qb}, {k_canvas, kb}, {v_canvas, kb},
+                                                {k_cache, cb}, {v_cache, cb}, {q_norm_w, wb},
+                                                {k_norm_w, wb}, {cos_sin, 2 * (size_t)p->T * wb}}))
+        return rc;
     if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
     if (int rc = rope_table(p, cos_sin, s)) return rc;
     dg::NormRopeParams n = norm_params(p);
@@ -917,6 +957,12 @@ int dg_attn_norm_rope(dg_attn_plan *p, const float *q, const float *k_canvas,
         set_error("k_hat and v_hat are required");
         return DG_ERR_ARG;
     }
+    const size_t qb = (size_t)p->T * p->nh * p->hd * 4, kb = (size_t)p->T * p->nkv * p->hd * 4;
+    const size_t wb = (size_t)p->hd * 4;
+    if (int rc = check_no_overlap({{q_hat, qb}, {k_hat, kb}, {v_hat, kb}},
+                                  {{q, qb}, {k_canvas, kb}, {v_canvas, kb}, {q_norm_w, wb},
+                                   {k_norm_w, wb}, {cos_sin, 2 * (size_t)p->T * wb}}))
+        return rc;
     if (int rc = rope_table(p, cos_sin, s)) return rc;
     dg::NormRopeParams n = norm_params(p);
     n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
@@ -933,6 +979,14 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
     if (int rc = check_canvas_args(p, q_hat, k_hat, v_hat, nullptr, nullptr, nullptr, out,
                                    nullptr, nullptr))
         return rc;
+    {
+        const size_t qb = (size_t)p->T * p->nh * p->hd * 4;
+        const size_t kb = (size_t)p->T * p->nkv * p->hd * 4;
+        const size_t cb = (size_t)p->nkv * p->ctx * p->hd * 4;
+        if (int rc = check_no_overlap({{out, qb}}, {{q_hat, qb}, {k_hat, kb}, {v_hat, kb},
+                                                    {k_cache, cb}, {v_cache, cb}}))
+            return rc;
+    }
     if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
     // the first-stage kernel with norm and rope switched off only re-lays the operands out
     dg::NormRopeParams n = norm_params(p);
@@ -966,13 +1020,8 @@ int dg_attn_proj_prepare(dg_attn_plan *p, int H, const float *ln_in_w, const flo
             set_error("pointers must be 16-byte aligned");
             return DG_ERR_ALIGN;
         }
-    static bool attrs_done = false;
-    cudaError_t err = cudaSuccess;
-    if (!attrs_done) {
-        err = dg::proj_prepare_attrs();
-        if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
-        attrs_done = true;
-    }
+    cudaError_t err = dg::once_per_device(g_proj_attrs, dg::proj_prepare_attrs);
+    if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
     const bool shared = wv == nullptr;
     const int rows = (p->nh + p->nkv + (shared ? 0 : p->nkv)) * p->hd;
     const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
@@ -1039,6 +1088,14 @@ int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache
             set_error("pointers must be 16-byte aligned");
             return DG_ERR_ALIGN;
         }
+    {
+        const size_t ob = (size_t)p->T * p->nh * p->hd * 4, xb = (size_t)p->T * p->H * 4;
+        const size_t cb = (size_t)p->nkv * p->ctx * p->hd * 4, wb = (size_t)p->hd * 4;
+        if (int rc = check_no_overlap({{out, ob}}, {{x, xb}, {k_cache, cb}, {v_cache, cb},
+                                                    {q_norm_w, wb}, {k_norm_w, wb},
+                                                    {cos_sin, 2 * (size_t)p->T * wb}}))
+            return rc;
+    }
     if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
     if (int rc = rope_table(p, cos_sin, s)) return rc;
     int rc = record_event(p, DG_STAGE_PROJECTION, s);
@@ -1083,13 +1140,8 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
         set_error("pointers must be 16-byte aligned");
         return DG_ERR_ALIGN;
     }
-    static bool attrs_done = false;
-    cudaError_t err = cudaSuccess;
-    if (!attrs_done) {
-        err = dg::proj_prepare_attrs();
-        if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
-        attrs_done = true;
-    }
+    cudaError_t err = dg::once_per_device(g_proj_attrs, dg::proj_prepare_attrs);
+    if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
     const int K = p->nh * p->hd;
     const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
     if (H != p->oH) {
@@ -1192,15 +1244,20 @@ int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)
     err = cudaMemcpy(&st, p->status, sizeof(st), cudaMemcpyDeviceToHost);
     if (err == cudaSuccess) err = cudaMemset(p->status, 0, sizeof(uint32_t));
     if (err != cudaSuccess) return cuda_fail(err, "reading the status word");
+    if (st & (dg::kErrWaitProducer | dg::kErrWaitMma | dg::kErrWaitSoftmax | dg::kErrWaitDrain)) {
+        set_error("a device wait ran out (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 drain)",
+                  st);
+        return DG_ERR_TIMEOUT;
+    }
     if (st & dg::kErrSchedule) {
         set_error("a stream-K run covered more than two (query tile, kv group) pairs (status 0x%x)",
                   st);
         return DG_ERR_STATE;
     }
-    if (st) {
-        set_error("a device wait ran out (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 drain)",
-                  st);
-        return DG_ERR_TIMEOUT;
+    if (st & dg::kErrRange) {
+        set_error("a cache V value lies outside the fp16 range (|v| > 65504 or not finite): the "
+                  "tensor-core path cannot hold it (status 0x%x); the exact path can", st);
+        return DG_ERR_RANGE;
     }
     return DG_OK;
 }
@@ -1239,10 +1296,16 @@ const char *dg_attn_status_string(int status)
     case DG_ERR_TIMEOUT: return "device wait timed out";
     case DG_ERR_UNSUPPORTED: return "unsupported";
     case DG_ERR_STATE: return "missing plan state";
+    case DG_ERR_RANGE: return "value outside the range of the tensor-core operands";
     default: return "unknown status";
     }
 }
 
 const char *dg_attn_last_error(void) { return g_last_error; }
+
+#ifndef DG_BUILD_ID
+#define DG_BUILD_ID "sha1:unknown"
+#endif
+const char *dg_attn_build_id(void) { return DG_BUILD_ID; }
 
 }  // extern "C"

@@ -6,9 +6,9 @@
 // A CTA takes 32 packed query rows (the G heads of one kv group, row R = t*G + h mod G) and one
 // key range; 256 threads, 8 per row.  Each 32-key tile of K and V is staged in shared memory.
 // Scores use blocked summation with a compensated outer sum (8-term fp32 FMA blocks folded into a
-// Knuth TwoSum pair), so a 256-long dot carries ~fp32 rounding of its final value only; the
-// online softmax keeps an fp32 running max and denominator per row (expf), and the P.V
-// accumulators live in registers (hd/8 columns per thread).
+// Knuth TwoSum pair) and stay an unrounded (hi, lo) pair until the running maximum has been
+// subtracted; the online softmax keeps an fp32 running max and denominator per row (expf), and
+// the P.V accumulators live in registers (hd/8 columns per thread).
 #include "dg_internal.cuh"
 
 namespace dg {
@@ -107,13 +107,15 @@ __global__ void __launch_bounds__(kThreads) attn_fp32_kernel(AttnFp32Params p)
                 two_sum(shi[m], slo[m], b);
             }
         }
-        float s[4];
+        // the maximum takes the rounded scores; the exponent below takes the unrounded pair
+        // (a score of ~60 rounded to fp32 is off by up to 2e-6, which moves the output by as much
+        // as 1e-5), with the maximum subtracted from the high part first (exact near the top)
         float mx = -INFINITY;
+        bool live[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const int j = k0 + c8 + 8 * m;
-            s[m] = (j < ke) ? shi[m] + slo[m] : -INFINITY;
-            mx = fmaxf(mx, s[m]);
+            live[m] = k0 + c8 + 8 * m < ke;
+            if (live[m]) mx = fmaxf(mx, shi[m] + slo[m]);
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) attn_fp32_kernel(AttnFp32Params p)
         float pv[4], psum = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            pv[m] = expf(s[m] - m_new);
+            pv[m] = live[m] ? expf((shi[m] - m_new) + slo[m]) : 0.f;
             psum += pv[m];
         }
         psum += __shfl_xor_sync(0xffffffffu, psum, 1);
@@ -176,14 +178,13 @@ cudaError_t launch_hd(const AttnFp32Params &p, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * ((size_t)kFp32TileM * HD + (size_t)kBK * (HD + 4) +
                                          (size_t)kBK * HD);
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fp32_kernel<HD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // the shared-memory opt-in is a per-device setting of the function
+    static std::atomic<unsigned long long> attr_set{0};
+    cudaError_t e = once_per_device(attr_set, [&] {
+        return cudaFuncSetAttribute(attn_fp32_kernel<HD>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (e != cudaSuccess) return e;
     dim3 grid((p.rows + kFp32TileM - 1) / kFp32TileM, p.nkv, p.splits);
     attn_fp32_kernel<HD><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();

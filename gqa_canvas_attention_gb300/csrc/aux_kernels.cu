@@ -32,11 +32,14 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const void *b
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+constexpr float kF16Max = 65504.0f;   // largest finite fp16 value
+
 template <typename T>
 __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
 {
     const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
     const int hd4 = p.hd / 4;
+    bool out_of_range = false;     // a V value the fp16 operand cannot hold (or not finite)
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
         const float4 k = load4<T>(p.k_cache, i);
@@ -66,11 +69,15 @@ __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
         ul.x = *reinterpret_cast<uint32_t *>(&l01); ul.y = *reinterpret_cast<uint32_t *>(&l23);
         *reinterpret_cast<uint2 *>(p.kh + dst) = uh;
         *reinterpret_cast<uint2 *>(p.kl + dst) = ul;
+        out_of_range |= !(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) <=
+                          kF16Max);
         __half2 v01 = __floats2half2_rn(v.x, v.y), v23 = __floats2half2_rn(v.z, v.w);
         uint2 uv;
         uv.x = *reinterpret_cast<uint32_t *>(&v01); uv.y = *reinterpret_cast<uint32_t *>(&v23);
         *reinterpret_cast<uint2 *>(p.vh + dst) = uv;
     }
+    if (__any_sync(0xffffffffu, out_of_range) && (threadIdx.x & 31) == 0 && p.status)
+        atomicOr(p.status, kErrRange);
 }
 
 // One warp per (packed row R, kv group g): every lane loads the (m, l) pairs and its slice of

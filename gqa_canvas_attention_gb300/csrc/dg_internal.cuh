@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 namespace dg {
@@ -17,6 +18,7 @@ enum : uint32_t {
     kErrWaitSoftmax = 4u,
     kErrWaitDrain = 8u,
     kErrSchedule = 16u,            // a stream-K run covered more than two pairs (host error)
+    kErrRange = 32u,               // a cache V value outside the fp16 range (tensor-core path)
 };
 
 // Rows of the tensor-core query tile: the G = nh/nkv query heads of one kv group are packed
@@ -65,6 +67,7 @@ struct CachePrepParams {
     float *k32, *v32;              // ... or an fp32 copy [nkv, ctx, hd] for the exact path
     int nkv, ctx, S, S_pad, hd;
     int dtype;                     // CacheType
+    uint32_t *status;              // kErrRange is OR-ed in for a V value beyond the fp16 range
 };
 
 struct AttnFp32Params {
@@ -209,6 +212,21 @@ inline cudaLaunchAttribute pdl_attribute()
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
     return a;
+}
+
+// Run `set` (a function-attribute call, which applies to the current device only) once per device:
+// `done` holds one bit per device ordinal below 64 (a higher ordinal runs `set` every time).
+// Threads that race on a device's first call may both run `set`; the calls are idempotent.
+template <class F> cudaError_t once_per_device(std::atomic<unsigned long long> &done, F &&set)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // Host launchers (return cudaGetLastError()).

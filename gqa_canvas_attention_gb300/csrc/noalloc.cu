@@ -44,6 +44,8 @@ __global__ void noalloc_inv_freq_kernel(float2 *out, int half, int hd, double th
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace
 
 extern "C" const char *dg_attn_noalloc_last_error(void) { return g_err; }
@@ -72,6 +74,15 @@ extern "C" int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, 
         snprintf(g_err, sizeof(g_err), "a required pointer is NULL (or a cache given with ctx=0)");
         return DG_ERR_ARG;
     }
+    // the kernels move every row with 16-byte vector loads and stores
+    const void *all[] = {q, k_canvas, v_canvas, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out};
+    for (const void *x : all)
+        if (x && !aligned16(x)) {
+            snprintf(g_err, sizeof(g_err), "pointers must be 16-byte aligned");
+            return DG_ERR_ALIGN;
+        }
+    // the scratch regions, each rounded up to 256 bytes: the RoPE frequencies (hd/2 float2),
+    // q-hat [T, nh, hd], k-hat and v-hat [T, nkv, hd] (fp32)
     const size_t freq_b = align256(sizeof(float2) * (size_t)(hd / 2));
     const size_t q_b = align256(sizeof(float) * (size_t)T * nh * hd);
     const size_t kv_b = align256(sizeof(float) * (size_t)T * nkv * hd);
@@ -79,7 +90,7 @@ extern "C" int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, 
     if (need > kDgNoallocScratchBytes) {
         snprintf(g_err, sizeof(g_err),
                  "needs %zu bytes of scratch for T=%d nh=%d nkv=%d hd=%d; the fixed array holds "
-                 "%zu (T*(nh+2*nkv)*hd*4 must stay below about 16 MiB)",
+                 "%zu (the sum of hd*4, T*nh*hd*4 and twice T*nkv*hd*4, each rounded up to 256)",
                  need, T, nh, nkv, hd, kDgNoallocScratchBytes);
         return DG_ERR_ARG;
     }

@@ -186,12 +186,25 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
         const int kind = job < p.nh ? 0 : job < p.nh + p.nkv ? 1 : 2;
         float *xr = x[g];
         if (p.do_norm) {
-            float ss = 0.f;
+            float rn;
+            if constexpr (MODE == kOutFp32) {
+                // the exact path: the sum of squares and the scale in fp64 (one scale per row),
+                // so a canvas key's scale -- which moves every score of that key, by up to
+                // |s| * 2^-22 from a 2-ulp rsqrtf at |s| ~ 60 -- carries only its final rounding
+                double ss = 0.0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(xr[e], xr[e], ss);
+                for (int e = 0; e < 8; ++e) ss = fma((double)xr[e], (double)xr[e], ss);
 #pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float rn = rsqrtf(ss * (1.0f / (float)HD) + p.eps);
+                for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                rn = (float)(1.0 / sqrt(ss / (double)HD + (double)p.eps));
+            } else {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(xr[e], xr[e], ss);
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                rn = rsqrtf(ss * (1.0f / (float)HD) + p.eps);
+            }
             const bool use_q = kind == 0 && p.wq, use_k = kind == 1 && p.wk;
             if (use_q || use_k) {
 #pragma unroll

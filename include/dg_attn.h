@@ -52,6 +52,9 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_ERR_TIMEOUT     4  /* a bounded device wait ran out (the kernel gave up cleanly) */
 #define DG_ERR_UNSUPPORTED 5  /* the request needs something this build or device lacks */
 #define DG_ERR_STATE       6  /* the call needs state the plan does not hold */
+#define DG_ERR_RANGE       7  /* (dg_attn_sync_status) a cache V value lies outside the fp16 range
+                                 that the tensor-core P.V operand holds (|v| > 65504 or not
+                                 finite); the outputs of that forward are not valid */
 
 /* Arithmetic paths (option DG_OPT_PATH). */
 #define DG_PATH_TC   0  /* tensor cores: Q.K^T as three bf16 MMAs (hi/lo split), P.V in fp16 (10-bit
@@ -59,25 +62,33 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_PATH_FP32 1  /* exact fp32 on the CUDA cores */
 
 /* Option keys for dg_attn_set_option / dg_attn_get_option. */
-#define DG_OPT_PATH          1  /* DG_PATH_TC (default when hd is 64, 128 or 256) or DG_PATH_FP32 */
-#define DG_OPT_POS0          2  /* position of canvas row 0 (default ctx, the cache length) */
-#define DG_OPT_SPLITS        3  /* key-range partitions per query tile (0..64); 0 = chosen per plan */
-#define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000) */
+#define DG_OPT_PATH          1  /* DG_PATH_TC (default when hd is 64, 128 or 256) or DG_PATH_FP32;
+                                   the exact path keeps the page's all-f32 contract (module doc) */
+#define DG_OPT_POS0          2  /* position of canvas row 0 (default ctx, the cache length): the page's
+                                   canvas_forward ropes canvas row t at rope_cos_sin(cache.seq_len
+                                   + t, ...), and a sliding layer's cache may be shorter than seq_len */
+#define DG_OPT_SPLITS        3  /* key-range partitions per query tile (0..64); 0 = chosen per plan.
+                                   Scheduling only (the page's DG_ATTN runs one workgroup per row
+                                   and head over all keys); results agree within rounding */
+#define DG_OPT_WAIT_LIMIT_MS 4  /* device wait limit in ms (default 2000); no counterpart on the page */
 #define DG_OPT_PROFILE       5  /* 1 = record CUDA events around each kernel launch, per stage (inside a
-                                   stream capture as external records, taken on every replay) */
+                                   stream capture as external records, taken on every replay);
+                                   measurement only, no counterpart on the page */
 #define DG_OPT_INJECT_STALL  6  /* test hook: 1 = the tensor-core kernel's softmax withholds its
                                    first "P ready" signal, so the bounded waits behind it run out
-                                   and the forward ends with DG_ERR_TIMEOUT (no fault, no hang) */
+                                   and the forward ends with DG_ERR_TIMEOUT (no fault, no hang);
+                                   no counterpart on the page */
 #define DG_OPT_INPUTS_RESIDENT 7 /* 1 = the caller guarantees that the inputs of every call (q,
                                    k_canvas, v_canvas, weights, cos_sin) are complete before the
                                    work enqueued ahead of that call on the stream started, e.g.
                                    canvases already resident in device memory: the first stage then
                                    reads them while the previous call's attention kernel is still
                                    running.  Default 0: the first stage waits for the preceding
-                                   kernel before reading anything */
+                                   kernel before reading anything.  Scheduling only (the page
+                                   records all dispatches of a forward into one pass) */
 #define DG_OPT_SCHEDULE      8  /* how the tensor-core kernel deals key tiles to CTAs: one of
                                    DG_SCHEDULE_AUTO (default), DG_SCHEDULE_SPLIT,
-                                   DG_SCHEDULE_STREAM_K */
+                                   DG_SCHEDULE_STREAM_K.  Scheduling only, as DG_OPT_SPLITS */
 #define DG_SCHEDULE_AUTO     0  /* the cheaper of the two for the plan's geometry (a cost model) */
 #define DG_SCHEDULE_SPLIT    1  /* one CTA per (query tile, kv group, key partition), partitions
                                    set by DG_OPT_SPLITS; 2..8 partitions merge inside the kernel,
@@ -96,10 +107,13 @@ typedef struct dg_attn_plan dg_attn_plan;
 #define DG_INFO_SCHEDULE_USED 20 /* DG_SCHEDULE_SPLIT or DG_SCHEDULE_STREAM_K: what the next forward
                                    uses (DG_SCHEDULE_SPLIT on the fp32 path) */
 
-/* Create a plan for one geometry on the current device.  Requires nh % nkv == 0, nh, nkv, T >= 1,
- * ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in {64, 128, 256}),
- * eps >= 0, rope_theta > 0.  Returns NULL on error (see
- * dg_attn_last_error()).  Allocates the plan's device scratch with cudaMalloc. */
+/* Create a plan for one geometry on the current device (page: the per-layer geometry that
+ * DgGpu::new checks -- n_kv, head_dim, nh % n_kv -- and the scratch buffers canvas_forward sizes
+ * for the normed q/k/v; the page's head_dim <= 128 limit is lifted).  Requires nh % nkv == 0,
+ * nh, nkv, T >= 1, ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in
+ * {64, 128, 256}), eps >= 0, rope_theta > 0, ctx + T < 2^24.  Returns NULL on error (see
+ * dg_attn_last_error()).  Allocates the plan's device scratch with cudaMalloc; the plan is tied
+ * to the device that was current at creation. */
 dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float eps,
                                   float rope_theta);
 
@@ -116,18 +130,23 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
 int dg_attn_schedule_info(int nh, int nkv, int hd, int ctx, int T, int num_sms,
                           const int *max_clusters, int schedule, long long *out);
 
-/* The whole block: norms + RoPE, attention, output.  k_cache and v_cache are [nkv, ctx, hd];
- * with ctx == 0 they must be NULL.  With ctx > 0 and both NULL the plan uses the cache copy made
- * by the last dg_attn_cache_prepare (DG_ERR_STATE if there is none).  v_canvas may alias
- * k_canvas (models whose V is the raw K projection).  out must not overlap any input.
- * Every pointer must be 16-byte aligned (DG_ERR_ALIGN).  Enqueued on `stream`. */
+/* The whole block (page: canvas_forward's attention branch from the three DG_HEADNORM_ROPE
+ * dispatches -- q weighted + RoPE, k weighted + RoPE, v weightless without RoPE -- through the
+ * DG_ATTN dispatch): norms + RoPE, attention, output.  k_cache and v_cache are [nkv, ctx, hd];
+ * with ctx == 0 they must be NULL (the page's 1-float stub cache).  With ctx > 0 and both NULL
+ * the plan uses the cache copy made by the last dg_attn_cache_prepare (DG_ERR_STATE if there is
+ * none).  v_canvas may alias k_canvas (the page's k_eq_v layers, whose V is the raw K
+ * projection).  out must not overlap any input (DG_ERR_ARG; checked on the byte ranges the plan's
+ * sizes give).  Every pointer must be 16-byte aligned (DG_ERR_ALIGN).  Enqueued on `stream`; on
+ * the tensor-core path a cache V outside the fp16 range is reported by dg_attn_sync_status
+ * (DG_ERR_RANGE). */
 int dg_attn_forward(dg_attn_plan *plan, const float *q, const float *k_canvas,
                     const float *v_canvas, const float *k_cache, const float *v_cache,
                     const float *q_norm_w, const float *k_norm_w, const float *cos_sin, float *out,
                     cudaStream_t stream);
 
 /* Copy a cache [nkv, ctx, hd] (K and V) into the plan in the tensor-core operand format, once
- * per cache.  A denoising loop that keeps its cache fixed for many steps calls this once, then
+ * per cache (page: DgGpuCache / upload_cache, the encoder cache rebuilt once per canvas block).  A denoising loop that keeps its cache fixed for many steps calls this once, then
  * dg_attn_forward with k_cache = v_cache = NULL.  The copy is taken on `stream`; the caller may
  * reuse its own buffers once that stream has passed this point.  On the fp32 path the plan
  * keeps the two pointers instead (the caller must keep the buffers alive and unchanged). */
@@ -148,26 +167,34 @@ int dg_attn_cache_prepare(dg_attn_plan *plan, const float *k_cache, const float 
 int dg_attn_cache_prepare_typed(dg_attn_plan *plan, const void *k_cache, const void *v_cache,
                                 int dtype, cudaStream_t stream);
 
-/* The first stage alone (RMSNorm + weight + RoPE on q and k, RMSNorm on v), in fp32, written in
- * the input layouts: q_hat [T, nh*hd], k_hat and v_hat [T, nkv*hd]. */
+/* The first stage alone (page: item DG_HEADNORM_ROPE and its three dispatches -- RMSNorm +
+ * weight + RoPE on q and k, RMSNorm on v), in fp32, written in the input layouts: q_hat
+ * [T, nh*hd], k_hat and v_hat [T, nkv*hd] (not overlapping any input: DG_ERR_ARG). */
 int dg_attn_norm_rope(dg_attn_plan *plan, const float *q, const float *k_canvas,
                       const float *v_canvas, const float *q_norm_w, const float *k_norm_w,
                       const float *cos_sin, float *q_hat, float *k_hat, float *v_hat,
                       cudaStream_t stream);
 
-/* The attention stage alone, on operands that are already normed and roped (q_hat [T, nh*hd],
- * k_hat / v_hat [T, nkv*hd], cache as in dg_attn_forward), with the plan's current path. */
+/* The attention stage alone (page: item DG_ATTN and its dispatch), on operands that are already
+ * normed and roped (q_hat [T, nh*hd], k_hat / v_hat [T, nkv*hd], cache as in dg_attn_forward),
+ * with the plan's current path; out must not overlap an input (DG_ERR_ARG). */
 int dg_attn_attend(dg_attn_plan *plan, const float *q_hat, const float *k_hat,
                    const float *v_hat, const float *k_cache, const float *v_cache, float *out,
                    cudaStream_t stream);
 
+/* Set one DG_OPT_* option of a plan (see the keys above for the page item each one follows).
+ * DG_ERR_ARG for an unknown key or a value out of range, DG_ERR_UNSUPPORTED for the tensor-core
+ * path at hd = 32; changing DG_OPT_SPLITS or DG_OPT_SCHEDULE may grow the plan's partial-result
+ * buffers (cudaMalloc). */
 int dg_attn_set_option(dg_attn_plan *plan, int key, long long value);
+/* Read a DG_OPT_* option or a DG_INFO_* value into *value (host only). */
 int dg_attn_get_option(const dg_attn_plan *plan, int key, long long *value);
 
 /* Synchronise `stream`, then read and clear the plan's device status word: DG_OK;
  * DG_ERR_TIMEOUT when a kernel gave up on a bounded wait since the last call; DG_ERR_STATE when a
  * stream-K CTA was handed a run it cannot hold (more than two pairs; the host layout rules this
- * out). */
+ * out); DG_ERR_RANGE when a cache converted for the tensor-core path held a V value outside the
+ * fp16 range.  No counterpart on the page (its dispatches cannot fail on the device). */
 int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 
 /* Stages for dg_attn_profile_read. */
@@ -239,8 +266,10 @@ int dg_attn_forward_layer(dg_attn_plan *plan, float *resid, const float *k_cache
  * as dg_attn_forward on the exact-fp32 path with one key-range partition, without a plan: its
  * working memory is a fixed 16 MiB __device__ array inside the library (held on every GPU that
  * loads the library until the process exits), so it allocates nothing.  Sizes must satisfy
- * T*(nh + 2*nkv)*hd*4 + hd*4 <= 16 MiB (checked: DG_ERR_ARG otherwise); other requirements as
- * for dg_attn_plan_create / dg_attn_forward; pos0 < 0 means pos0 = ctx.  The first call on a
+ * a(hd*4) + a(T*nh*hd*4) + 2*a(T*nkv*hd*4) <= 16 MiB, where a(x) rounds x up to a multiple of
+ * 256 (checked on the host: DG_ERR_ARG otherwise); every pointer must be 16-byte aligned (checked
+ * on the host: DG_ERR_ALIGN); other requirements as for dg_attn_plan_create / dg_attn_forward;
+ * pos0 < 0 means pos0 = ctx.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress), so make it before any stream
  * capture.  Calls share the array: calls that overlap on the GPU race and must be serialised by
  * the caller.  Host-side errors are described by dg_attn_noalloc_last_error(). */
@@ -251,8 +280,13 @@ int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, float eps,
                             const float *cos_sin, float *out, cudaStream_t stream);
 const char *dg_attn_noalloc_last_error(void);
 
+/* A static description of a DG_* status code. */
 const char *dg_attn_status_string(int status);
+/* The text of the calling thread's last host-side error (a static thread-local buffer). */
 const char *dg_attn_last_error(void);
+/* The build identity of the loaded library: "sha1:<hex>" of the CUDA sources and this header it
+ * was compiled from, hashed by the build script (a static string). */
+const char *dg_attn_build_id(void);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,25 @@ def test_noalloc_entry_point_checks_sizes_on_the_host(lib):
     assert "scratch" in lib.dg_attn_noalloc_last_error().decode()
 
 
+def test_noalloc_entry_point_checks_alignment_and_its_bound_on_the_host(lib):
+    """A misaligned pointer is DG_ERR_ALIGN and one canvas row beyond the fixed scratch is
+    DG_ERR_ARG, both before any CUDA call (the pointers here are never dereferenced).  The bound
+    is the sum of four regions rounded up to 256 bytes: for nh = nkv = 1, hd = 64, ctx = 0 that is
+    256 + 3 * T * 256 <= 16 MiB, so T = 21845 fits exactly (run on the GPU) and T = 21846 does
+    not."""
+    args = (1, 1, 64, 0)
+    ok = 1 << 20                                  # a 16-byte-aligned stand-in address
+    assert B.dg_attn_forward_noalloc(*args, 8, 1e-6, 1e4, -1, ok + 4, ok, ok, None, None, None,
+                                     None, None, ok, stream=0) == B.DG_ERR_ALIGN
+    assert B.dg_attn_forward_noalloc(*args, 8, 1e-6, 1e4, -1, ok, ok, ok, None, None, None,
+                                     None, ok + 8, ok, stream=0) == B.DG_ERR_ALIGN
+    assert "aligned" in lib.dg_attn_noalloc_last_error().decode()
+    assert B.dg_attn_forward_noalloc(*args, 21846, 1e-6, 1e4, -1, ok, ok, ok, None, None, None,
+                                     None, None, ok, stream=0) == B.DG_ERR_ARG
+    assert "scratch" in lib.dg_attn_noalloc_last_error().decode()
+    assert 256 + 3 * 21845 * 256 == 16 << 20
+
+
 def test_null_plan_is_an_argument_error_for_every_entry_point(lib):
     """Every entry point that takes a plan checks it on the host before any CUDA call."""
     assert lib.dg_attn_cache_prepare_typed(None, None, None, B.DG_DTYPE_F16, None) == B.DG_ERR_ARG
@@ -75,3 +94,56 @@ def test_null_plan_is_an_argument_error_for_every_entry_point(lib):
     assert lib.dg_attn_forward_layer(None, *([None] * 7)) == B.DG_ERR_ARG
     assert lib.dg_attn_norm_rope(None, *([None] * 10)) == B.DG_ERR_ARG
     assert lib.dg_attn_attend(None, *([None] * 7)) == B.DG_ERR_ARG
+
+
+def _cpu_plan(nh=4, nkv=2, hd=64, ctx=16, T=8):
+    """A Plan object with its geometry but no library handle (no GPU here): enough to show that
+    its methods reject bad tensors before any library call."""
+    p = object.__new__(B.Plan)
+    p.nh, p.nkv, p.hd, p.ctx, p.T = nh, nkv, hd, ctx, T
+    p.H = p.oH = None
+    p.device = 0
+    p.handle = None
+    return p
+
+
+def test_binding_rejects_bad_tensors_before_the_library():
+    import torch
+    p = _cpu_plan()
+    T, nh, nkv, hd, ctx = p.T, p.nh, p.nkv, p.hd, p.ctx
+    good = dict(q=torch.zeros(T, nh * hd), k_canvas=torch.zeros(T, nkv * hd),
+                v_canvas=torch.zeros(T, nkv * hd), k_cache=torch.zeros(nkv, ctx, hd),
+                v_cache=torch.zeros(nkv, ctx, hd), out=torch.zeros(T, nh * hd))
+    cases = {
+        "dtype": dict(good, q=torch.zeros(T, nh * hd, dtype=torch.float64)),
+        "contiguous": dict(good, q=torch.zeros(nh * hd, T).t()),
+        "elements": dict(good, k_canvas=torch.zeros(T - 1, nkv * hd)),
+        "cache elements": dict(good, v_cache=torch.zeros(nkv, ctx + 1, hd)),
+        "half cache": dict(good, k_cache=torch.zeros(nkv, ctx, hd, dtype=torch.float16)),
+        "out elements": dict(good, out=torch.zeros(T, nh * hd + 4)),
+    }
+    msgs = {"dtype": "dtype", "contiguous": "contiguous", "elements": "elements",
+            "cache elements": "elements", "half cache": "dtype", "out elements": "elements"}
+    for name, kw in cases.items():
+        with pytest.raises(ValueError, match=msgs[name]):
+            p.forward(**kw)
+    # right dtype, layout and size, but host memory: the device check
+    with pytest.raises(ValueError, match="cuda"):
+        p.forward(**good)
+    with pytest.raises(ValueError, match="elements"):
+        p.forward(**good, q_norm_w=torch.ones(hd + 1))
+    with pytest.raises(ValueError, match="elements"):
+        p.forward(**good, cos_sin=torch.ones(T, hd))
+    with pytest.raises(ValueError, match="both be"):
+        p.cache_prepare(torch.zeros(nkv, ctx, hd, dtype=torch.float16),
+                        torch.zeros(nkv, ctx, hd, dtype=torch.float32))
+    with pytest.raises(ValueError, match="elements"):
+        p.attend(good["q"], good["k_canvas"], torch.zeros(3), out=good["out"])
+    with pytest.raises(ValueError, match="elements"):
+        p.proj_prepare(128, None, torch.zeros(nh * hd, 127), torch.zeros(nkv * hd, 128))
+    with pytest.raises(ValueError, match="contiguous"):
+        B._ptr(torch.zeros(4, 4).t())
+
+
+def test_build_id_matches_the_sources(lib):
+    assert B.build_id() == build_mod.source_id()

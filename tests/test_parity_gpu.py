@@ -3,9 +3,9 @@ inputs, element by element.
 
 Tolerances (on outputs of RMS <= 1):
   tensor-core path: max |gpu - oracle| <= 5e-3 and mean <= 5e-4;
-  fp32 path:        max <= 1e-5.
-Full-size workloads are checked on sampled canvas rows that span several query tiles and the
-ragged tail; small shapes are checked whole.
+  fp32 path:        max <= 1e-5 and mean <= 1e-6.
+Every output row is compared, at the full sizes of the named workloads too (the oracle does a
+36.5-GFLOP forward of the 48-step workload in well under a second on 16 cores).
 """
 import numpy as np
 import pytest
@@ -41,11 +41,8 @@ def oracle_out(d, nh, nkv, hd, rows=None, pos0=None, cos_sin=None, theta=ROPE_TH
                           cos_sin=cos_sin, eps=EPS, theta=theta, pos0=pos0, rows=rows)
 
 
-def row_ranges(T):
-    if T <= 64:
-        return [(0, T)]
-    mid = T // 2
-    return [(0, 4), (mid - 3, mid + 3), (T - 5, T)]
+def all_rows(T):
+    return [(0, T)]
 
 
 def check(out, ref, path, ranges, label=""):
@@ -108,23 +105,22 @@ def test_norm_rope_with_table():
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_workload_parity(name, path):
+    """Every row of every named workload; every canvas of a batch of canvases."""
     w = WORKLOADS[name]
-    d = workload_inputs(w)
-    dd = to_dev(d)
     plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, w.theta)
     plan.set(B.DG_OPT_PATH, path)
     if w.pos0 is not None:
         plan.set(B.DG_OPT_POS0, w.pos0)
-    out = run_forward(plan, dd)
-    ranges = row_ranges(w.T)
-    ref = np.zeros((w.T, w.nh * w.hd))
-    for a, b in ranges:
-        ref[a:b] = oracle_out(d, w.nh, w.nkv, w.hd, rows=(a, b), pos0=w.pos0, theta=w.theta)[a:b]
-    check(out, ref, path, ranges, name)
+    for c in range(w.canvases):
+        d = workload_inputs(w, canvas=c)
+        out = run_forward(plan, to_dev(d))
+        ref = oracle_out(d, w.nh, w.nkv, w.hd, pos0=w.pos0, theta=w.theta)
+        check(out, ref, path, all_rows(w.T), f"{name}[{c}]")
 
 
 def test_denoise_loop_steps_share_a_prepared_cache():
-    """A few steps of the 48-step loop: cache prepared once, fresh canvas per step."""
+    """Steps 0, 1 and 47 of the 48-step loop, every row: cache prepared once, fresh canvas per
+    step."""
     w = WORKLOADS["denoise48_ctx8k"]
     plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
     d0 = workload_inputs(w, step=0)
@@ -137,8 +133,43 @@ def test_denoise_loop_steps_share_a_prepared_cache():
         dd = to_dev(d)
         out = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"])
         assert plan.sync_status() == B.DG_OK
-        ref = oracle_out(d, w.nh, w.nkv, w.hd, rows=(w.T - 4, w.T))
-        check(out, ref, B.DG_PATH_TC, [(w.T - 4, w.T)], f"step{step}")
+        check(out, oracle_out(d, w.nh, w.nkv, w.hd), B.DG_PATH_TC, all_rows(w.T), f"step{step}")
+
+
+def test_denoise_loop_in_the_bench_launch_configuration():
+    """The 48-step canvas exactly as the benchmark runs it: resident inputs, the cache prepared
+    once, 48 forwards captured into one CUDA graph and replayed twice.  Every row of steps 0, 1
+    and 47 and eight rows of every other step are compared with the oracle."""
+    w = WORKLOADS["denoise48_ctx8k"]
+    plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_INPUTS_RESIDENT, 1)
+    d0 = workload_inputs(w, step=0)
+    kc, vc = d0["k_cache"].cuda(), d0["v_cache"].cuda()
+    steps = [workload_inputs(w, step=s) for s in range(w.steps)]
+    dev = [to_dev(d) for d in steps]
+    outs = [torch.empty(w.T, w.nh * w.hd, device="cuda") for _ in steps]
+
+    def canvas():
+        plan.cache_prepare(kc, vc)
+        for dd, o in zip(dev, outs):
+            plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                         dd["k_norm_w"], None, o)
+
+    canvas()                                # builds the cos/sin table outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        canvas()
+    for o in outs:
+        o.fill_(float("nan"))
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert plan.sync_status() == B.DG_OK
+    for s, (d, o) in enumerate(zip(steps, outs)):
+        d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]
+        rows = (0, w.T) if s in (0, 1, w.steps - 1) else (8 * (s % 60), 8 * (s % 60) + 8)
+        check(o, oracle_out(d, w.nh, w.nkv, w.hd, rows=rows), B.DG_PATH_TC, [rows], f"step{s}")
 
 
 # ------------------------------------------------------------------ shapes and edge cases
@@ -220,10 +251,8 @@ def test_stream_k_schedule(shape):
     out = run_forward(plan, dd)
     again = run_forward(plan, dd)
     assert torch.equal(out, again), "the stream-K merge order is fixed: results repeat bit for bit"
-    ranges = row_ranges(T)
-    ref = np.zeros((T, nh * hd))
-    for a, b in ranges:
-        ref[a:b] = oracle_out(d, nh, nkv, hd, rows=(a, b))[a:b]
+    ranges = all_rows(T)
+    ref = oracle_out(d, nh, nkv, hd)
     check(out, ref, B.DG_PATH_TC, ranges, "stream-K %s" % (shape,))
     # the split schedule on the same inputs agrees within the same bound
     plan.set(B.DG_OPT_SCHEDULE, B.DG_SCHEDULE_SPLIT)
@@ -260,8 +289,7 @@ def test_stream_k_under_a_cuda_graph_with_resident_inputs():
     torch.cuda.synchronize()
     assert plan.sync_status() == B.DG_OK
     for (d, _), o in zip(ins, outs):
-        ranges = [(w.T - 4, w.T)]
-        check(o, oracle_out(d, w.nh, w.nkv, w.hd, rows=ranges[0]), B.DG_PATH_TC, ranges, "graph")
+        check(o, oracle_out(d, w.nh, w.nkv, w.hd), B.DG_PATH_TC, all_rows(w.T), "graph")
 
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
@@ -376,11 +404,7 @@ def test_bounded_wait_runs_out_cleanly_and_the_context_stays_usable(schedule):
     assert plan.sync_status() == B.DG_OK          # read-and-clear
     plan.set(B.DG_OPT_INJECT_STALL, 0)
     out = run_forward(plan, dd)
-    ranges = row_ranges(T)
-    ref = np.zeros((T, nh * hd))
-    for a, b in ranges:
-        ref[a:b] = oracle_out(d, nh, nkv, hd, rows=(a, b))[a:b]
-    check(out, ref, B.DG_PATH_TC, ranges, "after-timeout")
+    check(out, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, all_rows(T), "after-timeout")
 
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
@@ -442,7 +466,7 @@ def test_resident_inputs_give_the_same_bits():
     d = make_inputs(T, ctx, nh, nkv, hd, seed=53)
     d0 = make_inputs(T, ctx, nh, nkv, hd, seed=50)
     d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]     # the prepared cache
-    check(outs[1][3], oracle_out(d, nh, nkv, hd, rows=(0, 8)), B.DG_PATH_TC, [(0, 8)], "resident")
+    check(outs[1][3], oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, all_rows(T), "resident")
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
@@ -470,3 +494,53 @@ def test_sixteen_bit_cache_twin(dtype, path):
                         dd["k_norm_w"])
     assert plan.sync_status() == B.DG_OK
     assert torch.equal(out2, ref)
+
+
+def test_output_overlapping_an_input_is_refused_before_any_launch():
+    T, ctx, nh, nkv, hd = 8, 16, 2, 1, 64
+    d = to_dev(make_inputs(T, ctx, nh, nkv, hd, seed=17))
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    h = plan.handle
+    big = torch.zeros(4 * T * nh * hd, device="cuda")
+    for inp in ("q", "k_canvas", "v_cache", "q_norm_w"):
+        args = dict(d)
+        args[inp] = big[: args[inp].numel()]
+        with pytest.raises(B.DgAttnError) as e:
+            B.dg_attn_forward(h, args["q"], args["k_canvas"], args["v_canvas"], args["k_cache"],
+                              args["v_cache"], args["q_norm_w"], args["k_norm_w"], None,
+                              big[16:16 + T * nh * hd])
+        assert e.value.status == B.DG_ERR_ARG and "overlap" in B.last_error()
+    out = torch.empty(T, nh * hd, device="cuda")
+    with pytest.raises(B.DgAttnError) as e:
+        B.dg_attn_norm_rope(h, d["q"], d["k_canvas"], d["v_canvas"], None, None, None, out,
+                            out[0:1], torch.empty_like(d["v_canvas"]))
+    assert e.value.status == B.DG_ERR_ARG
+    assert plan.sync_status() == B.DG_OK
+
+
+@pytest.mark.parametrize("prepared", [True, False], ids=["prepared", "per_call"])
+def test_cache_value_beyond_fp16_is_reported(prepared):
+    """The tensor-core P.V takes V in fp16: a cache value beyond 65504 cannot be held, and the
+    forward reports DG_ERR_RANGE instead of silently overflowing.  The exact path takes it."""
+    T, ctx, nh, nkv, hd = 16, 100, 4, 2, 128
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=18)
+    d["v_cache"][1, 37, 5] = 1.0e5
+    dd = to_dev(d)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    if prepared:
+        plan.cache_prepare(dd["k_cache"], dd["v_cache"])
+        plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                     dd["k_norm_w"])
+    else:
+        plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["k_cache"], dd["v_cache"],
+                     dd["q_norm_w"], dd["k_norm_w"])
+    assert plan.sync_status() == B.DG_ERR_RANGE
+    assert "fp16" in B.last_error()
+    assert plan.sync_status() == B.DG_OK                  # read and cleared
+    plan.set(B.DG_OPT_PATH, B.DG_PATH_FP32)
+    out = run_forward(plan, dd).double().cpu().numpy()
+    ref = oracle_out(d, nh, nkv, hd)
+    # outputs that weigh the large value are far from RMS 1: compare relative to their size
+    rel = np.abs(out - ref) / np.maximum(1.0, np.abs(ref))
+    print(f"range-fp32: max |ref| {np.abs(ref).max():.3e}, max relative err {rel.max():.3e}")
+    assert rel.max() <= 1e-5
