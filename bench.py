@@ -25,20 +25,25 @@ if ROOT not in sys.path:
 
 METRIC = "canvas-attention TFLOP/s and us/denoise-step, % of TF32 tensor peak"
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio of the part
-
-# DRAM bytes (read + write) per launch of the tensor-core attention kernel on the bench workload,
-# from one ncu capture (profiles/attn_tc_kernel_denoise48_ctx8k.md), valid only for the kernel
-# source it was taken on: the bench reports null once attn_tc.cu has changed.
-ATTN_TRAFFIC = {"source_sha1_prefix": "ff27378fde19", "bytes": 59.92e6}
+# Workloads timed beside the bench workload, one forward each (a batch of canvases: all of them).
+SIDE_WORKLOADS = ["tiny", "gqa_hd256_ctx1k", "gqa_hd128_ctx4k", "mha_canvas4k_x4"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_tc_kernel_denoise48_ctx8k.md")
 
 
 def attn_traffic():
-    import hashlib
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gqa_canvas_attention_gb300",
-                       "csrc", "attn_tc.cu")
-    with open(src, "rb") as f:
-        sha = hashlib.sha1(f.read()).hexdigest()
-    return ATTN_TRAFFIC["bytes"] if sha.startswith(ATTN_TRAFFIC["source_sha1_prefix"]) else None
+    """DRAM bytes per launch of the tensor-core attention kernel on the bench workload, from the
+    ncu capture summarised in the profile summary's `traffic_per_launch_bytes:` line, or None
+    when the kernel's sources have changed since that capture (its `kernel_source:` id)."""
+    import re
+    from gqa_canvas_attention_gb300.build import attn_kernel_source_id
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+kernel_source:\s*(sha1:[0-9a-f]+)",
+                  text)
+    if not m or m.group(2) != attn_kernel_source_id():
+        return None
+    return float(m.group(1))
 
 
 def parse():
@@ -61,6 +66,10 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the 48 forwards one by one instead of replaying a CUDA graph")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the per-forward timings of the other workloads")
+    ap.add_argument("--side-reps", type=int, default=20)
+    ap.add_argument("--cpu-side-budget-s", type=float, default=3.0)
     return ap.parse_args()
 
 
@@ -141,49 +150,178 @@ class ClockSampler:
 _ORACLE_INPUTS = {}
 
 
-def _oracle_inputs(w, step):
-    """Seeded inputs of one step as numpy arrays (generated once per process)."""
+def _oracle_inputs(w, unit):
+    """Seeded inputs of one forward (denoising step, or canvas of a batch) of workload w as numpy
+    arrays, with the cache it attends to (generated once per process)."""
     from gqa_canvas_attention_gb300.workloads import shared_cache, workload_inputs
-    if "cache" not in _ORACLE_INPUTS:
-        kc, vc = shared_cache(w)
-        _ORACLE_INPUTS["cache"] = (kc.numpy(), vc.numpy())
-    if step not in _ORACLE_INPUTS:
-        d = workload_inputs(w, step=step)
-        _ORACLE_INPUTS[step] = {k: (None if v is None else v.numpy()) for k, v in d.items()}
-    return _ORACLE_INPUTS["cache"], _ORACLE_INPUTS[step]
+    key = (w.name, unit)
+    if key not in _ORACLE_INPUTS:
+        d = workload_inputs(w, canvas=unit) if w.canvases > 1 else workload_inputs(w, step=unit)
+        d = {k: (None if v is None else v.numpy()) for k, v in d.items()}
+        if w.ctx > 0 and w.canvases == 1:
+            if (w.name, "cache") not in _ORACLE_INPUTS:
+                kc, vc = shared_cache(w)
+                _ORACLE_INPUTS[(w.name, "cache")] = (kc.numpy(), vc.numpy())
+            d["k_cache"], d["v_cache"] = _ORACLE_INPUTS[(w.name, "cache")]
+        _ORACLE_INPUTS[key] = d
+    return _ORACLE_INPUTS[key]
 
 
-def oracle_sample(w, budget_s: float, rows_per_call: int = None):
-    """Time the fp64 oracle on whole denoising steps' canvas rows until ~budget_s of CPU work.
+def oracle_rows(w, unit, rows):
+    """The oracle's output rows [r0, r1) of one forward of w (fp64 [r1 - r0, nh*hd])."""
+    import oracle
+    from gqa_canvas_attention_gb300.workloads import EPS
+    d = _oracle_inputs(w, unit)
+    out = oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"], d["v_cache"], w.nh,
+                         w.nkv, w.hd, d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta,
+                         pos0=w.pos0, rows=rows)
+    return out[rows[0]:rows[1]]
 
-    Returns (useful flops computed, seconds, threads, description)."""
+
+def oracle_sample(w, budget_s: float, threads: int = 0):
+    """Time the fp64 oracle on whole forwards' canvas rows, forward after forward, until about
+    budget_s of CPU work (on `threads` OpenMP threads, 0 = all host cores).
+
+    Returns (useful flops computed, seconds, threads used, description)."""
     import oracle
     from gqa_canvas_attention_gb300.workloads import EPS
 
-    threads = oracle.set_threads(0)
-    (kc, vc), d = _oracle_inputs(w, 0)
-    per_row = 4 * w.nh * w.S * w.hd
-    # calibrate on a few rows of step 0
-    t0 = time.perf_counter()
-    oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], kc, vc, w.nh, w.nkv, w.hd,
-                   d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta, pos0=w.pos0, rows=(0, 16))
-    t_row = (time.perf_counter() - t0) / 16
-    rows_total = max(1, int(budget_s / max(t_row, 1e-9)))
-    rows = min(w.T, rows_total) if rows_per_call is None else rows_per_call
-    flops, secs, step, done = 0, 0.0, 0, 0
-    while done < rows_total and step < w.steps:
-        _, d = _oracle_inputs(w, step)
-        r = min(rows, rows_total - done)
+    prev = oracle.set_threads(0)
+    used = oracle.set_threads(threads) if threads else prev
+    try:
+        d = _oracle_inputs(w, 0)
+        per_row = 4 * w.nh * w.S * w.hd
+        cal = min(16, w.T)
         t0 = time.perf_counter()
-        oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], kc, vc, w.nh, w.nkv, w.hd,
-                       d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta, pos0=w.pos0, rows=(0, r))
-        secs += time.perf_counter() - t0
-        flops += per_row * r
-        done += r
-        step += 1
-    desc = (f"{done} canvas rows x {w.nh} heads over {step} denoising step(s) of {w.name} "
-            f"(ctx={w.ctx}, T={w.T}, hd={w.hd}), fp64, OpenMP over (row, head)")
-    return flops, secs, threads, desc
+        oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"], d["v_cache"], w.nh,
+                       w.nkv, w.hd, d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta,
+                       pos0=w.pos0, rows=(0, cal))
+        t_row = (time.perf_counter() - t0) / cal
+        rows_total = max(1, int(budget_s / max(t_row, 1e-9)))
+        flops, secs, unit, done = 0, 0.0, 0, 0
+        while done < rows_total and unit < w.forwards():
+            d = _oracle_inputs(w, unit)
+            r = min(w.T, rows_total - done)
+            t0 = time.perf_counter()
+            oracle.forward(d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"], d["v_cache"], w.nh,
+                           w.nkv, w.hd, d["q_norm_w"], d["k_norm_w"], eps=EPS, theta=w.theta,
+                           pos0=w.pos0, rows=(0, r))
+            secs += time.perf_counter() - t0
+            flops += per_row * r
+            done += r
+            unit += 1
+    finally:
+        oracle.set_threads(prev)
+    what = "canvas" if w.canvases > 1 else "denoising step"
+    desc = (f"{done} canvas rows x {w.nh} heads over {unit} {what}(s) of {w.name} "
+            f"(ctx={w.ctx}, T={w.T}, hd={w.hd}), fp64, OpenMP over (row, head) on {used} "
+            f"thread(s)")
+    return flops, secs, used, desc
+
+
+CHECK_TOL = {"tc": (5e-3, 5e-4), "fp32": (1e-5, 1e-6)}
+
+
+def workload_config(w):
+    """The `config` object of a line: the workload and its sizes (the same in both arms)."""
+    return {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv, "hd": w.hd,
+            "denoise_steps": w.steps, "canvases": w.canvases,
+            "l2": "inputs larger than L2 between reuses (a fresh canvas per forward, the cache "
+                  "reused by a canvas's forwards)" if w.forwards() > 1 else
+                  "L2 flushed (a 256 MiB write) before every timed forward"}
+
+
+def check_rows(w, unit, got, path):
+    """Compare 64 rows (four runs of 16 across the canvas) of one forward's output -- a CPU
+    tensor [T, nh*hd] -- with the oracle's; raise if the parity tolerance is exceeded."""
+    import numpy as np
+    T = w.T
+    starts = sorted({0, T // 3, (2 * T) // 3, max(0, T - 16)})
+    spans = [(a, min(T, a + 16)) for a in starts]
+    errs = []
+    for a, b in spans:
+        ref = oracle_rows(w, unit, (a, b))
+        errs.append(np.abs(got[a:b].double().numpy() - ref).ravel())
+    e = np.concatenate(errs)
+    tmax, tmean = CHECK_TOL[path]
+    res = {"forward": unit, "rows": [list(x) for x in spans], "max_err": float(np.max(e)),
+           "mean_err": float(np.mean(e)), "tol_max": tmax, "tol_mean": tmean}
+    if not (np.isfinite(e).all() and res["max_err"] <= tmax and res["mean_err"] <= tmean):
+        raise RuntimeError(f"output check against the oracle failed: {res}")
+    return res
+
+
+def side_workloads(B, dev, args, peak, peaks):
+    """One forward of each other workload, with its own cache passed in (converted by the call),
+    L2 flushed before every timed forward: the median time of `side_reps` forwards, the attention
+    kernel's own time (events around its launches, a second pass), sampled rows checked with the
+    oracle, and the oracle's own rate (one core for single-forward workloads, all cores for a
+    batch of canvases)."""
+    import statistics
+    import torch
+    from gqa_canvas_attention_gb300.workloads import EPS, WORKLOADS, workload_inputs
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)      # 256 MiB > L2
+    res = {}
+    for name in SIDE_WORKLOADS:
+        w = WORKLOADS[name]
+        plan = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, w.theta)
+        if w.pos0 is not None:
+            plan.set(B.DG_OPT_POS0, w.pos0)
+        plan.set(B.DG_OPT_PATH, B.DG_PATH_TC if args.path == "tc" else B.DG_PATH_FP32)
+        ins = []
+        for c in range(w.canvases):
+            d = workload_inputs(w, canvas=c) if w.canvases > 1 else workload_inputs(w)
+            ins.append({k: (v.to(dev) if v is not None else None) for k, v in d.items()})
+        out = torch.empty((w.T, w.nh * w.hd), dtype=torch.float32, device=dev)
+
+        def fwd():
+            for d in ins:
+                plan.forward(d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"], d["v_cache"],
+                             d["q_norm_w"], d["k_norm_w"], None, out)
+
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        if plan.sync_status() != B.DG_OK:
+            raise RuntimeError(f"{name}: device status after warm-up")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(args.side_reps):
+            flush.zero_()
+            e0.record()
+            fwd()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        fwd_us = statistics.median(times) * 1e3 / w.canvases
+        plan.set(B.DG_OPT_PROFILE, 1)
+        for _ in range(args.side_reps):
+            flush.zero_()
+            fwd()
+        torch.cuda.synchronize()
+        st = {k: B.dg_attn_profile_read(plan.handle, v) for k, v in
+              (("attention", B.DG_STAGE_ATTENTION), ("norm_rope", B.DG_STAGE_NORM_ROPE),
+               ("combine", B.DG_STAGE_COMBINE), ("cache", B.DG_STAGE_CACHE))}
+        plan.set(B.DG_OPT_PROFILE, 0)
+        if plan.sync_status() != B.DG_OK:
+            raise RuntimeError(f"{name}: device status after the timed forwards")
+        chk = check_rows(w, w.canvases - 1 if w.canvases > 1 else 0, out.cpu(), args.path)
+        plan.close()
+        flops = w.flops_per_forward()
+        kern_us = st["attention"][0] / max(1, st["attention"][1]) * 1e3
+        r = {"us_per_forward": fwd_us, "tflops": flops / (fwd_us * 1e-6) / 1e12,
+             "attention_kernel_us": kern_us,
+             "attention_kernel_tflops": flops / (kern_us * 1e-6) / 1e12,
+             "frac": flops / (kern_us * 1e-6) / 1e12 / peak,
+             "stage_us_per_forward": {k: v[0] * 1e3 / max(1, args.side_reps * w.canvases)
+                                      for k, v in st.items()},
+             "check": chk, "useful_flop_per_forward": flops}
+        if not args.no_cpu_baseline:
+            f, sec, thr, desc = oracle_sample(w, args.cpu_side_budget_s,
+                                              threads=0 if w.canvases > 1 else 1)
+            r["oracle"] = {"tflops": f / sec / 1e12, "cores": thr, "sample": desc}
+        res[name] = r
+    return res
 
 
 def run_reference(args, w):
@@ -210,8 +348,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv,
-                   "hd": w.hd, "denoise_steps": w.steps},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": desc + " per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -340,6 +477,11 @@ def main():
     ms = ev0.elapsed_time(ev1)
     if plan.sync_status() != B.DG_OK:
         raise RuntimeError("device wait timed out in the timed region")
+    # the last forward of the last replay left its output in `out`: compare sampled rows of it
+    # with the oracle (outside the timed region); a mismatch fails the run
+    checked = {"timed": None, "e2e": None}
+    if not args.hidden and rank == 0:
+        checked["timed"] = check_rows(w, n_fwd - 1, out.cpu(), args.path)
 
     # ---------------------------------------------------------------- per-kernel times
     # Each kernel of a forward may start while the one before it finishes (programmatic
@@ -372,10 +514,35 @@ def main():
 
     # ---------------------------------------------------------------- roofline of the kernels
     peaks, src = measured_peaks()
-    tf32_peak = peaks["bf16_tflops_sustained"] * NOMINAL_TF32_OVER_BF16
-    attn_avg_s = attn_ms / max(1, attn_n) / 1e3
-    attn_tflops = flops_fwd / attn_avg_s / 1e12
-    norm_bytes = 2 * 4 * w.T * (w.nh + 2 * w.nkv) * w.hd     # fp32 in + 4 bytes out per element
+    tc = args.path == "tc"
+    # The tensor-core kernel runs kind::f16 MMAs (bf16 products for Q.K^T, fp16 for P.V): its
+    # peak is the measured bf16 burst rate (the kernel is timed launch by launch).  It executes
+    # two MMA units per useful one (three bf16 products for Q.K^T, one for P.V, against one each).
+    # The exact path runs fp32 FMAs on the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x the clock.
+    if tc:
+        attn_peak, attn_bound, exec_per_useful = peaks["bf16_tflops"], "tensor", 2.0
+        peak_src = f"{src}: bf16_tflops (burst cuBLAS bf16 GEMM; the kernel runs kind::f16 MMAs)"
+    else:
+        attn_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        attn_bound, exec_per_useful = "alu", 1.0
+        peak_src = "152 SMs x 128 fp32 lanes x 2 FLOP x sm_max_mhz"
+    ev_us = attn_ms / max(1, attn_n) * 1e3
+    live_us = None if args.hidden else ms_per_step * 1e3 / n_fwd
+    if live_us is not None and live_us < ev_us:
+        kern_us, kern_src = live_us, ("live: the whole forward's time in the timed region, "
+                                      "which bounds the kernel's (events around each launch gave "
+                                      f"{ev_us:.2f} us)")
+    else:
+        kern_us, kern_src = ev_us, ("CUDA events around each launch, "
+                                    f"{max(1, min(args.steps, 5))} replays of the step right after "
+                                    "the timed region")
+    attn_tflops = flops_fwd / (kern_us * 1e-6) / 1e12
+    # first stage: fp32 q, k, v read; q-hat and k-hat written as bf16 hi/lo (4 bytes per element)
+    # and v-hat as fp16 (2 bytes) for the tensor-core kernel, fp32 for the exact path
+    if tc:
+        norm_bytes = w.T * w.hd * (4 * (w.nh + 2 * w.nkv) + 4 * (w.nh + w.nkv) + 2 * w.nkv)
+    else:
+        norm_bytes = w.T * w.hd * 8 * (w.nh + 2 * w.nkv)
     norm_avg_s = norm_ms / max(1, norm_n) / 1e3
     norm_gbs = norm_bytes / norm_avg_s / 1e9 if norm_n else 0.0   # no first-stage launch on the
                                                                     # projection path (fused)
@@ -469,6 +636,10 @@ def main():
         torch.cuda.synchronize()
         if plan.sync_status() != B.DG_OK:
             raise RuntimeError("device wait timed out in the end-to-end run")
+        # the outputs copied back to the host by the last end-to-end step: first and last forward
+        if rank == 0:
+            checked["e2e"] = [check_rows(w, 0, h_out[0], args.path),
+                              check_rows(w, n_fwd - 1, h_out[n_fwd - 1], args.path)]
         ems, e2e_flops = replicas.aggregate(e0.elapsed_time(e1), flops_step * args.e2e_steps,
                                             dev if world > 1 else None)
         e2e = {"value": replicas.throughput(ems, e2e_flops) / 1e12,
@@ -481,54 +652,78 @@ def main():
     launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (plan.get(B.DG_INFO_LAUNCHES)
                                                            + (1 if args.hidden else 0)
                                                            + (3 if args.layer else 0))
+    plan.close()
+
+    # ---------------------------------------------------------------- the other workloads
+    side = None
+    if not args.no_side and not args.hidden and world == 1:
+        side = side_workloads(B, dev, args, attn_peak, peaks)
+
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16x3+f16" if args.path == "tc" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "ctx": w.ctx, "nh": w.nh, "nkv": w.nkv,
-                   "hd": w.hd, "denoise_steps": w.steps, "canvases": w.canvases,
-                   "path": args.path, "splits": splits, "cuda_graph": not args.no_graph,
-                   "l2": "inputs larger than L2 (fresh canvas per step, 8 MiB x 48 + 64 MiB cache)"},
+        "config": workload_config(w),
+        "run": {"path": args.path, "splits": splits, "cuda_graph": not args.no_graph,
+                "inputs_resident": True},
         "us_per_denoise_step": ms_per_step * 1e3 / n_fwd,
         "canvas_steps_per_s": n_fwd * args.steps * world / (ms / 1e3),
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf32_peak,
-                     "unit": "TFLOP/s", "frac": attn_tflops / tf32_peak,
-                     "traffic": attn_traffic() if args.path == "tc" and w.name == "denoise48_ctx8k"
-                     else None,
-                     "kernel": "attn_tc_kernel" if args.path == "tc" else "attn_fp32_kernel",
-                     "peak_source": f"{src}: bf16_tflops_sustained x nominal tf32/bf16 (1.1/2.25)",
-                     "avg_launch_us": attn_avg_s * 1e6, "launches": attn_n,
-                     "timing": f"CUDA events around each launch, {prof_steps} replays of the step "
-                               "right after the timed region (events between launches serialise "
-                               "them, so the timed region itself carries none)"},
+        "roofline": {"bound": attn_bound, "achieved": attn_tflops, "peak": attn_peak,
+                     "unit": "TFLOP/s", "frac": attn_tflops / attn_peak,
+                     "traffic": attn_traffic() if tc and w.name == "denoise48_ctx8k" else None,
+                     "kernel": "attn_tc_kernel" if tc else "attn_fp32_kernel",
+                     "peak_source": peak_src,
+                     "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"] if tc else None,
+                     "kernel_us": kern_us, "kernel_us_source": kern_src,
+                     "event_us_per_launch": ev_us, "launches": attn_n,
+                     "useful_flop_per_launch": flops_fwd,
+                     "executed_mma": None if not tc else {
+                         "tflops": attn_tflops * exec_per_useful,
+                         "frac": attn_tflops * exec_per_useful / attn_peak,
+                         "note": "MMA work the tensor pipe executes: Q.K^T as three bf16 products "
+                                 "(hi.hi + hi.lo + lo.hi) and P.V as one fp16 product, two units "
+                                 "per useful one; the scheme's ceiling is 0.5 of the peak in "
+                                 "useful FLOPs"},
+                     "tf32_nominal": None if not tc else {
+                         "peak": attn_peak * NOMINAL_TF32_OVER_BF16,
+                         "frac": attn_tflops / (attn_peak * NOMINAL_TF32_OVER_BF16),
+                         "note": "useful FLOPs against a TF32 rate of the measured bf16 burst "
+                                 "x the nominal tf32/bf16 ratio (1.1/2.25): the basis the target "
+                                 "is stated on; these MMAs do not run at that rate"}},
         "norm_rope": {"bound": "hbm", "achieved": norm_gbs, "peak": peaks["hbm_gbs"],
                       "unit": "GB/s", "frac": norm_gbs / peaks["hbm_gbs"],
-                      "avg_launch_us": norm_avg_s * 1e6, "bytes_per_launch": norm_bytes},
+                      "avg_launch_us": norm_avg_s * 1e6, "bytes_per_launch": norm_bytes,
+                      "bytes": "fp32 q, k, v read; bf16 hi/lo q-hat, k-hat and fp16 v-hat "
+                               "written" if tc else "fp32 q, k, v read and written"},
         "stage_ms_per_step": {k: v / rec_steps for k, v in (("norm_rope", norm_ms),
                               ("attention", attn_ms), ("combine", comb_ms), ("cache", cache_ms))},
         "gpu_launches": launches_per_step * args.steps,
+        "checked": all(c is not None for c in checked.values()) if not args.hidden else False,
+        "check": checked,
+        "configs": side,
         "projection": None if not args.hidden else {
             "H": args.hidden, "bound": "tensor",
             "useful_gflop_per_launch": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd / 1e9,
             "avg_launch_us": proj_ms / max(1, proj_n) * 1e3,
             "achieved": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd
                         / (proj_ms / max(1, proj_n) / 1e3) / 1e12,
-            "unit": "TFLOP/s", "peak": tf32_peak,
+            "unit": "TFLOP/s", "peak": attn_peak,
             "frac": 2 * w.T * args.hidden * (w.nh + 2 * w.nkv) * w.hd
-                    / (proj_ms / max(1, proj_n) / 1e3) / 1e12 / tf32_peak,
+                    / (proj_ms / max(1, proj_n) / 1e3) / 1e12 / attn_peak,
             "note": "input norm + q/k/v projections with the first stage fused (two launches), "
-                    "useful fp32-GEMM FLOPs; the step's value then includes this work"},
+                    "useful fp32-GEMM FLOPs against the bf16 burst peak (the GEMM runs three "
+                    "bf16 products); the step's value then includes this work"},
         "oproj": None if not args.layer else {
             "H": args.hidden, "bound": "tensor",
             "useful_gflop_per_launch": 2 * w.T * args.hidden * w.nh * w.hd / 1e9,
             "avg_launch_us": oproj_ms / max(1, oproj_n) * 1e3,
             "achieved": 2 * w.T * args.hidden * w.nh * w.hd / (oproj_ms / max(1, oproj_n) / 1e3) / 1e12,
-            "unit": "TFLOP/s", "peak": tf32_peak,
+            "unit": "TFLOP/s", "peak": attn_peak,
             "frac": 2 * w.T * args.hidden * w.nh * w.hd / (oproj_ms / max(1, oproj_n) / 1e3) / 1e12
-                    / tf32_peak,
+                    / attn_peak,
             "note": "operand split + o_proj GEMM + post-attention norm and residual add (three "
-                    "launches), useful fp32-GEMM FLOPs"},
+                    "launches), useful fp32-GEMM FLOPs against the bf16 burst peak"},
         "layer_us_per_forward": ms_per_step * 1e3 / n_fwd if args.layer else None,
         "e2e": e2e,
         "clocks": clk.summary(),
@@ -537,7 +732,9 @@ def main():
         f, s, threads, desc = oracle_sample(w, args.cpu_budget_s)
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
-    plan.close()
+        f1, s1, _, desc1 = oracle_sample(w, args.cpu_budget_s / 4, threads=1)
+        line["cpu_baseline"]["one_core"] = {"value": f1 / s1 / 1e12, "unit": "TFLOP/s",
+                                            "sample": desc1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
