@@ -546,6 +546,29 @@ def main():
     norm_avg_s = norm_ms / max(1, norm_n) / 1e3
     norm_gbs = norm_bytes / norm_avg_s / 1e9 if norm_n else 0.0   # no first-stage launch on the
                                                                     # projection path (fused)
+    # What one launch of that size can reach at all: a device-to-device copy moving the same
+    # bytes (half read, half written), timed the same way (events around each launch, L2 flushed
+    # by a larger write before each).
+    copy_ref = None
+    if norm_n:
+        half = norm_bytes // 8                                   # floats read = floats written
+        src_buf = torch.empty(half, dtype=torch.float32, device=dev)
+        dst_buf = torch.empty_like(src_buf)
+        flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+        ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(20):
+            flush.zero_()
+            ca.record()
+            dst_buf.copy_(src_buf)
+            cb.record()
+            cb.synchronize()
+            times.append(ca.elapsed_time(cb))
+        times.sort()
+        cu = times[len(times) // 2] * 1e3
+        copy_ref = {"bytes": 2 * half * 4, "us": cu, "gbs": 2 * half * 4 / (cu * 1e-6) / 1e9,
+                    "frac": 2 * half * 4 / (cu * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+        del src_buf, dst_buf, flush
 
     # ---------------------------------------------------------------- end to end from host memory
     # Each forward's canvas goes host -> device and its output device -> host through pinned
@@ -695,7 +718,8 @@ def main():
                       "unit": "GB/s", "frac": norm_gbs / peaks["hbm_gbs"],
                       "avg_launch_us": norm_avg_s * 1e6, "bytes_per_launch": norm_bytes,
                       "bytes": "fp32 q, k, v read; bf16 hi/lo q-hat, k-hat and fp16 v-hat "
-                               "written" if tc else "fp32 q, k, v read and written"},
+                               "written" if tc else "fp32 q, k, v read and written",
+                      "same_size_copy": copy_ref},
         "stage_ms_per_step": {k: v / rec_steps for k, v in (("norm_rope", norm_ms),
                               ("attention", attn_ms), ("combine", comb_ms), ("cache", cache_ms))},
         "gpu_launches": launches_per_step * args.steps,

@@ -114,13 +114,15 @@ template <int HD> struct Layout {
 // relative.  O is rescaled when a row's maximum exceeds m + 15, so P <= 2^15 (inside the fp16
 // range, 65504) in between.
 constexpr float kRescaleThreshold = 15.0f;
+constexpr float kHeadroom = 0.0f;
 
 // Rows [r0, r0 + nr) of the in-cluster merge of P partitions: out = sum_p w_p O_p with the
-// per-row weights w (already divided by the merged denominator).  The staged O rows are read
-// through distributed shared memory, whose latency is long: each thread takes U float4 columns
-// (of different rows) at once, so U * P loads are in flight per thread.
+// per-row weights w (already divided by the merged denominator).  The peers' staged O rows are
+// read through distributed shared memory, whose latency is long: each thread takes U float4
+// columns (of different rows) at once, so U * P loads are in flight per thread.  The CTA's own
+// rows (partition `self`) are read through the local shared-memory path.
 template <int P, int HD, int THREADS, int PITCH>
-__device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int r0, int nr,
+__device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int self, int r0, int nr,
                                                    const float *wgt, float *const *dst)
 {
     constexpr int V4 = HD / 4;
@@ -137,7 +139,8 @@ __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int r0, i
             if (item < n) {
                 const uint32_t off = (uint32_t)(((r0 + item / V4) * PITCH + 4 * (item % V4)) * 4);
 #pragma unroll
-                for (int q = 0; q < P; ++q) v[u][q] = dsmem_ld_f4(peer[q] + off);
+                for (int q = 0; q < P; ++q)
+                    v[u][q] = q == self ? lds_f4(smem_base + off) : dsmem_ld_f4(peer[q] + off);
             }
         }
 #pragma unroll
@@ -544,34 +547,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             }
             m_used = -INFINITY;
             l2 = make_float2(0.f, 0.f);
-            {
-                // Start the reference from the maximum over the piece's first score tile.
-                // Waiting for more tiles to take a wider maximum delayed the first softmax, and
-                // with it the first P.V and the refill of that buffer: two tiles at hd = 256 were
-                // 2.4% slower, all three buffers at hd = 64 1.3%.  A buffer's first phase is
-                // waited for again in the loop below; that wait returns at once.
-                constexpr int NW = 1;
-                const int nw = min(NW, nloc);
-                float m0 = -INFINITY;
-                for (int t = 0; t < nw; ++t) {
-                    const int bt = (base + t) % NSP;
-                    ok = mbar_wait_bounded(&s_full[bt], ((base + t) / NSP) & 1, limit);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    tc_fence_after();
-                    const int valid = p.S - (tile0 + t) * NK;
-                    constexpr int CW = NK % 32 == 0 ? 32 : 16;
-#pragma unroll 1
-                    for (int c = 0; c < NK / CW; ++c) {
-                        uint32_t sr[CW];
-                        tmem_ld_chunk<CW>(tbase + lane_off + C::SP_COL + bt * NK + CW * c, sr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < CW; ++i)
-                            if (CW * c + i < valid) m0 = fmaxf(m0, __uint_as_float(sr[i]));
-                    }
-                }
-                if (ok && nw > 0) m_used = m0;
-            }
+            // The reference starts at -inf: the first score tile of the piece takes the rescale
+            // branch below with alpha = 0 and sets it from that tile's maximum (a separate pass
+            // over the first tile for its maximum cost an extra read of the tile).
             for (int it = base; ok && it < base + nloc; ++it) {
                 const int b = it % NSP;
                 ok = mbar_wait_bounded(&s_full[b], (it / NSP) & 1, limit);
@@ -629,46 +607,17 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
                 }
                 const bool need = mx > m_used + kRescaleThreshold;
+                // A rescale moves the reference first and P of this tile is computed against the
+                // new one; O (in TMEM) is scaled only afterwards, once the previous P.V product
+                // has landed -- by then it usually has, so the softmax does not stall on it.
+                float alpha = 1.0f;
+                bool rescale_o = false;
                 if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = fmaxf(m_used, mx);
-                    const float alpha = exp2f(m_used - m_new);   // 0 while nothing is accumulated
-                    if (it > base) {
-                        // O is only touched once the previous P.V product (buffer (it-1) mod NSP)
-                        // has landed
-                        const int pb = (it - 1) % NSP;
-                        if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        tc_fence_after();
-                        const float2 a2 = make_float2(alpha, alpha);
-                        // two 32-column chunks per round trip to TMEM (one when the score row
-                        // already holds 64 registers)
-                        constexpr int RW = NK <= 32 ? 2 : 1;
-#pragma unroll 1
-                        for (int c = 0; c < HD / 32; c += RW) {
-                            uint32_t o0[32], o1[32];
-                            tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, o0);
-                            if constexpr (RW == 2) tmem_ld32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                const float2 x0 = mul_f32x2(
-                                    make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
-                                o0[i] = __float_as_uint(x0.x);
-                                o0[i + 1] = __float_as_uint(x0.y);
-                                if constexpr (RW == 2) {
-                                    const float2 x1 = mul_f32x2(
-                                        make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
-                                    o1[i] = __float_as_uint(x1.x);
-                                    o1[i + 1] = __float_as_uint(x1.y);
-                                }
-                            }
-                            tmem_st32(tbase + lane_off + C::O_COL + 32 * c, o0);
-                            if constexpr (RW == 2) tmem_st32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
-                        }
-                        tmem_wait_st();
-                    }
+                    const float m_new = fmaxf(m_used, mx + kHeadroom);
+                    alpha = exp2f(m_used - m_new);          // 0 while nothing is accumulated
                     l2 = mul_f32x2(l2, make_float2(alpha, alpha));
                     m_used = m_new;
+                    rescale_o = it > base;                  // warp-uniform
                 }
                 // P in fp16, two keys per 32-bit column, written over the start of the score buffer
                 // (chunk c of 32 scores lands in columns 16c..16c+15, already read).  The denominator
@@ -712,6 +661,36 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     }
                 }
                 tmem_wait_st();
+                if (rescale_o) {
+                    // O is only touched once the previous P.V product (buffer (it-1) mod NSP) has
+                    // landed; two 32-column chunks per round trip to TMEM
+                    const int pb = (it - 1) % NSP;
+                    if (!mbar_wait_bounded(&sp_free[pb], ((it - 1) / NSP) & 1, limit)) ok = false;
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; c += 2) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                        tmem_ld32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 x0 = mul_f32x2(
+                                make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
+                            const float2 x1 = mul_f32x2(
+                                make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
+                            o0[i] = __float_as_uint(x0.x);
+                            o0[i + 1] = __float_as_uint(x0.y);
+                            o1[i] = __float_as_uint(x1.x);
+                            o1[i + 1] = __float_as_uint(x1.y);
+                        }
+                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c, o0);
+                        tmem_st32(tbase + lane_off + C::O_COL + 32 * c + 32, o1);
+                    }
+                    tmem_wait_st();
+                }
                 tc_fence_before();
                 if (!(p.inject_stall && it == 0)) mbar_arrive(&p_full[b]);
             }
@@ -840,13 +819,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         const uint32_t sb = smem_u32(smem);
         constexpr int TH = Lay::THREADS, PI = Lay::STG_PITCH;
         switch (P) {
-        case 2: cluster_merge_rows<2, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        case 3: cluster_merge_rows<3, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        case 4: cluster_merge_rows<4, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        case 5: cluster_merge_rows<5, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        case 6: cluster_merge_rows<6, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        case 7: cluster_merge_rows<7, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
-        default: cluster_merge_rows<8, HD, TH, PI>(sb, r0, nr, wgt, dst); break;
+        case 2: cluster_merge_rows<2, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 3: cluster_merge_rows<3, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 4: cluster_merge_rows<4, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 5: cluster_merge_rows<5, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 6: cluster_merge_rows<6, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 7: cluster_merge_rows<7, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        default: cluster_merge_rows<8, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
         }
         // no CTA leaves (or frees its shared memory) while a peer may still read it
         cluster_sync_all();

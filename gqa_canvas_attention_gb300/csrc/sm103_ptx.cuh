@@ -162,6 +162,17 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t caddr)
     return v;
 }
 
+// 16-byte load from this CTA's own shared memory (a shared::cta address).
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t caddr)
 {
     float v;

@@ -29,8 +29,10 @@ def _lib():
 
 
 def planned(d, nh, nkv, hd, ctx, T, cos_sin, pos0):
+    """dg_attn_forward on the fp32 path with one key partition: the arithmetic of the
+    allocation-free entry point, so the two agree to rounding."""
     plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
-    plan.set(B.DG_OPT_PATH, B.DG_PATH_FP32)
+    plan.set(B.DG_OPT_PATH, B.DG_PATH_FP32).set(B.DG_OPT_SPLITS, 1)
     if pos0 >= 0:
         plan.set(B.DG_OPT_POS0, pos0)
     out = plan.forward(d["q"], d["k_canvas"], d["v_canvas"], d["k_cache"], d["v_cache"],
