@@ -22,6 +22,7 @@
 #include <cstring>
 #include <initializer_list>
 #include <new>
+#include <utility>
 #include <vector>
 
 namespace {
@@ -109,6 +110,15 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, void *base, ui
     return r == CUDA_SUCCESS;
 }
 
+// The operand arrays the first stage writes and the tensor-core attention kernel reads, with the
+// kernel's tensor maps over them.
+struct OperandSet {
+    __nv_bfloat16 *qh, *ql;      // [nkv, rows_pad, hd] q-hat bf16 hi / lo (kernel layouts)
+    __nv_bfloat16 *kh, *kl;      // [nkv, S, hd] k-hat bf16 hi / lo: cache rows, then canvas rows
+    __half *vh;                  // [nkv, S, hd] v-hat fp16
+    dg::TcMaps maps;
+};
+
 }  // namespace
 
 struct dg_attn_plan {
@@ -132,8 +142,12 @@ struct dg_attn_plan {
     bool rope_dirty;             // rope_cs does not hold the current pos0 yet
     uint32_t *status;
     float *q32, *k32, *v32;
-    __nv_bfloat16 *qh, *ql, *kh, *kl;
-    __half *vh;
+    // Tensor-core operands: `op` is the set the next attention kernel reads.  With resident
+    // inputs a second set `alt` is allocated and each forward swaps the two, so that a forward's
+    // first stage writes the set the previous forward's attention kernel is not reading.
+    OperandSet op, alt;
+    bool alt_cache;              // alt holds the prepared cache rows too
+    unsigned long long attn_launched;   // tensor-core attention kernels enqueued
     float *part_o;
     float2 *part_ml;
     int part_capacity;           // partitions the partial buffers hold
@@ -184,8 +198,10 @@ void *dalloc(dg_attn_plan *p, size_t bytes, cudaError_t &err)
 void free_scratch(dg_attn_plan *p)
 {
     void *ptrs[] = {p->woh, p->wol, p->aoh, p->aol, p->ybuf, p->part_ss, p->ln_post, p->attn_buf,
-                    p->wh, p->wl, p->xh, p->xl, p->rin, p->c32k, p->c32v, p->inv_freq, p->rope_cs, p->status, p->q32, p->k32, p->v32, p->qh, p->ql,
-                    p->kh, p->kl, p->vh, p->part_o, p->part_ml};
+                    p->wh, p->wl, p->xh, p->xl, p->rin, p->c32k, p->c32v, p->inv_freq, p->rope_cs,
+                    p->status, p->q32, p->k32, p->v32, p->op.qh, p->op.ql, p->op.kh, p->op.kl,
+                    p->op.vh, p->alt.qh, p->alt.ql, p->alt.kh, p->alt.kl, p->alt.vh, p->part_o,
+                    p->part_ml};
     for (void *x : ptrs)
         if (x) cudaFree(x);
     for (auto &v : p->ev) {
@@ -389,18 +405,37 @@ int record_event(dg_attn_plan *p, int stage, cudaStream_t s)
     return err == cudaSuccess ? DG_OK : cuda_fail(err, "cudaEventRecord");
 }
 
-int build_maps(dg_attn_plan *p)
+// Allocate one operand set and encode its tensor maps.
+int alloc_set(dg_attn_plan *p, OperandSet &o)
 {
+    const size_t nqt = (size_t)p->nkv * p->rows_pad * p->hd, nkt = (size_t)p->nkv * p->S * p->hd;
+    cudaError_t err = cudaSuccess;
+    o.qh = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
+    o.ql = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
+    o.kh = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
+    o.kl = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
+    o.vh = (__half *)dalloc(p, nkt * 2, err);
+    if (err != cudaSuccess) {
+        const size_t sizes[5] = {nqt * 2, nqt * 2, nkt * 2, nkt * 2, nkt * 2};
+        void *ptrs[5] = {o.qh, o.ql, o.kh, o.kl, o.vh};
+        for (int i = 0; i < 5; ++i)
+            if (ptrs[i]) {
+                cudaFree(ptrs[i]);
+                p->scratch_bytes -= sizes[i];
+            }
+        o = OperandSet{};
+        return cuda_fail(err, "allocating the tensor-core operand arrays");
+    }
     const dg::TcGeom geo = dg::tc_geometry(p->hd);
     const int nk = geo.nk;
     bool ok = true;
-    ok &= encode_3d(&p->maps.ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->ql, p->hd, p->rows_pad,
+    ok &= encode_3d(&o.maps.ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.ql, p->hd, p->rows_pad,
                     p->nkv, 64, dg::kTileM, p->hd);
-    ok &= encode_3d(&p->maps.kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kh, p->hd, p->S, p->nkv,
+    ok &= encode_3d(&o.maps.kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.kh, p->hd, p->S, p->nkv,
                     64, nk, p->hd);
-    ok &= encode_3d(&p->maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->kl, p->hd, p->S, p->nkv,
+    ok &= encode_3d(&o.maps.kl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.kl, p->hd, p->S, p->nkv,
                     64, nk, p->hd);
-    ok &= encode_3d(&p->maps.vh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->vh, p->hd, p->S, p->nkv,
+    ok &= encode_3d(&o.maps.vh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, o.vh, p->hd, p->S, p->nkv,
                     64, geo.vk, p->hd);
     if (!ok) {
         set_error("cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
@@ -420,9 +455,41 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
     n.do_norm = 1; n.do_rope = 1;
     n.inputs_resident = p->inputs_resident;
     n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
-    n.qh = p->qh; n.ql = p->ql; n.kh = p->kh; n.kl = p->kl; n.vh = p->vh;
+    n.qh = p->op.qh; n.ql = p->op.ql; n.kh = p->op.kh; n.kl = p->op.kl; n.vh = p->op.vh;
     n.ql_interleaved = p->tc_ok ? dg::tc_geometry(p->hd).ql_in_tmem : 0;
     return n;
+}
+
+// With resident inputs on the tensor-core path, make the other operand set the current one and
+// return 1: the first stage then writes a set the previous forward's attention kernel does not
+// read, and need not wait for that kernel (the ordering argument is in the first-stage and
+// attention kernels).  A prepared cache is copied into a set that lacks it, once, on the stream.
+int swap_sets(dg_attn_plan *p, cudaStream_t s, int &other)
+{
+    other = 0;
+    if (p->path != DG_PATH_TC || !p->inputs_resident || !p->alt.qh) return DG_OK;
+    if (p->ctx > 0 && p->cache_ready && !p->alt_cache) {
+        const size_t pitch = (size_t)p->S * p->hd * 2, width = (size_t)p->ctx * p->hd * 2;
+        cudaError_t err = cudaSuccess;
+        const void *src[3] = {p->op.kh, p->op.kl, p->op.vh};
+        void *dst[3] = {p->alt.kh, p->alt.kl, p->alt.vh};
+        for (int i = 0; i < 3 && err == cudaSuccess; ++i)
+            err = cudaMemcpy2DAsync(dst[i], pitch, src[i], pitch, width, p->nkv,
+                                    cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "copying the prepared cache rows");
+        p->alt_cache = true;
+    }
+    std::swap(p->op, p->alt);
+    other = 1;
+    return DG_OK;
+}
+
+// A call that swapped the sets and then failed before its attention kernel was enqueued swaps
+// them back: the current set must stay the one the last enqueued attention kernel reads.
+int unswap_unless_launched(dg_attn_plan *p, int rc, int other, unsigned long long launched)
+{
+    if (rc != DG_OK && other && p->attn_launched == launched) std::swap(p->op, p->alt);
+    return rc;
 }
 
 // Attention + (when partitioned) combine, reading the operands the first stage left in scratch.
@@ -447,7 +514,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
     cudaError_t err;
     if (p->path == DG_PATH_TC) {
         dg::AttnTcParams a{};
-        a.qh = p->qh; a.ql = p->ql; a.out = out; a.part_o = p->part_o; a.part_ml = p->part_ml;
+        a.qh = p->op.qh; a.ql = p->op.ql; a.out = out; a.part_o = p->part_o; a.part_ml = p->part_ml;
         a.status = p->status;
         a.wait_limit_ns = (unsigned long long)p->wait_limit_ms * 1000000ull;
         a.T = p->T; a.nh = p->nh; a.nkv = p->nkv; a.S = p->S; a.G = p->G;
@@ -460,8 +527,9 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
             a.sk_units = sk.units;
             a.qtiles = p->rows_pad / dg::kTileM;
         }
-        err = dg::launch_attn_tc(a, p->maps, p->hd, s);
+        err = dg::launch_attn_tc(a, p->op.maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
+        ++p->attn_launched;
     } else {
         dg::AttnFp32Params a{};
         a.q = p->q32; a.k = p->k32; a.v = p->v32;
@@ -526,8 +594,8 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
     }
     if (p->path == DG_PATH_TC) {
         // the per-call conversion overwrites the plan's cache copy
-        p->cache_ready = false;
-        dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
+        p->cache_ready = p->alt_cache = false;
+        dg::CachePrepParams c{k_cache, v_cache, p->op.kh, p->op.kl, p->op.vh, nullptr, nullptr,
                               p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32, p->status};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
@@ -617,7 +685,6 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     p->num_sms = prop.multiProcessorCount;
 
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
-    const size_t nqt = (size_t)nkv * p->rows_pad * hd, nkt = (size_t)nkv * p->S * hd;
     p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
     p->rope_cs = (float *)dalloc(p, sizeof(float) * 2 * (size_t)T * hd, err);
     p->rope_dirty = true;
@@ -625,13 +692,6 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     p->q32 = (float *)dalloc(p, nq * sizeof(float), err);
     p->k32 = (float *)dalloc(p, nk * sizeof(float), err);
     p->v32 = (float *)dalloc(p, nk * sizeof(float), err);
-    if (p->tc_ok) {
-        p->qh = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
-        p->ql = (__nv_bfloat16 *)dalloc(p, nqt * 2, err);
-        p->kh = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
-        p->kl = (__nv_bfloat16 *)dalloc(p, nkt * 2, err);
-        p->vh = (__half *)dalloc(p, nkt * 2, err);
-    }
     if (err != cudaSuccess) {
         cuda_fail(err, "allocating plan scratch");
         free_scratch(p);
@@ -651,7 +711,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
                                   ? dg::attn_tc_max_clusters(hd, sp, p->rows_pad / dg::kTileM, nkv)
                                   : 0;
     int rc = (err == cudaSuccess) ? DG_OK : cuda_fail(err, "plan set-up");
-    if (rc == DG_OK && p->tc_ok) rc = build_maps(p);
+    if (rc == DG_OK && p->tc_ok) rc = alloc_set(p, p->op);
     if (rc == DG_OK) {
         // room for the partitions both paths would pick
         const int saved = p->path;
@@ -735,7 +795,7 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
             set_error("unknown path %lld", value);
             return DG_ERR_ARG;
         }
-        if (p->path != (int)value) p->cache_ready = false;
+        if (p->path != (int)value) p->cache_ready = p->alt_cache = false;
         p->path = (int)value;
         return DG_OK;
     case DG_OPT_POS0:
@@ -779,6 +839,10 @@ int dg_attn_set_option(dg_attn_plan *p, int key, long long value)
         p->inject_stall = value ? 1 : 0;
         return DG_OK;
     case DG_OPT_INPUTS_RESIDENT:
+        if (value && p->tc_ok && !p->alt.qh) {
+            if (int rc = alloc_set(p, p->alt)) return rc;
+            p->alt_cache = false;
+        }
         p->inputs_resident = value ? 1 : 0;
         return DG_OK;
     case DG_OPT_PROFILE:
@@ -866,7 +930,7 @@ int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void
     }
     const int type = dtype == DG_DTYPE_F16 ? dg::kCacheF16
                    : dtype == DG_DTYPE_BF16 ? dg::kCacheBf16 : dg::kCacheF32;
-    dg::CachePrepParams c{k_cache, v_cache, p->kh, p->kl, p->vh, nullptr, nullptr,
+    dg::CachePrepParams c{k_cache, v_cache, p->op.kh, p->op.kl, p->op.vh, nullptr, nullptr,
                           p->nkv, p->ctx, p->S, p->S_pad, p->hd, type, p->status};
     if (p->path == DG_PATH_FP32) {
         if (dtype == DG_DTYPE_F32) {
@@ -888,9 +952,14 @@ int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void
     }
     int rc = record_event(p, DG_STAGE_CACHE, s);
     if (rc) return rc;
+    if (p->path == DG_PATH_TC && p->alt.qh) {
+        // the second operand set gets the same rows in the same pass
+        c.kh2 = p->alt.kh; c.kl2 = p->alt.kl; c.vh2 = p->alt.vh;
+    }
     cudaError_t err = dg::launch_cache_prep(c, s);
     if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
     if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
+    p->alt_cache = p->path == DG_PATH_TC && p->alt.qh;
     if (p->path == DG_PATH_FP32) {
         p->prep_k = p->c32k;
         p->prep_v = p->c32v;
@@ -931,17 +1000,25 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
                                                 {k_cache, cb}, {v_cache, cb}, {q_norm_w, wb},
                                                 {k_norm_w, wb}, {cos_sin, 2 * (size_t)p->T * wb}}))
         return rc;
-    if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
-    if (int rc = rope_table(p, cos_sin, s)) return rc;
-    dg::NormRopeParams n = norm_params(p);
-    n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
-    const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
-    int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
-    if (rc) return rc;
-    cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
-    if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
-    if ((rc = record_event(p, DG_STAGE_NORM_ROPE, s))) return rc;
-    return enqueue_attention(p, k_cache, v_cache, out, s);
+    int other;
+    if (int rc = swap_sets(p, s, other)) return rc;
+    const unsigned long long launched = p->attn_launched;
+    auto run = [&]() -> int {
+        if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+        if (int rc = rope_table(p, cos_sin, s)) return rc;
+        dg::NormRopeParams n = norm_params(p);
+        n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w;
+        n.cos_sin = cos_sin;
+        n.other_set = other;
+        const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
+        int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
+        if (rc) return rc;
+        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+        if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
+        if ((rc = record_event(p, DG_STAGE_NORM_ROPE, s))) return rc;
+        return enqueue_attention(p, k_cache, v_cache, out, s);
+    };
+    return unswap_unless_launched(p, run(), other, launched);
 }
 
 int dg_attn_norm_rope(dg_attn_plan *p, const float *q, const float *k_canvas,
@@ -987,15 +1064,22 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
                                                     {k_cache, cb}, {v_cache, cb}}))
             return rc;
     }
-    if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
-    // the first-stage kernel with norm and rope switched off only re-lays the operands out
-    dg::NormRopeParams n = norm_params(p);
-    n.q = q_hat; n.k = k_hat; n.v = v_hat;
-    n.do_norm = 0; n.do_rope = 0;
-    const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
-    cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
-    if (err != cudaSuccess) return cuda_fail(err, "operand layout launch");
-    return enqueue_attention(p, k_cache, v_cache, out, s);
+    int other;
+    if (int rc = swap_sets(p, s, other)) return rc;
+    const unsigned long long launched = p->attn_launched;
+    auto run = [&]() -> int {
+        if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+        // the first-stage kernel with norm and rope switched off only re-lays the operands out
+        dg::NormRopeParams n = norm_params(p);
+        n.q = q_hat; n.k = k_hat; n.v = v_hat;
+        n.other_set = other;
+        n.do_norm = 0; n.do_rope = 0;
+        const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
+        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+        if (err != cudaSuccess) return cuda_fail(err, "operand layout launch");
+        return enqueue_attention(p, k_cache, v_cache, out, s);
+    };
+    return unswap_unless_launched(p, run(), other, launched);
 }
 
 int dg_attn_proj_prepare(dg_attn_plan *p, int H, const float *ln_in_w, const float *wq,
@@ -1108,7 +1192,7 @@ int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache
     q.wq_norm = q_norm_w;
     q.wk_norm = k_norm_w;
     q.cos_sin = cos_sin;
-    q.qh = p->qh; q.ql = p->ql; q.kh = p->kh; q.kl = p->kl; q.vh = p->vh;
+    q.qh = p->op.qh; q.ql = p->op.ql; q.kh = p->op.kh; q.kl = p->op.kl; q.vh = p->op.vh;
     q.status = p->status;
     q.wait_limit_ns = (unsigned long long)p->wait_limit_ms * 1000000ull;
     q.T = p->T; q.H = p->H; q.nh = p->nh; q.nkv = p->nkv; q.G = p->G; q.ctx = p->ctx; q.S = p->S;

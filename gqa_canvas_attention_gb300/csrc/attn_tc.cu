@@ -193,8 +193,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     uint64_t *drain = o_free + 1;           // [NQI + 1]: one per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + NQI + 1);
 
-    // the next kernel of the stream may be scheduled now; it waits for this one to finish
-    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
@@ -271,6 +269,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     const uint32_t tbase = *tmem_slot;
     // the operands are written by the kernel before this one in the stream
     pdl_wait();
+    // Only now may the next kernel of the stream be scheduled.  With resident inputs the plan
+    // alternates two operand sets, and the next forward's first stage writes the set this kernel
+    // does not read without waiting for anything; its start after this point is what guarantees
+    // that the attention kernel before this one, the last reader of that set, has finished.
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ---------------------------------------------------------------- K producer

@@ -69,12 +69,17 @@ __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
         ul.x = *reinterpret_cast<uint32_t *>(&l01); ul.y = *reinterpret_cast<uint32_t *>(&l23);
         *reinterpret_cast<uint2 *>(p.kh + dst) = uh;
         *reinterpret_cast<uint2 *>(p.kl + dst) = ul;
+        if (p.kh2) {
+            *reinterpret_cast<uint2 *>(p.kh2 + dst) = uh;
+            *reinterpret_cast<uint2 *>(p.kl2 + dst) = ul;
+        }
         out_of_range |= !(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) <=
                           kF16Max);
         __half2 v01 = __floats2half2_rn(v.x, v.y), v23 = __floats2half2_rn(v.z, v.w);
         uint2 uv;
         uv.x = *reinterpret_cast<uint32_t *>(&v01); uv.y = *reinterpret_cast<uint32_t *>(&v23);
         *reinterpret_cast<uint2 *>(p.vh + dst) = uv;
+        if (p.vh2) *reinterpret_cast<uint2 *>(p.vh2 + dst) = uv;
     }
     if (__any_sync(0xffffffffu, out_of_range) && (threadIdx.x & 31) == 0 && p.status)
         atomicOr(p.status, kErrRange);

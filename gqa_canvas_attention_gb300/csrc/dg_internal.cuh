@@ -45,6 +45,9 @@ struct NormRopeParams {
     int do_norm, do_rope;          // 0/1 (the attention-only entry point passes 0, 0)
     int inputs_resident;           // 1: q, k, v, weights and cos_sin are complete before the
                                    // previous kernel in the stream started (DG_OPT_INPUTS_RESIDENT)
+    int other_set;                 // 1: the operand arrays written here are not the ones the
+                                   // previous forward's attention kernel reads (the plan
+                                   // alternates two sets), so the stores need not wait for it
     // kOutFp32 destinations
     float *q_out, *k_out, *v_out;
     // kOutTc destinations
@@ -68,6 +71,8 @@ struct CachePrepParams {
     int nkv, ctx, S, S_pad, hd;
     int dtype;                     // CacheType
     uint32_t *status;              // kErrRange is OR-ed in for a V value beyond the fp16 range
+    __nv_bfloat16 *kh2, *kl2;      // null, or a second set of tensor-core arrays written with
+    __half *vh2;                   // the same rows (the plan's other operand set)
 };
 
 struct AttnFp32Params {

@@ -119,8 +119,11 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     constexpr int LPR = R::LPR, RPI = R::RPI;
     constexpr int RG = 2;                         // rows per lane
     // The inputs may come from the kernel before this one in the stream: wait for it first,
-    // unless the caller has declared them resident (then only the stores below wait, and the
-    // loads and arithmetic overlap the end of the previous forward's attention kernel).
+    // unless the caller has declared them resident.  Then, if the arrays written here are the
+    // ones the previous forward's attention kernel reads, only the stores below wait (the loads
+    // and arithmetic overlap the end of that kernel); if they are the other operand set, nothing
+    // waits but one thread at the very end, which keeps this grid from completing before the
+    // kernel ahead of it.
     pdl_launch_dependents();
     if (!p.inputs_resident) pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     }
 
     // the operand arrays are read by the previous forward's attention kernel until it ends
-    if (p.inputs_resident) pdl_wait();
+    if (p.inputs_resident && !p.other_set) pdl_wait();
 
 #pragma unroll
     for (int g = 0; g < RG; ++g) {
@@ -284,6 +287,10 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
             }
         }
     }
+    // With the other operand set nothing above waited.  One thread waits here, so that this grid
+    // completes only after the kernel ahead of it: the attention kernel that follows relies on
+    // that before it writes the output and partial buffers the one ahead also writes.
+    if (p.other_set && p.inputs_resident && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 // The cos|sin table of the canvas positions pos0 .. pos0 + T - 1: row t = cos(hd) | sin(hd), both

@@ -84,7 +84,13 @@ typedef struct dg_attn_plan dg_attn_plan;
                                    canvases already resident in device memory: the first stage then
                                    reads them while the previous call's attention kernel is still
                                    running.  Default 0: the first stage waits for the preceding
-                                   kernel before reading anything.  Scheduling only (the page
+                                   kernel before reading anything.  On the tensor-core path,
+                                   switching it on allocates a second set of operand arrays (the
+                                   size of the first, DG_INFO_SCRATCH_BYTES grows); forwards then
+                                   alternate between the two sets, so a forward's first stage
+                                   writes the set the previous attention kernel is not reading and
+                                   waits for nothing.  Consecutive calls must then share one
+                                   stream, or the caller orders them.  Scheduling only (the page
                                    records all dispatches of a forward into one pass) */
 #define DG_OPT_SCHEDULE      8  /* how the tensor-core kernel deals key tiles to CTAs: one of
                                    DG_SCHEDULE_AUTO (default), DG_SCHEDULE_SPLIT,

@@ -469,6 +469,56 @@ def test_resident_inputs_give_the_same_bits():
     check(outs[1][3], oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, all_rows(T), "resident")
 
 
+def test_resident_operand_sets_across_entry_points_and_a_failed_call():
+    """With DG_OPT_INPUTS_RESIDENT the plan keeps a second set of tensor-core operand arrays and
+    each forward's first stage writes the set the previous forward's attention kernel is not
+    reading.  A sequence that switches the option on after the cache is prepared (the prepared
+    rows are then copied into the new set), mixes forward, attend and a per-call cache, and has a
+    call in the middle that fails before any launch, must give the same bits as the same sequence
+    without the option, and match the oracle."""
+    T, ctx, nh, nkv, hd = 130, 700, 8, 2, 128
+    hosts = [make_inputs(T, ctx, nh, nkv, hd, seed=70 + i) for i in range(4)]
+    other_cache = make_inputs(T, ctx, nh, nkv, hd, seed=80)
+    cv = [to_dev(h) for h in hosts]
+    c2 = to_dev(other_cache)
+    results = []
+    for resident in (0, 1):
+        plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+        base = plan.get(B.DG_INFO_SCRATCH_BYTES)
+        plan.cache_prepare(cv[0]["k_cache"], cv[0]["v_cache"])
+        # the attend call's inputs, complete before the sequence (resident inputs must be)
+        qh, kh, vh = plan.norm_rope(cv[2]["q"], cv[2]["k_canvas"], cv[2]["v_canvas"],
+                                    cv[2]["q_norm_w"], cv[2]["k_norm_w"])
+        torch.cuda.synchronize()
+        plan.set(B.DG_OPT_INPUTS_RESIDENT, resident)
+        assert (plan.get(B.DG_INFO_SCRATCH_BYTES) > base) == bool(resident)
+
+        def fw(c, kc=None, vc=None):
+            return plan.forward(c["q"], c["k_canvas"], c["v_canvas"], kc, vc, c["q_norm_w"],
+                                c["k_norm_w"])
+
+        outs = [fw(cv[0]), fw(cv[1])]                    # the prepared cache
+        outs.append(plan.attend(qh, kh, vh))
+        outs.append(fw(cv[3], c2["k_cache"], c2["v_cache"]))   # replaces the prepared cache
+        with pytest.raises(B.DgAttnError) as e:
+            fw(cv[0])                                    # no cache given and none prepared
+        assert e.value.status == B.DG_ERR_STATE
+        outs.append(fw(cv[1], c2["k_cache"], c2["v_cache"]))
+        plan.cache_prepare(cv[0]["k_cache"], cv[0]["v_cache"])
+        outs += [fw(cv[2]), fw(cv[3])]
+        assert plan.sync_status() == B.DG_OK
+        results.append(outs)
+    for i, (a, b) in enumerate(zip(*results)):
+        assert torch.equal(a, b), i
+    caches = [0, 0, 0, None, None, 0, 0]
+    canvases = [0, 1, 2, 3, 1, 2, 3]
+    for o, ci, ca in zip(results[1], canvases, caches):
+        d = dict(hosts[ci])
+        src = hosts[0] if ca == 0 else other_cache
+        d["k_cache"], d["v_cache"] = src["k_cache"], src["v_cache"]
+        check(o, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, all_rows(T), f"canvas{ci}")
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PNAME[p])
 def test_sixteen_bit_cache_twin(dtype, path):
