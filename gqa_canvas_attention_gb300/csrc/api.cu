@@ -457,7 +457,20 @@ dg::NormRopeParams norm_params(const dg_attn_plan *p)
     n.q_out = p->q32; n.k_out = p->k32; n.v_out = p->v32;
     n.qh = p->op.qh; n.ql = p->op.ql; n.kh = p->op.kh; n.kl = p->op.kl; n.vh = p->op.vh;
     n.ql_interleaved = p->tc_ok ? dg::tc_geometry(p->hd).ql_in_tmem : 0;
+    n.status = p->status;
     return n;
+}
+
+// Hand a per-call cache to the first-stage launch (its last blocks convert it).
+void fuse_cache(const dg_attn_plan *p, dg::NormRopeParams &n, const float *k_cache,
+                const float *v_cache)
+{
+    const long long n4 = (long long)p->nkv * p->ctx * p->hd / 4;
+    const long long per_block = 128ll * dg::kNormCacheUnroll;
+    n.kc = k_cache;
+    n.vc = v_cache;
+    n.cache_blocks = (int)std::min<long long>((n4 + per_block - 1) / per_block,
+                                              (long long)p->num_sms * 16);
 }
 
 // With resident inputs on the tensor-core path, make the other operand set the current one and
@@ -563,9 +576,13 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
     return DG_OK;
 }
 
-// Resolve which cache the attention reads; converts a per-call cache on the tensor-core path.
-int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache, cudaStream_t s)
+// Resolve which cache the attention reads.  A per-call cache on the tensor-core path is
+// converted into the current operand set: by the first-stage launch when `fused` is given (set
+// to true here; the caller hands the cache to that launch), else by a launch of its own.
+int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache, cudaStream_t s,
+                  bool *fused = nullptr)
 {
+    if (fused) *fused = false;
     if (p->ctx == 0) {
         if (k_cache || v_cache) {
             set_error("ctx == 0: k_cache and v_cache must be NULL");
@@ -595,6 +612,10 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
     if (p->path == DG_PATH_TC) {
         // the per-call conversion overwrites the plan's cache copy
         p->cache_ready = p->alt_cache = false;
+        if (fused) {
+            *fused = true;
+            return DG_OK;
+        }
         dg::CachePrepParams c{k_cache, v_cache, p->op.kh, p->op.kl, p->op.vh, nullptr, nullptr,
                               p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32, p->status};
         int rc = record_event(p, DG_STAGE_CACHE, s);
@@ -1004,12 +1025,14 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
     if (int rc = swap_sets(p, s, other)) return rc;
     const unsigned long long launched = p->attn_launched;
     auto run = [&]() -> int {
-        if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+        bool fused;
+        if (int rc = resolve_cache(p, k_cache, v_cache, s, &fused)) return rc;
         if (int rc = rope_table(p, cos_sin, s)) return rc;
         dg::NormRopeParams n = norm_params(p);
         n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w;
         n.cos_sin = cos_sin;
         n.other_set = other;
+        if (fused) fuse_cache(p, n, k_cache, v_cache);
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
         int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
         if (rc) return rc;
@@ -1068,11 +1091,13 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
     if (int rc = swap_sets(p, s, other)) return rc;
     const unsigned long long launched = p->attn_launched;
     auto run = [&]() -> int {
-        if (int rc = resolve_cache(p, k_cache, v_cache, s)) return rc;
+        bool fused;
+        if (int rc = resolve_cache(p, k_cache, v_cache, s, &fused)) return rc;
         // the first-stage kernel with norm and rope switched off only re-lays the operands out
         dg::NormRopeParams n = norm_params(p);
         n.q = q_hat; n.k = k_hat; n.v = v_hat;
         n.other_set = other;
+        if (fused) fuse_cache(p, n, k_cache, v_cache);
         n.do_norm = 0; n.do_rope = 0;
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
         cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);

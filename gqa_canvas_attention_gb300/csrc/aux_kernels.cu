@@ -5,6 +5,7 @@
 //    hi/lo pair, V rounded to fp16) or, for the exact path, into an fp32 copy;
 //  * combine: merges the partial results of the key-range partitions (split-KV) of one query
 //    row with the log-sum-exp rule  out = sum_s w_s O_s / sum_s w_s l_s,  w_s = b^(m_s - max m).
+#include "cache_rows.cuh"
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -32,13 +33,10 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const void *b
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-constexpr float kF16Max = 65504.0f;   // largest finite fp16 value
-
 template <typename T>
 __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
 {
     const size_t n4 = (size_t)p.nkv * p.ctx * p.hd / 4;
-    const int hd4 = p.hd / 4;
     bool out_of_range = false;     // a V value the fp16 operand cannot hold (or not finite)
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -50,36 +48,8 @@ __global__ void __launch_bounds__(256) cache_kv_kernel(CachePrepParams p)
             reinterpret_cast<float4 *>(p.v32)[i] = v;
             continue;
         }
-        const size_t row = i / hd4;              // g * ctx + j
-        const int c4 = (int)(i % hd4);
-        const size_t g = row / p.ctx, j = row % p.ctx;
-        const size_t dst = (g * p.S + j) * p.hd + 4 * (size_t)c4;
-        const float kx[4] = {k.x, k.y, k.z, k.w};
-        __nv_bfloat16 hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            hi[e] = __float2bfloat16_rn(kx[e]);
-            lo[e] = __float2bfloat16_rn(kx[e] - __bfloat162float(hi[e]));
-        }
-        __nv_bfloat162 h01, h23, l01, l23;
-        h01.x = hi[0]; h01.y = hi[1]; h23.x = hi[2]; h23.y = hi[3];
-        l01.x = lo[0]; l01.y = lo[1]; l23.x = lo[2]; l23.y = lo[3];
-        uint2 uh, ul;
-        uh.x = *reinterpret_cast<uint32_t *>(&h01); uh.y = *reinterpret_cast<uint32_t *>(&h23);
-        ul.x = *reinterpret_cast<uint32_t *>(&l01); ul.y = *reinterpret_cast<uint32_t *>(&l23);
-        *reinterpret_cast<uint2 *>(p.kh + dst) = uh;
-        *reinterpret_cast<uint2 *>(p.kl + dst) = ul;
-        if (p.kh2) {
-            *reinterpret_cast<uint2 *>(p.kh2 + dst) = uh;
-            *reinterpret_cast<uint2 *>(p.kl2 + dst) = ul;
-        }
-        out_of_range |= !(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) <=
-                          kF16Max);
-        __half2 v01 = __floats2half2_rn(v.x, v.y), v23 = __floats2half2_rn(v.z, v.w);
-        uint2 uv;
-        uv.x = *reinterpret_cast<uint32_t *>(&v01); uv.y = *reinterpret_cast<uint32_t *>(&v23);
-        *reinterpret_cast<uint2 *>(p.vh + dst) = uv;
-        if (p.vh2) *reinterpret_cast<uint2 *>(p.vh2 + dst) = uv;
+        out_of_range |= cache_store4(k, v, i, p.hd, p.ctx, p.S, p.kh, p.kl, p.vh);
+        if (p.kh2) cache_store4(k, v, i, p.hd, p.ctx, p.S, p.kh2, p.kl2, p.vh2);
     }
     if (__any_sync(0xffffffffu, out_of_range) && (threadIdx.x & 31) == 0 && p.status)
         atomicOr(p.status, kErrRange);

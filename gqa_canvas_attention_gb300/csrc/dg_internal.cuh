@@ -57,6 +57,11 @@ struct NormRopeParams {
     int ql_interleaved;
     __nv_bfloat16 *kh, *kl;        // [nkv, S, hd] (canvas rows ctx..ctx+T-1)
     __half *vh;                    // [nkv, S, hd] fp16 (canvas rows ctx..ctx+T-1)
+    // kOutTc with a cache passed with the call: its fp32 rows [nkv, ctx, hd] are converted into
+    // rows 0..ctx-1 of kh / kl / vh by the last cache_blocks blocks of the same launch
+    const float *kc, *vc;
+    int cache_blocks;
+    uint32_t *status;              // kErrRange is OR-ed in for a V value beyond the fp16 range
 };
 
 // Conversion of a cache [nkv, ctx, hd] into the tensor-core operand arrays (rows 0..ctx-1).
@@ -233,6 +238,9 @@ template <class F> cudaError_t once_per_device(std::atomic<unsigned long long> &
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
+
+// float4 units of K (and of V) each thread of the first stage's cache blocks converts a pass
+constexpr int kNormCacheUnroll = 4;
 
 // Host launchers (return cudaGetLastError()).
 cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);

@@ -20,6 +20,7 @@
 //
 // For the tensor-core layouts q-hat (times log2 e) and k-hat are written as bf16 hi/lo pairs and
 // v-hat as fp16, next to the cache rows of the same kv head.
+#include "cache_rows.cuh"
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -112,6 +113,45 @@ __device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c,
 // or 64 values per lane).
 template <int HD> constexpr int kChunkRows = 2 * Rows<HD>::RPI;
 
+// A cache passed with the call, converted by the last blocks of the first-stage launch: each
+// thread takes kNormCacheUnroll float4 units of K and of V a pass, every load of the pass issued
+// before the first store.  The waits are the canvas rows' (a cache is an input like q).
+constexpr int kCacheUnroll = kNormCacheUnroll;
+
+template <int HD>
+__device__ __forceinline__ void convert_cache(const float4 *kc, const float4 *vc, int nkv, int ctx,
+                                              int S, int blocks, unsigned blk, bool wait_stores,
+                                              __nv_bfloat16 *kh, __nv_bfloat16 *kl, __half *vh,
+                                              uint32_t *status)
+{
+    const size_t n4 = (size_t)nkv * ctx * HD / 4;
+    const size_t stride = (size_t)blocks * 128;
+    bool out_of_range = false;     // a V value the fp16 operand cannot hold (or not finite)
+    for (size_t i0 = (size_t)blk * 128 + threadIdx.x; i0 < n4; i0 += kCacheUnroll * stride) {
+        float4 k[kCacheUnroll], v[kCacheUnroll];
+#pragma unroll
+        for (int u = 0; u < kCacheUnroll; ++u) {
+            const size_t i = i0 + u * stride;
+            k[u] = i < n4 ? kc[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = i < n4 ? vc[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // the rows written here are read by the previous forward's attention kernel until it
+        // ends, unless the plan alternates operand sets
+        if (wait_stores) {
+            pdl_wait();
+            wait_stores = false;
+        }
+#pragma unroll
+        for (int u = 0; u < kCacheUnroll; ++u) {
+            const size_t i = i0 + u * stride;
+            if (i < n4) out_of_range |= cache_store4(k[u], v[u], i, HD, ctx, S, kh, kl, vh);
+        }
+    }
+    if (wait_stores) pdl_wait();
+    if (__any_sync(0xffffffffu, out_of_range) && (threadIdx.x & 31) == 0 && status)
+        atomicOr(status, kErrRange);
+}
+
 template <int HD, int MODE>
 __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int chunks)
 {
@@ -126,6 +166,15 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     // kernel ahead of it.
     pdl_launch_dependents();
     if (!p.inputs_resident) pdl_wait();
+    if constexpr (MODE == kOutTc) {
+        if ((int)blockIdx.x >= (int)gridDim.x - p.cache_blocks) {
+            convert_cache<HD>(reinterpret_cast<const float4 *>(p.kc),
+                              reinterpret_cast<const float4 *>(p.vc), p.nkv, p.ctx, p.S,
+                              p.cache_blocks, blockIdx.x - (gridDim.x - p.cache_blocks),
+                              p.inputs_resident && !p.other_set, p.kh, p.kl, p.vh, p.status);
+            return;
+        }
+    }
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPR, rsub = lane / LPR;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -317,7 +366,7 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
     const int chunks = (jobs + kChunkRows<HD> - 1) / kChunkRows<HD>;
     const long long warps = (long long)p.T * chunks;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4 + p.cache_blocks));
     cfg.blockDim = dim3(128);
     cfg.stream = s;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};

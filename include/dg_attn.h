@@ -79,7 +79,8 @@ typedef struct dg_attn_plan dg_attn_plan;
                                    and the forward ends with DG_ERR_TIMEOUT (no fault, no hang);
                                    no counterpart on the page */
 #define DG_OPT_INPUTS_RESIDENT 7 /* 1 = the caller guarantees that the inputs of every call (q,
-                                   k_canvas, v_canvas, weights, cos_sin) are complete before the
+                                   k_canvas, v_canvas, weights, cos_sin, and a cache passed with
+                                   the call) are complete before the
                                    work enqueued ahead of that call on the stream started, e.g.
                                    canvases already resident in device memory: the first stage then
                                    reads them while the previous call's attention kernel is still
@@ -145,7 +146,8 @@ int dg_attn_schedule_info(int nh, int nkv, int hd, int ctx, int T, int num_sms,
  * projection).  out must not overlap any input (DG_ERR_ARG; checked on the byte ranges the plan's
  * sizes give).  Every pointer must be 16-byte aligned (DG_ERR_ALIGN).  Enqueued on `stream`; on
  * the tensor-core path a cache V outside the fp16 range is reported by dg_attn_sync_status
- * (DG_ERR_RANGE). */
+ * (DG_ERR_RANGE), and a cache passed with the call is converted by the first-stage launch
+ * itself (it replaces the prepared cache copy: DG_INFO_CACHE_READY becomes 0). */
 int dg_attn_forward(dg_attn_plan *plan, const float *q, const float *k_canvas,
                     const float *v_canvas, const float *k_cache, const float *v_cache,
                     const float *q_norm_w, const float *k_norm_w, const float *cos_sin, float *out,
@@ -207,7 +209,9 @@ int dg_attn_sync_status(dg_attn_plan *plan, cudaStream_t stream);
 #define DG_STAGE_NORM_ROPE 0  /* the norm + RoPE kernel */
 #define DG_STAGE_ATTENTION 1  /* the attention kernel (tensor-core or fp32) */
 #define DG_STAGE_COMBINE   2  /* the split-KV combine kernel */
-#define DG_STAGE_CACHE     3  /* the cache conversion kernel */
+#define DG_STAGE_CACHE     3  /* the cache conversion kernel (dg_attn_cache_prepare, and a cache
+                                 passed to dg_attn_forward_hidden; dg_attn_forward and
+                                 dg_attn_attend convert one inside the norm + RoPE launch) */
 #define DG_STAGE_PROJECTION 4 /* the input norm + q/k/v projection kernels (dg_attn_forward_hidden) */
 #define DG_STAGE_OPROJ      5 /* the o_proj, post-attention norm and residual kernels */
 

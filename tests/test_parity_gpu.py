@@ -340,17 +340,30 @@ def test_attend_on_oracle_normed_inputs(path):
     check(out, ref, path, [(0, T)], "attend")
 
 
-def test_per_call_cache_and_prepared_cache_agree():
-    T, ctx, nh, nkv, hd = 32, 500, 4, 2, 128
+@pytest.mark.parametrize("shape", [
+    (32, 500, 4, 2, 128),
+    (40, 333, 4, 2, 64),       # 10656 float4 units of K: a ragged last pass of its blocks
+    (64, 4100, 16, 8, 256),    # 2.1 M float4 units: more than one pass of the capped block count
+], ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d" % s)
+@pytest.mark.parametrize("resident", [0, 1])
+def test_per_call_cache_and_prepared_cache_agree(shape, resident):
+    """A cache passed with the call is converted by the first-stage launch itself; the prepared
+    cache by its own kernel.  Both give the same operand bits, so the same outputs, and those
+    match the oracle."""
+    T, ctx, nh, nkv, hd = shape
     d = make_inputs(T, ctx, nh, nkv, hd, seed=15)
     dd = to_dev(d)
     plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan.set(B.DG_OPT_INPUTS_RESIDENT, resident)
     a = run_forward(plan, dd).clone()
+    assert plan.get(B.DG_INFO_CACHE_READY) == 0
     plan.cache_prepare(dd["k_cache"], dd["v_cache"])
     b = plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
                      dd["k_norm_w"])
+    c = run_forward(plan, dd).clone()          # per call again, after a prepared one
     assert plan.sync_status() == B.DG_OK
-    assert torch.equal(a, b)
+    assert torch.equal(a, b) and torch.equal(a, c)
+    check(a, oracle_out(d, nh, nkv, hd), B.DG_PATH_TC, all_rows(T), "per-call cache")
 
 
 def test_errors_are_reported_not_raised_on_device():
