@@ -506,8 +506,10 @@ int unswap_unless_launched(dg_attn_plan *p, int rc, int other, unsigned long lon
 }
 
 // Attention + (when partitioned) combine, reading the operands the first stage left in scratch.
+// `fresh_cache`: the cache rows were converted by this call's first-stage launch, so the
+// tensor-core kernel may not load them before its wait for that launch.
 int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cache, float *out,
-                      cudaStream_t s)
+                      cudaStream_t s, bool fresh_cache = false)
 {
     int splits, tps, nt;
     split_layout(p, splits, tps, nt);
@@ -535,6 +537,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
         a.cluster_combine = !stream_k && cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
+        a.static_keys = fresh_cache ? 0 : p->ctx;
         if (stream_k) {
             a.sk_ctas = sk.ctas;
             a.sk_units = sk.units;
@@ -1039,7 +1042,7 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
         cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
         if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
         if ((rc = record_event(p, DG_STAGE_NORM_ROPE, s))) return rc;
-        return enqueue_attention(p, k_cache, v_cache, out, s);
+        return enqueue_attention(p, k_cache, v_cache, out, s, fused);
     };
     return unswap_unless_launched(p, run(), other, launched);
 }
@@ -1102,7 +1105,7 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
         cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
         if (err != cudaSuccess) return cuda_fail(err, "operand layout launch");
-        return enqueue_attention(p, k_cache, v_cache, out, s);
+        return enqueue_attention(p, k_cache, v_cache, out, s, fused);
     };
     return unswap_unless_launched(p, run(), other, launched);
 }

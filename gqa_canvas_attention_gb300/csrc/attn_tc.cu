@@ -267,13 +267,27 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    // the operands are written by the kernel before this one in the stream
-    pdl_wait();
-    // Only now may the next kernel of the stream be scheduled.  With resident inputs the plan
-    // alternates two operand sets, and the next forward's first stage writes the set this kernel
-    // does not read without waiting for anything; its start after this point is what guarantees
-    // that the attention kernel before this one, the last reader of that set, has finished.
-    pdl_launch_dependents();
+    // The operands are written by the kernel before this one in the stream: every thread waits
+    // for it before its role touches them, except that the producers first load the ring stages
+    // of cache rows that were complete before that kernel started (keys < p.static_keys).
+    // Only after its wait may a thread let the next kernel of the stream be scheduled.  With
+    // resident inputs the plan alternates two operand sets, and the next forward's first stage
+    // writes the set this kernel does not read without waiting for anything; its start after
+    // this point is what guarantees that the attention kernel before this one, the last reader
+    // of that set, has finished.
+    auto wait_previous = [&]() {
+        pdl_wait();
+        pdl_launch_dependents();
+    };
+    // ring stages of this CTA's first tiles whose keys are all such cache rows
+    auto static_prefix = [&](int stages, int keys_per_stage) -> int {
+        int n = 0;
+        const int per_tile = NK / keys_per_stage;
+        while (n < stages && n < n_all * per_tile &&
+               key_tile(n / per_tile) * NK + (n % per_tile + 1) * keys_per_stage <= p.static_keys)
+            ++n;
+        return n;
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------------------- K producer
@@ -282,6 +296,22 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             bool ok = true;
             int issued[KST] = {};
             int cur = -1, q_loads = 0;
+            auto load_k = [&](int it) {
+                const int s = it % KST;
+                uint8_t *kst = smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES;
+                const int key0 = key_tile(it) * NK, g = pg[piece_of(it)];
+                mbar_arrive_expect_tx(&k_full[s], Lay::KSTAGE_BYTES);
+                for (int pn = 0; pn < Lay::KPANELS; ++pn) {
+                    tma_load_3d_hint(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64,
+                                     key0, g, pol);
+                    tma_load_3d_hint(kst + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES, &maps.kl,
+                                     &k_full[s], pn * 64, key0, g, pol);
+                }
+                ++issued[s];
+            };
+            const int pre = static_prefix(KST, NK);
+            for (int it = 0; it < pre; ++it) load_k(it);
+            wait_previous();
             for (int it = 0; it < n_all; ++it) {
                 const int sg = piece_of(it), g = pg[sg];
                 if (sg != cur) {
@@ -298,27 +328,21 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         ++q_loads;
                     }
                 }
+                if (it < pre) continue;             // loaded before the wait
                 const int s = it % KST;
                 if (it >= KST && !mbar_wait_bounded(&k_empty[s], ((it / KST) - 1) & 1, limit)) {
                     ok = false;
                     break;
                 }
-                uint8_t *kst = smem + Lay::K_OFF + s * Lay::KSTAGE_BYTES;
-                const int key0 = key_tile(it) * NK;
-                mbar_arrive_expect_tx(&k_full[s], Lay::KSTAGE_BYTES);
-                for (int pn = 0; pn < Lay::KPANELS; ++pn) {
-                    tma_load_3d_hint(kst + pn * Lay::KPANEL_BYTES, &maps.kh, &k_full[s], pn * 64,
-                                     key0, g, pol);
-                    tma_load_3d_hint(kst + (Lay::KPANELS + pn) * Lay::KPANEL_BYTES, &maps.kl,
-                                     &k_full[s], pn * 64, key0, g, pol);
-                }
-                ++issued[s];
+                load_k(it);
             }
             if (!ok) atomicOr(p.status, kErrWaitProducer);
             // let every load issued by this thread land before the CTA can exit
             for (int s = 0; s < KST; ++s)
                 if (issued[s] > 0) mbar_wait_bounded(&k_full[s], (issued[s] - 1) & 1, limit);
             if (q_loads > 0) mbar_wait_bounded(q_full, (q_loads - 1) & 1, limit);
+        } else {
+            wait_previous();
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -329,12 +353,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
             int issued[VST] = {};
             // VK-key stages, NK/VK of them per score tile
             constexpr int VPT = NK / C::VK;
-            for (int it = 0; it < n_all * VPT; ++it) {
+            auto load_v = [&](int it) {
                 const int s = it % VST;
-                if (it >= VST && !mbar_wait_bounded(&v_empty[s], ((it / VST) - 1) & 1, limit)) {
-                    ok = false;
-                    break;
-                }
                 uint8_t *vst = smem + Lay::V_OFF + s * Lay::VSTAGE_BYTES;
                 const int tile = it / VPT;
                 const int key0 = key_tile(tile) * NK + (it % VPT) * C::VK;
@@ -344,10 +364,23 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     tma_load_3d_hint(vst + pn * Lay::VPANEL_BYTES, &maps.vh, &v_full[s], pn * 64,
                                      key0, g, pol);
                 ++issued[s];
+            };
+            const int pre = static_prefix(VST, C::VK);
+            for (int it = 0; it < pre; ++it) load_v(it);
+            wait_previous();
+            for (int it = pre; it < n_all * VPT; ++it) {
+                const int s = it % VST;
+                if (it >= VST && !mbar_wait_bounded(&v_empty[s], ((it / VST) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                load_v(it);
             }
             if (!ok) atomicOr(p.status, kErrWaitProducer);
             for (int s = 0; s < VST; ++s)
                 if (issued[s] > 0) mbar_wait_bounded(&v_full[s], (issued[s] - 1) & 1, limit);
+        } else {
+            wait_previous();
         }
         __syncwarp();
     } else if (warp == 1 || warp == 3 || warp >= 8) {
@@ -355,6 +388,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         // The whole warp runs the issue loop, so tile indices and descriptors are warp-uniform
         // values; the lane chosen by elect.sync issues every tcgen05 instruction (the same lane
         // each time, so its commits track all of its MMAs).
+        wait_previous();
         const uint32_t leader = elect_one_sync();
         constexpr uint32_t idesc_qk = make_idesc(1, 0, 0, kTileM, NK);
         constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, kTileM, HD);   // fp16, B MN-major
@@ -465,6 +499,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
         // ---------------------------------------------------------------- softmax / epilogue
+        wait_previous();
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                  // tile row == TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;

@@ -104,6 +104,9 @@ struct AttnTcParams {
     int cluster_combine;           // 1: the splits CTAs of a query tile form a cluster and merge
                                    // their partial results through distributed shared memory
     int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
+    int static_keys;               // keys [0, static_keys) of every kv group (cache rows) were
+                                   // complete before the kernel ahead of this one started: the
+                                   // producers may load them before waiting for that kernel
     // stream-K schedule (sk_ctas > 0): CTA c takes key-tile units [sk_begin(c), sk_begin(c + 1))
     // of the qtiles * nkv pairs in order p = g * qtiles + qt, n_tiles units each; its pieces go
     // to part_o / part_ml at slot = its rank among the CTAs of that pair
