@@ -46,6 +46,21 @@ struct Rows {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
+    // A row read exactly once (the canvas inputs): no L1 allocation, and an L2 policy that
+    // evicts these lines first, so the stream does not push the attention kernel's cache tiles
+    // out of L2.
+    __device__ static __forceinline__ void load_once(const float *row, int l, uint64_t pol,
+                                                     float (&x)[8])
+    {
+        const float4 *a = reinterpret_cast<const float4 *>(row) + l;
+        const float4 *b = reinterpret_cast<const float4 *>(row + HALF) + l;
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3])
+                     : "l"(a), "l"(pol));
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7])
+                     : "l"(b), "l"(pol));
+    }
     __device__ static __forceinline__ void store(float *row, int l, const float (&x)[8])
     {
         reinterpret_cast<float4 *>(row)[l] = make_float4(x[0], x[1], x[2], x[3]);
@@ -193,11 +208,13 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
     // every row of the chunk is requested before any arithmetic; lanes past the chunk's last row
     // hold zeros (they join the shuffles, store nothing)
     float x[RG][8];
+    uint64_t stream_pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
 #pragma unroll
     for (int g = 0; g < RG; ++g) {
         const int r = g * RPI + rsub;
         if (r < nj) {
-            R::load(src_row(j0 + r), sub, x[g]);
+            R::load_once(src_row(j0 + r), sub, stream_pol, x[g]);
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[g][e] = 0.f;
