@@ -166,6 +166,17 @@ def test_denoise_loop_in_the_bench_launch_configuration():
     graph.replay()
     torch.cuda.synchronize()
     assert plan.sync_status() == B.DG_OK
+    # With resident inputs each forward's first stage writes the operand set the previous
+    # forward's attention kernel is not reading, ordered by programmatic dependent launch alone.
+    # The same canvases run eagerly without the option, one kernel after the other, must give
+    # the same bits for every step.
+    ref = B.Plan(w.nh, w.nkv, w.hd, w.ctx, w.T, EPS, ROPE_THETA)
+    ref.cache_prepare(kc, vc)
+    for s, (dd, o) in enumerate(zip(dev, outs)):
+        r = ref.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], None, None, dd["q_norm_w"],
+                        dd["k_norm_w"])
+        assert torch.equal(o, r), f"step {s}: resident graph replay differs from eager"
+    assert ref.sync_status() == B.DG_OK
     for s, (d, o) in enumerate(zip(steps, outs)):
         d["k_cache"], d["v_cache"] = d0["k_cache"], d0["v_cache"]
         rows = (0, w.T) if s in (0, 1, w.steps - 1) else (8 * (s % 60), 8 * (s % 60) + 8)
@@ -456,17 +467,22 @@ def test_forward_replays_from_a_cuda_graph(path):
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], "graph")
 
 
-def test_resident_inputs_give_the_same_bits():
-    """With DG_OPT_INPUTS_RESIDENT the first stage of each forward loads and computes while the
-    previous forward's attention kernel runs; the results must be bit-identical."""
-    T, ctx, nh, nkv, hd = 130, 1500, 8, 4, 256
+@pytest.mark.parametrize("shape", [(130, 1500, 8, 4, 256), (200, 700, 16, 8, 128),
+                                   (512, 0, 16, 16, 64)],
+                         ids=lambda s: "T%d_ctx%d_nh%d_nkv%d_hd%d" % s)
+def test_resident_inputs_give_the_same_bits(shape):
+    """With DG_OPT_INPUTS_RESIDENT the first stage of each forward runs while the previous
+    forward's attention kernel does, writing the other operand set; the results must be
+    bit-identical to forwards that wait for each other."""
+    T, ctx, nh, nkv, hd = shape
     plans, outs = [], []
     canvases = [to_dev(make_inputs(T, ctx, nh, nkv, hd, seed=50 + i)) for i in range(4)]
     for resident in (0, 1):
         plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
         plan.set(B.DG_OPT_INPUTS_RESIDENT, resident)
         assert plan.get(B.DG_OPT_INPUTS_RESIDENT) == resident
-        plan.cache_prepare(canvases[0]["k_cache"], canvases[0]["v_cache"])
+        if ctx:
+            plan.cache_prepare(canvases[0]["k_cache"], canvases[0]["v_cache"])
         res = [torch.empty((T, nh * hd), device="cuda") for _ in canvases]
         for c, o in zip(canvases, res):
             plan.forward(c["q"], c["k_canvas"], c["v_canvas"], None, None, c["q_norm_w"],
