@@ -3,7 +3,7 @@
 // enqueueing of the kernels of one forward on the caller's stream.
 //
 // The plan's scratch, all device-resident and allocated once at creation:
-//   inv_freq  [hd/2] float2        theta^(-2i/hd) as a double-float (hi, lo), made on the host in fp64
+//   inv_freq  [hd/2] float4        theta^(-2i/hd) in fp64, held exactly as the sum of three floats
 //   fp32 path: q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd]
 //   tensor-core path: Q hi/lo bf16 [nkv, rows_pad, hd] (row R = t*G + h mod G, padded to 128),
 //             K hi/lo bf16 [nkv, S, hd] (S = ctx + T) with the cache in rows 0..ctx-1 and the
@@ -137,7 +137,7 @@ struct dg_attn_plan {
     // clusters of s CTAs (s = 2..8) the tensor-core kernel can hold at once (0: not launchable)
     int max_clusters[dg::kMaxClusterSplits + 1];
     // scratch
-    float2 *inv_freq;
+    float4 *inv_freq;
     float *rope_cs;              // [T, 2*hd] cos|sin of the positions pos0 .. pos0 + T - 1
     bool rope_dirty;             // rope_cs does not hold the current pos0 yet
     uint32_t *status;
@@ -709,7 +709,7 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     p->num_sms = prop.multiProcessorCount;
 
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
-    p->inv_freq = (float2 *)dalloc(p, sizeof(float2) * (hd / 2), err);
+    p->inv_freq = (float4 *)dalloc(p, sizeof(float4) * (hd / 2), err);
     p->rope_cs = (float *)dalloc(p, sizeof(float) * 2 * (size_t)T * hd, err);
     p->rope_dirty = true;
     p->status = (uint32_t *)dalloc(p, sizeof(uint32_t) * 4, err);
@@ -722,13 +722,16 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
         delete p;
         return nullptr;
     }
-    std::vector<float2> f(hd / 2);
+    // each fp64 frequency as three floats whose sum is exactly it (24 + 24 + the last 5 bits)
+    std::vector<float4> f(hd / 2);
     for (int i = 0; i < hd / 2; ++i) {
         const double v = std::pow((double)rope_theta, -2.0 * i / (double)hd);
-        const float hi = (float)v;
-        f[i] = make_float2(hi, (float)(v - (double)hi));
+        const float a = (float)v;
+        const float b = (float)(v - (double)a);
+        const float c = (float)(v - (double)a - (double)b);
+        f[i] = make_float4(a, b, c, 0.f);
     }
-    err = cudaMemcpy(p->inv_freq, f.data(), sizeof(float2) * f.size(), cudaMemcpyHostToDevice);
+    err = cudaMemcpy(p->inv_freq, f.data(), sizeof(float4) * f.size(), cudaMemcpyHostToDevice);
     if (err == cudaSuccess && p->tc_ok) err = dg::attn_tc_prepare(hd);
     for (int sp = 0; sp <= dg::kMaxClusterSplits; ++sp)
         p->max_clusters[sp] = (err == cudaSuccess && p->tc_ok)

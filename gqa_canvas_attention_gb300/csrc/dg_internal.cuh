@@ -38,7 +38,7 @@ struct NormRopeParams {
     const float *q, *k, *v;        // [T, nh*hd], [T, nkv*hd], [T, nkv*hd]
     const float *wq, *wk;          // [hd] or null
     const float *cos_sin;          // [T, 2*hd] or null (then computed per lane from inv_freq)
-    const float2 *inv_freq;        // [hd/2] (hi, lo) double-float of theta^(-2i/hd)
+    const float4 *inv_freq;        // [hd/2] theta^(-2i/hd) in fp64, exactly x + y + z (w unused)
     int T, nh, nkv, ctx, S, S_pad, rows_pad;
     long long pos0;
     float eps;
@@ -248,7 +248,7 @@ constexpr int kNormCacheUnroll = 4;
 // Host launchers (return cudaGetLastError()).
 cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);
 // cos|sin table [T, 2*hd] of the positions pos0 .. pos0 + T - 1 (layout of a caller's table).
-cudaError_t launch_rope_table(float *cs, const float2 *inv_freq, int T, int hd, long long pos0,
+cudaError_t launch_rope_table(float *cs, const float4 *inv_freq, int T, int hd, long long pos0,
                               cudaStream_t s);
 cudaError_t launch_cache_prep(const CachePrepParams &p, cudaStream_t s);
 cudaError_t launch_attn_fp32(const AttnFp32Params &p, int hd, cudaStream_t s);

@@ -32,14 +32,15 @@ std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 thread_local char g_err[256] = "";
 
-// theta^(-2i/hd) in fp64, split into a (hi, lo) pair of floats, one thread per frequency.
-__global__ void noalloc_inv_freq_kernel(float2 *out, int half, int hd, double theta)
+// theta^(-2i/hd) in fp64, held exactly as the sum of three floats, one thread per frequency.
+__global__ void noalloc_inv_freq_kernel(float4 *out, int half, int hd, double theta)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= half) return;
     const double v = pow(theta, -2.0 * i / (double)hd);
-    const float hi = (float)v;
-    out[i] = make_float2(hi, (float)(v - (double)hi));
+    const float a = (float)v;
+    const float b = (float)(v - (double)a);
+    out[i] = make_float4(a, b, (float)(v - (double)a - (double)b), 0.f);
 }
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -81,16 +82,16 @@ extern "C" int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, 
             snprintf(g_err, sizeof(g_err), "pointers must be 16-byte aligned");
             return DG_ERR_ALIGN;
         }
-    // the scratch regions, each rounded up to 256 bytes: the RoPE frequencies (hd/2 float2),
+    // the scratch regions, each rounded up to 256 bytes: the RoPE frequencies (hd/2 float4),
     // q-hat [T, nh, hd], k-hat and v-hat [T, nkv, hd] (fp32)
-    const size_t freq_b = align256(sizeof(float2) * (size_t)(hd / 2));
+    const size_t freq_b = align256(sizeof(float4) * (size_t)(hd / 2));
     const size_t q_b = align256(sizeof(float) * (size_t)T * nh * hd);
     const size_t kv_b = align256(sizeof(float) * (size_t)T * nkv * hd);
     const size_t need = freq_b + q_b + 2 * kv_b;
     if (need > kDgNoallocScratchBytes) {
         snprintf(g_err, sizeof(g_err),
                  "needs %zu bytes of scratch for T=%d nh=%d nkv=%d hd=%d; the fixed array holds "
-                 "%zu (the sum of hd*4, T*nh*hd*4 and twice T*nkv*hd*4, each rounded up to 256)",
+                 "%zu (the sum of hd*8, T*nh*hd*4 and twice T*nkv*hd*4, each rounded up to 256)",
                  need, T, nh, nkv, hd, kDgNoallocScratchBytes);
         return DG_ERR_ARG;
     }
@@ -114,7 +115,7 @@ extern "C" int dg_attn_forward_noalloc(int nh, int nkv, int hd, int ctx, int T, 
         }
         base = static_cast<unsigned char *>(g_scratch_addr[dev]);
     }
-    float2 *inv_freq = reinterpret_cast<float2 *>(base);
+    float4 *inv_freq = reinterpret_cast<float4 *>(base);
     float *qh = reinterpret_cast<float *>(base + freq_b);
     float *kh = reinterpret_cast<float *>(base + freq_b + q_b);
     float *vh = reinterpret_cast<float *>(base + freq_b + q_b + kv_b);

@@ -7,12 +7,14 @@
 // every row of its chunk, its norm weights and its cos/sin row before any arithmetic, then
 // normalises, rotates and stores the rows, 256/hd rows per instruction.  The cos/sin rows come from a table (the
 // caller's, or the plan's, built once per set of positions by rope_table_kernel); without one each
-// lane computes those of its own elements.  Either way the angle
-// (pos0 + t) * theta^(-2i/hd) is formed in double-float (the frequency arrives as an fp64 value
-// split into two floats, the product is made exact with an FMA), reduced modulo 2*pi with a
-// Cody-Waite split of 2*pi (Cody & Waite, "Software Manual for the Elementary Functions", 1980)
-// and the leftover low part folded in with the second-order angle-addition formula around
-// CUDA's sincosf.  fp32 angles would be off by up to ~1e-3 rad at positions near 8192.
+// lane computes those of its own elements.  Either way the angle (pos0 + t) * theta^(-2i/hd) is
+// reduced modulo 2*pi without rounding anything that matters: the fp64 frequency arrives exactly
+// as three floats, the position is an integer below 2^24 (exact in fp32), the large products are
+// split exactly with FMAs, 2*pi is a three-float split (Cody & Waite, "Software Manual for the
+// Elementary Functions", 1980, with Dekker's exact products), and the pieces are summed with
+// Knuth's TwoSum into r_hi + r_lo, |r_lo| <= half an ulp of r_hi.  CUDA's sincosf of r_hi, moved
+// to first order in r_lo, then gives cos and sin of the fp64 angle to fp32 accuracy at every
+// position.  (fp32 angles would be off by up to ~1e-3 rad at positions near 8192.)
 //
 // A row is held by hd/8 lanes, 8 elements each (elements 4l..4l+3 and hd/2+4l..hd/2+4l+3 of
 // sub-lane l), so a warp instruction covers 256/hd rows; the RMS is a shuffle reduction over the
@@ -102,25 +104,49 @@ __device__ __forceinline__ void store_q_interleaved(__nv_bfloat16 *tile, int r, 
     }
 }
 
-// cos and sin of p * f with f = f_hi + f_lo (see the file comment for the method).
-__device__ __forceinline__ void rope_angle_cos_sin(float pf, float2 f, float &c, float &s)
+// a + b = s + e exactly (Knuth's TwoSum; no multiplication, so nothing for the compiler to fuse)
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
 {
-    const float kTwoPiHi = 6.28318548202514648f;     // 2*pi rounded to fp32
-    const float kTwoPiLo = -1.7484555314695172e-07f; // 2*pi - kTwoPiHi
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// cos and sin of p * f for an integer position p < 2^24 and the fp64 frequency f held exactly as
+// f.x + f.y + f.z (see the file comment for the method).
+__device__ __forceinline__ void rope_angle_cos_sin(float pf, float4 f, float &c, float &s)
+{
+    // 2*pi = kC1 + kC2 + kC3 to 72 bits (the rest is below 5e-23)
+    const float kC1 = 0x1.921fb6p+2f, kC2 = -0x1.777a5cp-23f, kC3 = -0x1.ee59dap-48f;
     const float kInvTwoPi = 0.15915494309189535f;
-    const float a_hi = pf * f.x;
-    const float a_err = fmaf(pf, f.x, -a_hi);        // p*f_hi = a_hi + a_err exactly
-    const float a_lo = fmaf(pf, f.y, a_err);
-    const float kq = rintf(a_hi * kInvTwoPi);
-    const float P = kq * kTwoPiHi;
-    const float Pe = fmaf(kq, kTwoPiHi, -P);         // kq*2pi_hi = P + Pe exactly
-    const float d = a_hi - P;                         // exact (Sterbenz)
-    const float e = (a_lo - Pe) - kq * kTwoPiLo;      // small remainder of the angle
+    // the angle: p*f.x = A1 + e1 and p*f.y = A2 + e2 exactly, p*f.z below 2^-23 * p*f.x
+    const float A1 = __fmul_rn(pf, f.x), e1 = fmaf(pf, f.x, -A1);
+    const float A2 = __fmul_rn(pf, f.y), e2 = fmaf(pf, f.y, -A2);
+    const float A3 = __fmul_rn(pf, f.z);
+    // kq turns of 2*pi: kq*kC1 = P1 + E1 and kq*kC2 = P2 + E2 exactly
+    const float kq = rintf(A1 * kInvTwoPi);
+    const float P1 = __fmul_rn(kq, kC1), E1 = fmaf(kq, kC1, -P1);
+    const float P2 = __fmul_rn(kq, kC2), E2 = fmaf(kq, kC2, -P2);
+    const float P3 = __fmul_rn(kq, kC3);
+    // the reduced angle (A1 - P1) + e1 - E1 + A2 - P2 + (e2 - E2 + A3 - P3): A1 - P1 is exact
+    // (Sterbenz), the next four terms are summed without loss, the last ones are tiny
+    float r = __fsub_rn(A1, P1), lo = 0.f, t;
+    two_sum(r, e1, r, t);
+    lo = __fadd_rn(lo, t);
+    two_sum(r, -E1, r, t);
+    lo = __fadd_rn(lo, t);
+    two_sum(r, A2, r, t);
+    lo = __fadd_rn(lo, t);
+    two_sum(r, -P2, r, t);
+    lo = __fadd_rn(lo, t);
+    lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(e2, E2), __fsub_rn(A3, P3)));
+    // r_hi + r_lo with |r_lo| <= half an ulp of r_hi; cos(r_hi + r_lo) to first order in r_lo
+    const float r_hi = __fadd_rn(r, lo);
+    const float r_lo = __fsub_rn(lo, __fsub_rn(r_hi, r));
     float sd, cd;
-    sincosf(d, &sd, &cd);
-    const float h = 0.5f * e * e;
-    c = cd - sd * e - cd * h;
-    s = sd + cd * e - sd * h;
+    sincosf(r_hi, &sd, &cd);
+    c = fmaf(-sd, r_lo, cd);
+    s = fmaf(cd, r_lo, sd);
 }
 
 // Rows (heads) of one token that one warp takes: 16 values per lane in registers, two rows per
@@ -361,7 +387,7 @@ __global__ void __launch_bounds__(128) norm_rope_kernel(NormRopeParams p, int ch
 
 // The cos|sin table of the canvas positions pos0 .. pos0 + T - 1: row t = cos(hd) | sin(hd), both
 // halves of each equal, one thread per (t, frequency).
-__global__ void rope_table_kernel(float *cs, const float2 *inv_freq, int T, int hd, long long pos0)
+__global__ void rope_table_kernel(float *cs, const float4 *inv_freq, int T, int hd, long long pos0)
 {
     const int half = hd / 2;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -399,7 +425,7 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
 
 }  // namespace
 
-cudaError_t launch_rope_table(float *cs, const float2 *inv_freq, int T, int hd, long long pos0,
+cudaError_t launch_rope_table(float *cs, const float4 *inv_freq, int T, int hd, long long pos0,
                               cudaStream_t s)
 {
     const long long n = (long long)T * (hd / 2);

@@ -276,7 +276,7 @@ int dg_attn_forward_layer(dg_attn_plan *plan, float *resid, const float *k_cache
  * as dg_attn_forward on the exact-fp32 path with one key-range partition, without a plan: its
  * working memory is a fixed 16 MiB __device__ array inside the library (held on every GPU that
  * loads the library until the process exits), so it allocates nothing.  Sizes must satisfy
- * a(hd*4) + a(T*nh*hd*4) + 2*a(T*nkv*hd*4) <= 16 MiB, where a(x) rounds x up to a multiple of
+ * a(hd*8) + a(T*nh*hd*4) + 2*a(T*nkv*hd*4) <= 16 MiB, where a(x) rounds x up to a multiple of
  * 256 (checked on the host: DG_ERR_ARG otherwise); every pointer must be 16-byte aligned (checked
  * on the host: DG_ERR_ALIGN); other requirements as for dg_attn_plan_create / dg_attn_forward;
  * pos0 < 0 means pos0 = ctx.  The first call on a

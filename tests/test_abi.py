@@ -68,20 +68,20 @@ def test_noalloc_entry_point_checks_sizes_on_the_host(lib):
 def test_noalloc_entry_point_checks_alignment_and_its_bound_on_the_host(lib):
     """A misaligned pointer is DG_ERR_ALIGN and one canvas row beyond the fixed scratch is
     DG_ERR_ARG, both before any CUDA call (the pointers here are never dereferenced).  The bound
-    is the sum of four regions rounded up to 256 bytes: for nh = nkv = 1, hd = 64, ctx = 0 that is
-    256 + 3 * T * 256 <= 16 MiB, so T = 21845 fits exactly (run on the GPU) and T = 21846 does
-    not."""
-    args = (1, 1, 64, 0)
+    is the sum of four regions rounded up to 256 bytes: for nh = nkv = 1, hd = 128, ctx = 0 that
+    is 64 * 16 + 3 * T * 512 <= 16 MiB (the frequencies as four floats each), so T = 10922 fits
+    exactly (run on the GPU) and T = 10923 does not."""
+    args = (1, 1, 128, 0)
     ok = 1 << 20                                  # a 16-byte-aligned stand-in address
     assert B.dg_attn_forward_noalloc(*args, 8, 1e-6, 1e4, -1, ok + 4, ok, ok, None, None, None,
                                      None, None, ok, stream=0) == B.DG_ERR_ALIGN
     assert B.dg_attn_forward_noalloc(*args, 8, 1e-6, 1e4, -1, ok, ok, ok, None, None, None,
                                      None, ok + 8, ok, stream=0) == B.DG_ERR_ALIGN
     assert "aligned" in lib.dg_attn_noalloc_last_error().decode()
-    assert B.dg_attn_forward_noalloc(*args, 21846, 1e-6, 1e4, -1, ok, ok, ok, None, None, None,
+    assert B.dg_attn_forward_noalloc(*args, 10923, 1e-6, 1e4, -1, ok, ok, ok, None, None, None,
                                      None, None, ok, stream=0) == B.DG_ERR_ARG
     assert "scratch" in lib.dg_attn_noalloc_last_error().decode()
-    assert 256 + 3 * 21845 * 256 == 16 << 20
+    assert 64 * 16 + 3 * 10922 * 512 == 16 << 20
 
 
 def test_null_plan_is_an_argument_error_for_every_entry_point(lib):

@@ -212,6 +212,36 @@ def test_shapes(shape, path):
     check(out, oracle_out(d, nh, nkv, hd), path, [(0, T)], str(shape))
 
 
+# Near the limits the plan accepts, compared on sampled rows (the oracle computes those rows
+# only): positions up to the largest the plan takes (pos0 + T < 2^24, so the last canvas row at
+# 2^24 - 2), a 256 Ki-key cache, and
+# 65536 packed query rows per kv group (G = 16, 512 query tiles each).
+LARGE_CASES = [
+    # T, ctx, nh, nkv, hd, pos0 (None: ctx), sampled row ranges
+    (4, 262144, 2, 1, 64, (1 << 24) - 5, [(0, 4)]),
+    (4096, 0, 32, 2, 64, None, [(0, 8), (2041, 2047), (4088, 4096)]),
+    (1024, 2048, 16, 1, 256, (1 << 24) - 1025, [(0, 4), (511, 515), (1020, 1024)]),
+]
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=lambda c: "T%d_ctx%d_nh%d_nkv%d_hd%d" % c[:5])
+def test_sizes_near_the_limits(case):
+    T, ctx, nh, nkv, hd, pos0, ranges = case
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=400 + hd, weighted=True)
+    dd = to_dev(d)
+    ref = np.zeros((T, nh * hd))
+    for a, b in ranges:
+        ref[a:b] = oracle_out(d, nh, nkv, hd, rows=(a, b), pos0=pos0)[a:b]
+    for path in PATHS:
+        plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+        plan.set(B.DG_OPT_PATH, path)
+        if pos0 is not None:
+            plan.set(B.DG_OPT_POS0, pos0)
+        out = run_forward(plan, dd)
+        check(out, ref, path, ranges, "large %s" % (case[:5],))
+        plan.close()
+
+
 # (requested partitions, cache length, partitions the tensor-core path uses): with hd = 128 a key
 # tile is 64 keys, so ctx = 700 / 2000 / 2250 (+ T = 40) give 12 / 32 / 36 tiles.  2..8
 # partitions merge inside the kernel (thread-block clusters); 9 and 12 use the combine kernel.

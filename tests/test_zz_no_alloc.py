@@ -99,9 +99,9 @@ def test_noalloc_matches_planned_forward_and_oracle_twice_in_a_row(case):
 
 
 def test_noalloc_accepts_the_largest_size_its_scratch_holds():
-    """T = 21845, nh = nkv = 1, hd = 64, ctx = 0 needs 256 + 3 * 21845 * 256 bytes = 16 MiB
+    """T = 10922, nh = nkv = 1, hd = 128, ctx = 0 needs 64 * 16 + 3 * 10922 * 512 bytes = 16 MiB
     exactly (one more canvas row is refused, checked on the CPU)."""
-    T, ctx, nh, nkv, hd = 21845, 0, 1, 1, 64
+    T, ctx, nh, nkv, hd = 10922, 0, 1, 1, 128
     h = make_inputs(T, ctx, nh, nkv, hd, seed=23, weighted=False)
     d = {k: (v.cuda() if v is not None else None) for k, v in h.items()}
     out = noalloc(d, nh, nkv, hd, ctx, T, None, -1)
