@@ -677,6 +677,11 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
         set_error("positions must stay below 2^24");
         return nullptr;
     }
+    if ((long long)nkv * ctx >= (1ll << 32)) {
+        // the cache conversion numbers its rows (kv head, cache row) in 32 bits
+        set_error("nkv * ctx must stay below 2^32");
+        return nullptr;
+    }
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     cudaDeviceProp prop;

@@ -118,7 +118,8 @@ typedef struct dg_attn_plan dg_attn_plan;
  * DgGpu::new checks -- n_kv, head_dim, nh % n_kv -- and the scratch buffers canvas_forward sizes
  * for the normed q/k/v; the page's head_dim <= 128 limit is lifted).  Requires nh % nkv == 0,
  * nh, nkv, T >= 1, ctx >= 0, hd in {32, 64, 128, 256} (the tensor-core path needs hd in
- * {64, 128, 256}), eps >= 0, rope_theta > 0, ctx + T < 2^24.  Returns NULL on error (see
+ * {64, 128, 256}), eps >= 0, rope_theta > 0, ctx + T < 2^24, nkv * ctx < 2^32.  Returns NULL
+ * on error (see
  * dg_attn_last_error()).  Allocates the plan's device scratch with cudaMalloc; the plan is tied
  * to the device that was current at creation. */
 dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float eps,

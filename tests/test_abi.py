@@ -42,6 +42,12 @@ def test_bad_geometry_is_rejected_before_any_device_call(lib):
         h = lib.dg_attn_plan_create(*args, 1e-6, 10000.0)
         assert not h
         assert B.last_error()
+    # positions: ctx + T < 2^24
+    assert not lib.dg_attn_plan_create(2, 1, 64, (1 << 24) - 8, 8, 1e-6, 10000.0)
+    assert "2^24" in B.last_error()
+    # cache rows (kv head, row) are numbered in 32 bits: nkv * ctx < 2^32
+    assert not lib.dg_attn_plan_create(512, 512, 64, 1 << 23, 8, 1e-6, 10000.0)
+    assert "2^32" in B.last_error()
 
 
 def test_null_plan_is_an_argument_error(lib):

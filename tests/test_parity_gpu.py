@@ -242,6 +242,31 @@ def test_sizes_near_the_limits(case):
         plan.close()
 
 
+def test_the_longest_cache_the_plan_accepts():
+    """ctx + T = 2^24 - 1 keys with nkv = 2: each operand array holds 2.1e9 elements (past 2^31),
+    the key range is cut into 64 partitions (more than a cluster merges, so through the combine
+    kernel), and the one canvas row sits at position 2^24 - 2.  The cache is drawn on the device
+    (seeded) and copied back for the oracle."""
+    T, nh, nkv, hd = 1, 2, 2, 64
+    ctx = (1 << 24) - 1 - T
+    d = make_inputs(T, 0, nh, nkv, hd, seed=410, weighted=True)
+    g = torch.Generator(device="cuda").manual_seed(411)
+    kc = torch.randn((nkv, ctx, hd), generator=g, device="cuda")
+    vc = torch.randn((nkv, ctx, hd), generator=g, device="cuda")
+    dd = to_dev(d)
+    dd["k_cache"], dd["v_cache"] = kc, vc
+    d["k_cache"], d["v_cache"] = kc.cpu(), vc.cpu()
+    ref = oracle_out(d, nh, nkv, hd)
+    for path in PATHS:
+        plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+        plan.set(B.DG_OPT_PATH, path)
+        out = run_forward(plan, dd)
+        check(out, ref, path, all_rows(T), "longest cache")
+        plan.close()
+        del plan
+        torch.cuda.empty_cache()
+
+
 # (requested partitions, cache length, partitions the tensor-core path uses): with hd = 128 a key
 # tile is 64 keys, so ctx = 700 / 2000 / 2250 (+ T = 40) give 12 / 32 / 36 tiles.  2..8
 # partitions merge inside the kernel (thread-block clusters); 9 and 12 use the combine kernel.
