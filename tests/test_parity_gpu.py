@@ -65,20 +65,30 @@ def run_forward(plan, dd, **kw):
 
 # ------------------------------------------------------------------ first stage alone
 
+# positions: the default (pos0 = ctx), and the largest the plan takes (the last row at 2^24 - 2)
+# with the global layers' rope base
+POSITIONS = [(None, ROPE_THETA), ((1 << 24) - 38, 1.0e6)]
+
+
 @pytest.mark.parametrize("hd", [32, 64, 128, 256])
 @pytest.mark.parametrize("weighted", [True, False])
-def test_norm_rope_stage(hd, weighted):
+@pytest.mark.parametrize("pos", POSITIONS, ids=["pos_ctx", "pos_2e24"])
+def test_norm_rope_stage(hd, weighted, pos):
     T, ctx, nh, nkv = 37, 8100, 4, 2
+    pos0, theta = pos
+    p0 = ctx if pos0 is None else pos0
     d = make_inputs(T, ctx, nh, nkv, hd, seed=5, weighted=weighted, draw_cache=False)
     dd = to_dev(d)
-    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+    plan = B.Plan(nh, nkv, hd, ctx, T, EPS, theta)
+    if pos0 is not None:
+        plan.set(B.DG_OPT_POS0, pos0)
     qh, kh, vh = plan.norm_rope(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["q_norm_w"],
                                 dd["k_norm_w"])
     torch.cuda.synchronize()
     w = lambda x: None if x is None else x.numpy()
-    rq = oracle.norm_rope(d["q"].numpy(), nh, hd, w(d["q_norm_w"]), EPS, True, ctx, ROPE_THETA)
-    rk = oracle.norm_rope(d["k_canvas"].numpy(), nkv, hd, w(d["k_norm_w"]), EPS, True, ctx,
-                          ROPE_THETA)
+    rq = oracle.norm_rope(d["q"].numpy(), nh, hd, w(d["q_norm_w"]), EPS, True, p0, theta)
+    rk = oracle.norm_rope(d["k_canvas"].numpy(), nkv, hd, w(d["k_norm_w"]), EPS, True, p0,
+                          theta)
     rv = oracle.norm_rope(d["v_canvas"].numpy(), nkv, hd, None, EPS, False)
     for got, ref, name in ((qh, rq, "q"), (kh, rk, "k"), (vh, rv, "v")):
         e = np.abs(got.cpu().double().numpy().reshape(ref.shape) - ref)

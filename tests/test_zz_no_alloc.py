@@ -67,6 +67,7 @@ CASES = [
     (50, 0, 4, 4, 64, False, -1),        # no cache: NULL cache pointers
     (30, 200, 4, 2, 128, True, -1),      # a caller's cos|sin table
     (30, 200, 4, 2, 128, False, 4321),   # canvas positions from 4321
+    (30, 200, 4, 2, 64, False, (1 << 24) - 31),   # the largest positions (per-lane angles)
 ]
 
 
