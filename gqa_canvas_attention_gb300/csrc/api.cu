@@ -7,7 +7,8 @@
 //   fp32 path: q_hat [T, nh, hd], k_hat / v_hat [T, nkv, hd]
 //   tensor-core path: Q hi/lo bf16 [nkv, rows_pad, hd] (row R = t*G + h mod G, padded to 128),
 //             K hi/lo bf16 [nkv, S, hd] (S = ctx + T) with the cache in rows 0..ctx-1 and the
-//             canvas in rows ctx..ctx+T-1; V in fp16, same layout
+//             canvas in rows ctx..ctx+T-1; V in fp16, same layout; with DG_OPT_INPUTS_RESIDENT
+//             a second set of these five arrays, the forwards alternating between the two
 //   partials  O [splits, nkv, rows_pad, hd] and (m, l) [splits, nkv, rows_pad]
 //   status    one uint32 that kernels OR their wait failures into
 #include "../../include/dg_attn.h"
@@ -78,17 +79,19 @@ int check_no_overlap(std::initializer_list<Range> outs, std::initializer_list<Ra
     return DG_OK;
 }
 
+// The driver's tensor-map encoder, looked up once (a function-local static: its initialisation
+// is thread-safe, so plans may be created from several host threads at once).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return PFN_cuTensorMapEncodeTiled_v12000(nullptr);
+    }();
     return fn;
 }
 
