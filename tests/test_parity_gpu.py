@@ -688,3 +688,45 @@ def test_cache_value_beyond_fp16_is_reported(prepared):
     rel = np.abs(out - ref) / np.maximum(1.0, np.abs(ref))
     print(f"range-fp32: max |ref| {np.abs(ref).max():.3e}, max relative err {rel.max():.3e}")
     assert rel.max() <= 1e-5
+
+
+def test_plans_on_several_host_threads():
+    """Four host threads each create their own plan (both paths, two head sizes) and run forwards
+    on their own stream at the same time; each result equals the same forward run alone.  The
+    library's host state (the last-error text, the tensor-map encoder and the per-device kernel
+    attributes) is per thread or set up once under a thread-safe guard."""
+    import threading
+    cases = [(40, 300, 4, 2, 128, B.DG_PATH_TC), (40, 300, 4, 2, 256, B.DG_PATH_TC),
+             (33, 100, 8, 2, 64, B.DG_PATH_FP32), (50, 0, 4, 4, 64, B.DG_PATH_TC)]
+    inputs = [to_dev(make_inputs(T, ctx, nh, nkv, hd, seed=500 + i))
+              for i, (T, ctx, nh, nkv, hd, _) in enumerate(cases)]
+    torch.cuda.synchronize()                # the inputs are read on other streams
+
+    def run(i, results):
+        T, ctx, nh, nkv, hd, path = cases[i]
+        dd = inputs[i]
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+            plan.set(B.DG_OPT_PATH, path)
+            outs = [plan.forward(dd["q"], dd["k_canvas"], dd["v_canvas"], dd["k_cache"],
+                                 dd["v_cache"], dd["q_norm_w"], dd["k_norm_w"],
+                                 stream=stream.cuda_stream) for _ in range(3)]
+            stream.synchronize()
+            assert plan.sync_status(stream.cuda_stream) == B.DG_OK
+            plan.close()
+        results[i] = outs
+
+    alone = {}
+    for i in range(len(cases)):
+        run(i, alone)
+    together = {}
+    threads = [threading.Thread(target=run, args=(i, together)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for i in range(len(cases)):
+        assert i in together, f"thread {i} failed"
+        for a, b in zip(alone[i], together[i]):
+            assert torch.equal(a, b)
