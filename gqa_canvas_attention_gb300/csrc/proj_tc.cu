@@ -519,7 +519,11 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
         if (ok) {
             tc_fence_after();
             float ss = 0.f;
-            float4 *dst = reinterpret_cast<float4 *>(p.y + (size_t)t * p.H + n0);
+            // Every MMA has completed, so the operand ring is free: each warp stages 16 columns
+            // of its 32 rows at a time (row pitch 20 floats, conflict-free for float4) and writes
+            // them back row-contiguous, 8 rows x 64 bytes per store instruction.
+            float *stage = reinterpret_cast<float *>(smem) + quarter * (32 * 20);
+            const int j0 = lane >> 2, q4 = lane & 3;
 #pragma unroll 1
             for (int c = 0; c < N / 16; ++c) {
                 uint32_t u[16];
@@ -530,8 +534,18 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
                     const float4 f = make_float4(__uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
                                                  __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
                     ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
-                    if (t < p.T) dst[4 * c + v] = f;
+                    *reinterpret_cast<float4 *>(stage + lane * 20 + 4 * v) = f;
                 }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int jr = 8 * k + j0;                     // row of the warp's 32
+                    const int tr = m0 + quarter * 32 + jr;
+                    if (tr < p.T)
+                        *reinterpret_cast<float4 *>(p.y + (size_t)tr * p.H + n0 + 16 * c + 4 * q4) =
+                            *reinterpret_cast<const float4 *>(stage + jr * 20 + 4 * q4);
+                }
+                __syncwarp();
             }
             if (t < p.T) p.part_ss[(size_t)t * gridDim.x + blockIdx.x] = ss;
         } else if (lane == 0) {
