@@ -283,18 +283,13 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     const uint32_t tacc = *tmem_slot;
 
     // Epilogue: eight warps, two per TMEM lane quarter.  Thread (row r, half h) takes columns
-    // 32h..32h+31 of each of the two groups (RoPE partners stay in one thread).  The row's
-    // input-norm scale and, for q and k heads, the cos / sin of its columns are loaded while the
-    // main loop still runs (these warps have nothing else to do until it ends); the accumulator
-    // is then read twice from TMEM, once for the sum of squares and once, 16 columns at a time,
-    // for the outputs, so that only a few of its values are live beside the cos / sin.
-    constexpr int CW = 32, CH = 16;
-    float cosv[CW], sinv[CW];     // cos / sin of the angles of this thread's columns
-    float rs = 0.f;               // the row's input-norm scale
+    // 32h..32h+31 of each of the two groups (RoPE partners stay in one thread).
+    constexpr int CW = 32;
+    float a[CW], b[CW];           // the token row's values of groups g0 and g1 (this half)
+    float ss_local = 0.f;
     bool epi_ok = false;
     const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
     float *ss_part = ss_ex + kTileM;                         // [2][128] per-half partial sums
-    const int kind = head < p.nh ? 0 : head < p.nh + p.nkv ? 1 : 2;   // q, k, v
 
     if (warp == 0) {
         if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, g0 * 64, g1 * 64, nk, limit))
@@ -305,36 +300,29 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         if (e && lane == 0) atomicOr(p.status, e);
         __syncwarp();
     } else {
-        // part 1: the row's partial sum of squares (this half's columns of both groups)
+        // part 1: accumulator columns into registers, input-norm scale, partial sum of squares
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int t = m0 + r;
-        rs = t < p.T ? p.rin[t] : 0.f;
-        if (kind < 2 && t < p.T) {
-            const float *cs = p.cos_sin + (size_t)t * 2 * HD + c0 + CW * half;
-#pragma unroll
-            for (int i = 0; i < CW; i += 4) {
-                const float4 c4 = *reinterpret_cast<const float4 *>(cs + i);
-                const float4 s4 = *reinterpret_cast<const float4 *>(cs + HD + i);
-                cosv[i] = c4.x; cosv[i + 1] = c4.y; cosv[i + 2] = c4.z; cosv[i + 3] = c4.w;
-                sinv[i] = s4.x; sinv[i + 1] = s4.y; sinv[i + 2] = s4.z; sinv[i + 3] = s4.w;
-            }
-        }
-        float ss_local = 0.f;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, limit));
         if (ok) {
             tc_fence_after();
-#pragma unroll 1
-            for (int grp = 0; grp < 2; ++grp) {
-                uint32_t u[32];
-                tmem_ld32(tacc + lane_off + 64 * grp + CW * half, u);
-                tmem_wait_ld();
+            uint32_t u[32];
+            tmem_ld32(tacc + lane_off + CW * half, u);
+            tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < CW; ++i) {
-                    const float x = __uint_as_float(u[i]) * rs;
-                    ss_local = fmaf(x, x, ss_local);
-                }
+            for (int i = 0; i < CW; ++i) a[i] = __uint_as_float(u[i]);
+            tmem_ld32(tacc + lane_off + 64 + CW * half, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < CW; ++i) b[i] = __uint_as_float(u[i]);
+            const int t = m0 + r;
+            const float rs = t < p.T ? p.rin[t] : 0.f;
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                a[i] *= rs;
+                b[i] *= rs;
+                ss_local = fmaf(a[i], a[i], fmaf(b[i], b[i], ss_local));
             }
             epi_ok = true;
         } else if (lane == 0) {
@@ -356,39 +344,21 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     if (warp >= 2 && epi_ok) {
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int t = m0 + r;
         float ss = ss_ex[r];
         if constexpr (HD == 256)
             ss += dsmem_ld_f32(dsmem_map(smem_u32(&ss_ex[r]), cluster_ctarank() ^ 1u));
         const float rn = rsqrtf(ss / (float)HD + p.eps);
         const int nq = p.nh, nkh = p.nkv;
+        const int kind = head < nq ? 0 : head < nq + nkh ? 1 : 2;   // q, k, v
         const int hh = kind == 0 ? head : kind == 1 ? head - nq : head - nq - nkh;
         const int ca = c0 + CW * half, cb = ca + HD / 2;         // first columns (in the head)
-        const bool vout = kind == 2 || (kind == 1 && p.kv_shared);
-        const float *w = kind == 0 ? p.wq_norm : p.wk_norm;
-        const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;   // q in log2 units
-        // every lane reads TMEM (warp-collective); only rows below T store.  Unrolled, so that
-        // cosv / sinv are indexed with constants (they stay in registers).
-#pragma unroll
-        for (int c = 0; c < CW; c += CH) {
-            uint32_t ua[CH], ub[CH];
-            tmem_ld16(tacc + lane_off + CW * half + c, ua);
-            tmem_ld16(tacc + lane_off + 64 + CW * half + c, ub);
-            tmem_wait_ld();
-            if (t >= p.T) continue;
-            float a[CH], b[CH];
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                a[i] = __uint_as_float(ua[i]) * rs;
-                b[i] = __uint_as_float(ub[i]) * rs;
-            }
-            if (vout) {
-                // v-hat: the weightless, un-roped norm (of the k projection when v is not
-                // projected)
+        if (t < p.T) {
+            // v-hat: the weightless, un-roped norm (of the k projection when v is not projected)
+            if (kind == 2 || (kind == 1 && p.kv_shared)) {
                 __half *vrow = p.vh + ((size_t)hh * p.S + p.ctx + t) * HD;
 #pragma unroll
-                for (int u = 0; u < CH / 8; ++u) {
+                for (int u = 0; u < CW / 8; ++u) {
                     uint4 wa, wb;
                     uint32_t *pa = reinterpret_cast<uint32_t *>(&wa);
                     uint32_t *pb = reinterpret_cast<uint32_t *>(&wb);
@@ -400,48 +370,54 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
                         pa[e] = *reinterpret_cast<const uint32_t *>(&ha);
                         pb[e] = *reinterpret_cast<const uint32_t *>(&hb);
                     }
-                    reinterpret_cast<uint4 *>(vrow + ca + c)[u] = wa;
-                    reinterpret_cast<uint4 *>(vrow + cb + c)[u] = wb;
+                    reinterpret_cast<uint4 *>(vrow + ca)[u] = wa;
+                    reinterpret_cast<uint4 *>(vrow + cb)[u] = wb;
                 }
             }
             if (kind < 2) {
-                // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (ca + c + i, cb + c + i)
+                // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (ca + i, cb + i)
+                const float *w = kind == 0 ? p.wq_norm : p.wk_norm;
+                const float *cs = p.cos_sin + (size_t)t * 2 * HD;
+                const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;   // q in log2 units
 #pragma unroll
-                for (int i = 0; i < CH; i += 4) {
+                for (int i = 0; i < CW; i += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + ca + i);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + HD + ca + i);
                     float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
                     if (w) {
-                        wa = *reinterpret_cast<const float4 *>(w + ca + c + i);
-                        wb = *reinterpret_cast<const float4 *>(w + cb + c + i);
+                        wa = *reinterpret_cast<const float4 *>(w + ca + i);
+                        wb = *reinterpret_cast<const float4 *>(w + cb + i);
                     }
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
                     const float ww[4] = {wa.x, wa.y, wa.z, wa.w}, vv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float ya = a[i + e] * rn * ww[e], yb = b[i + e] * rn * vv[e];
-                        a[i + e] = fmaf(ya, cosv[c + i + e], -yb * sinv[c + i + e]) * sc;
-                        b[i + e] = fmaf(yb, cosv[c + i + e], ya * sinv[c + i + e]) * sc;
+                        a[i + e] = fmaf(ya, cc[e], -yb * sn[e]) * sc;
+                        b[i + e] = fmaf(yb, cc[e], ya * sn[e]) * sc;
                     }
                 }
-                float hi[CH], lo[CH];
+                float hi[CW], lo[CW];
                 if (kind == 0) {
                     const int g = hh / p.G, R = t * p.G + hh % p.G;
                     const size_t tile = ((size_t)g * (p.rows_pad / kTileM) + R / kTileM) * HD * kTileM;
                     const size_t qrow = ((size_t)g * p.rows_pad + R) * HD;
-                    split_n<CH>(a, hi, lo);
-                    store_q_rows<CH>(p.qh + tile, R % kTileM, ca + c, hi);
-                    if (p.ql_interleaved) store_q_rows<CH>(p.ql + tile, R % kTileM, ca + c, lo);
-                    else store_bf16_row<CH>(p.ql + qrow + ca + c, lo);
-                    split_n<CH>(b, hi, lo);
-                    store_q_rows<CH>(p.qh + tile, R % kTileM, cb + c, hi);
-                    if (p.ql_interleaved) store_q_rows<CH>(p.ql + tile, R % kTileM, cb + c, lo);
-                    else store_bf16_row<CH>(p.ql + qrow + cb + c, lo);
+                    split_n<CW>(a, hi, lo);
+                    store_q_rows<CW>(p.qh + tile, R % kTileM, ca, hi);
+                    if (p.ql_interleaved) store_q_rows<CW>(p.ql + tile, R % kTileM, ca, lo);
+                    else store_bf16_row<CW>(p.ql + qrow + ca, lo);
+                    split_n<CW>(b, hi, lo);
+                    store_q_rows<CW>(p.qh + tile, R % kTileM, cb, hi);
+                    if (p.ql_interleaved) store_q_rows<CW>(p.ql + tile, R % kTileM, cb, lo);
+                    else store_bf16_row<CW>(p.ql + qrow + cb, lo);
                 } else {
                     const size_t row = ((size_t)hh * p.S + p.ctx + t) * HD;
-                    split_n<CH>(a, hi, lo);
-                    store_bf16_row<CH>(p.kh + row + ca + c, hi);
-                    store_bf16_row<CH>(p.kl + row + ca + c, lo);
-                    split_n<CH>(b, hi, lo);
-                    store_bf16_row<CH>(p.kh + row + cb + c, hi);
-                    store_bf16_row<CH>(p.kl + row + cb + c, lo);
+                    split_n<CW>(a, hi, lo);
+                    store_bf16_row<CW>(p.kh + row + ca, hi);
+                    store_bf16_row<CW>(p.kl + row + ca, lo);
+                    split_n<CW>(b, hi, lo);
+                    store_bf16_row<CW>(p.kh + row + cb, hi);
+                    store_bf16_row<CW>(p.kl + row + cb, lo);
                 }
             }
         }
