@@ -305,6 +305,33 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, limit));
+        if (ok && head < p.nh + p.nkv) {
+            // Every MMA has completed, so the operand ring is free: the eight warps copy the cos
+            // and sin of columns c0..c0+63 of the tile's 128 rows into it with row-contiguous
+            // loads (two 256-byte rows per warp instruction); the rotation below reads them back
+            // (row pitch 68 floats, conflict-free for float4), ordered by the barrier that follows.
+            // 4096 float4 over 256 threads: each thread's 16 loads are all issued before its
+            // first store (one memory round trip, not sixteen)
+            float *cs_s = reinterpret_cast<float *>(smem);
+            constexpr int kItems = kTileM * 2 * 16 / 256;
+            float4 v[kItems];
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int it = (int)threadIdx.x - 64 + 256 * k;
+                const int row = it >> 5, w = (it >> 4) & 1, q4 = it & 15;
+                const int tt = m0 + row;
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tt < p.T)
+                    v[k] = *reinterpret_cast<const float4 *>(p.cos_sin + (size_t)tt * 2 * HD +
+                                                             w * HD + c0 + 4 * q4);
+            }
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int it = (int)threadIdx.x - 64 + 256 * k;
+                const int row = it >> 5, w = (it >> 4) & 1, q4 = it & 15;
+                *reinterpret_cast<float4 *>(cs_s + (row * 2 + w) * 68 + 4 * q4) = v[k];
+            }
+        }
         if (ok) {
             tc_fence_after();
             uint32_t u[32];
@@ -377,12 +404,13 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             if (kind < 2) {
                 // q-hat / k-hat: norm, weight, NeoX rotation of the pairs (ca + i, cb + i)
                 const float *w = kind == 0 ? p.wq_norm : p.wk_norm;
-                const float *cs = p.cos_sin + (size_t)t * 2 * HD;
+                // this row's cos / sin of columns ca.., staged in shared memory above
+                const float *cs = reinterpret_cast<const float *>(smem) + r * 2 * 68 + CW * half;
                 const float sc = kind == 0 ? 1.4426950408889634f : 1.0f;   // q in log2 units
 #pragma unroll
                 for (int i = 0; i < CW; i += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + ca + i);
-                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + HD + ca + i);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + i);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + 68 + i);
                     float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
                     if (w) {
                         wa = *reinterpret_cast<const float4 *>(w + ca + i);
