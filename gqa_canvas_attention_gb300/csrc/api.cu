@@ -510,10 +510,13 @@ int unswap_unless_launched(dg_attn_plan *p, int rc, int other, unsigned long lon
 
 // Attention + (when partitioned) combine, reading the operands the first stage left in scratch.
 // `fresh_cache`: the cache rows were converted by this call's first-stage launch, so the
-// tensor-core kernel may not load them before its wait for that launch.
+// tensor-core kernel may not load them before its wait for that launch.  `split` (the layer
+// path): where the attention kernel writes the output itself, have it also write the bf16 hi /
+// lo split the o_proj GEMM reads (p->aoh / p->aol), and set *split to say so.
 int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cache, float *out,
-                      cudaStream_t s, bool fresh_cache = false)
+                      cudaStream_t s, bool fresh_cache = false, bool *split = nullptr)
 {
+    if (split) *split = false;
     int splits, tps, nt;
     split_layout(p, splits, tps, nt);
     SkLayout sk;
@@ -541,6 +544,10 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.cluster_combine = !stream_k && cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
         a.static_keys = fresh_cache ? 0 : p->ctx;
+        if (split && p->aoh && !stream_k && (splits == 1 || a.cluster_combine)) {
+            a.out_hi = p->aoh;
+            a.out_lo = p->aol;
+        }
         if (stream_k) {
             a.sk_ctas = sk.ctas;
             a.sk_units = sk.units;
@@ -549,6 +556,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         err = dg::launch_attn_tc(a, p->op.maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
         ++p->attn_launched;
+        if (split) *split = a.out_hi != nullptr;
     } else {
         dg::AttnFp32Params a{};
         a.q = p->q32; a.k = p->k32; a.v = p->v32;
@@ -1188,9 +1196,14 @@ int dg_attn_proj_prepare(dg_attn_plan *p, int H, const float *ln_in_w, const flo
     return DG_OK;
 }
 
-int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache,
-                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
-                           const float *cos_sin, float *out, cudaStream_t s)
+}  // extern "C"
+
+namespace {
+
+// dg_attn_forward_hidden, and (with `split`) the first half of dg_attn_forward_layer.
+int forward_hidden_impl(dg_attn_plan *p, const float *x, const float *k_cache,
+                        const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                        const float *cos_sin, float *out, cudaStream_t s, bool *split)
 {
     if (int rc = check_plan(p)) return rc;
     if (!p->proj_ready) {
@@ -1243,7 +1256,19 @@ int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache
     err = dg::launch_qkv_proj(q, p->pmaps, p->hd, p->proj_rows / 128, s);
     if (err != cudaSuccess) return cuda_fail(err, "projection launch");
     if ((rc = record_event(p, DG_STAGE_PROJECTION, s))) return rc;
-    return enqueue_attention(p, k_cache, v_cache, out, s);
+    return enqueue_attention(p, k_cache, v_cache, out, s, false, split);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dg_attn_forward_hidden(dg_attn_plan *p, const float *x, const float *k_cache,
+                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
+                           const float *cos_sin, float *out, cudaStream_t s)
+{
+    return forward_hidden_impl(p, x, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin, out, s,
+                               nullptr);
 }
 
 int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *ln_post_w,
@@ -1311,7 +1336,14 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
     return DG_OK;
 }
 
-int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid, cudaStream_t s)
+}  // extern "C"
+
+namespace {
+
+// dg_attn_oproj_residual; `split_ready`: the attention kernel has already written the bf16 hi /
+// lo split of attn_out into p->aoh / p->aol, so the operand split kernel is skipped.
+int oproj_residual_impl(dg_attn_plan *p, const float *attn_out, float *resid, cudaStream_t s,
+                        bool split_ready)
 {
     if (int rc = check_plan(p)) return rc;
     if (!p->oproj_ready) {
@@ -1329,9 +1361,12 @@ int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid,
     const int K = p->nh * p->hd;
     int rc = record_event(p, DG_STAGE_OPROJ, s);
     if (rc) return rc;
-    dg::ProjPrepParams pp{attn_out, nullptr, p->aoh, p->aol, p->T, K, p->eps};
-    cudaError_t err = dg::launch_hidden_prep(pp, s);
-    if (err != cudaSuccess) return cuda_fail(err, "o_proj operand launch");
+    cudaError_t err = cudaSuccess;
+    if (!split_ready) {
+        dg::ProjPrepParams pp{attn_out, nullptr, p->aoh, p->aol, p->T, K, p->eps};
+        err = dg::launch_hidden_prep(pp, s);
+        if (err != cudaSuccess) return cuda_fail(err, "o_proj operand launch");
+    }
     dg::OprojParams o{p->ybuf, p->part_ss, p->status,
                       (unsigned long long)p->wait_limit_ms * 1000000ull, p->T, p->oH, K, p->otile};
     err = dg::launch_oproj(o, p->omaps, s);
@@ -1343,6 +1378,15 @@ int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid,
     return record_event(p, DG_STAGE_OPROJ, s);
 }
 
+}  // namespace
+
+extern "C" {
+
+int dg_attn_oproj_residual(dg_attn_plan *p, const float *attn_out, float *resid, cudaStream_t s)
+{
+    return oproj_residual_impl(p, attn_out, resid, s, false);
+}
+
 int dg_attn_forward_layer(dg_attn_plan *p, float *resid, const float *k_cache,
                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
                           const float *cos_sin, cudaStream_t s)
@@ -1352,10 +1396,12 @@ int dg_attn_forward_layer(dg_attn_plan *p, float *resid, const float *k_cache,
         set_error("the layer needs dg_attn_proj_prepare and dg_attn_oproj_prepare with one H");
         return DG_ERR_STATE;
     }
-    if (int rc = dg_attn_forward_hidden(p, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
-                                        p->attn_buf, s))
+    // the attention kernel writes o_proj's bf16 operand split itself where it writes the output
+    bool split = false;
+    if (int rc = forward_hidden_impl(p, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
+                                     p->attn_buf, s, &split))
         return rc;
-    return dg_attn_oproj_residual(p, p->attn_buf, resid, s);
+    return oproj_residual_impl(p, p->attn_buf, resid, s, split);
 }
 
 int dg_attn_sync_status(dg_attn_plan *p, cudaStream_t s)

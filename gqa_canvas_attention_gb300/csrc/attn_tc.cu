@@ -121,9 +121,27 @@ constexpr float kHeadroom = 0.0f;
 // read through distributed shared memory, whose latency is long: each thread takes U float4
 // columns (of different rows) at once, so U * P loads are in flight per thread.  The CTA's own
 // rows (partition `self`) are read through the local shared-memory path.
+// Four output values as the bf16 hi / lo pair the o_proj GEMM takes (hi = bf16(o),
+// lo = bf16(o - hi)), at element i of the two [T, nh*hd] arrays.
+__device__ __forceinline__ void store_split4(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i,
+                                             float4 v)
+{
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+    *reinterpret_cast<uint2 *>(hi + i) = make_uint2(*reinterpret_cast<const uint32_t *>(&h01),
+                                                    *reinterpret_cast<const uint32_t *>(&h23));
+    *reinterpret_cast<uint2 *>(lo + i) = make_uint2(*reinterpret_cast<const uint32_t *>(&l01),
+                                                    *reinterpret_cast<const uint32_t *>(&l23));
+}
+
 template <int P, int HD, int THREADS, int PITCH>
 __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int self, int r0, int nr,
-                                                   const float *wgt, float *const *dst)
+                                                   const float *wgt, float *const *dst,
+                                                   const float *out, __nv_bfloat16 *out_hi,
+                                                   __nv_bfloat16 *out_lo)
 {
     constexpr int V4 = HD / 4;
     constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1);
@@ -160,6 +178,7 @@ __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int self,
                 acc.w = fmaf(w, v[u][q].w, acc.w);
             }
             *reinterpret_cast<float4 *>(d + 4 * (item % V4)) = acc;
+            if (out_hi) store_split4(out_hi, out_lo, (size_t)(d - out) + 4 * (item % V4), acc);
         }
     }
 }
@@ -801,9 +820,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                     const int j = 4 * k + rsub;
                     float *d = reinterpret_cast<float *>(
                         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mydst), j));
-                    if (d)
-                        *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) =
-                            *reinterpret_cast<const float4 *>(stage + j * 36 + 4 * sub);
+                    if (d) {
+                        const float4 o4 = *reinterpret_cast<const float4 *>(stage + j * 36 + 4 * sub);
+                        *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) = o4;
+                        if (p.out_hi && p.splits == 1)
+                            store_split4(p.out_hi, p.out_lo,
+                                         (size_t)(d - p.out) + 32 * c + 4 * sub, o4);
+                    }
                 }
                 __syncwarp();
             }
@@ -856,14 +879,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
         __syncthreads();
         const uint32_t sb = smem_u32(smem);
         constexpr int TH = Lay::THREADS, PI = Lay::STG_PITCH;
+        float *const o = p.out;
+        __nv_bfloat16 *const oh = p.out_hi, *const ol = p.out_lo;
         switch (P) {
-        case 2: cluster_merge_rows<2, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        case 3: cluster_merge_rows<3, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        case 4: cluster_merge_rows<4, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        case 5: cluster_merge_rows<5, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        case 6: cluster_merge_rows<6, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        case 7: cluster_merge_rows<7, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
-        default: cluster_merge_rows<8, HD, TH, PI>(sb, rank, r0, nr, wgt, dst); break;
+        case 2: cluster_merge_rows<2, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        case 3: cluster_merge_rows<3, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        case 4: cluster_merge_rows<4, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        case 5: cluster_merge_rows<5, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        case 6: cluster_merge_rows<6, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        case 7: cluster_merge_rows<7, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
+        default: cluster_merge_rows<8, HD, TH, PI>(sb, rank, r0, nr, wgt, dst, o, oh, ol); break;
         }
         // no CTA leaves (or frees its shared memory) while a peer may still read it
         cluster_sync_all();

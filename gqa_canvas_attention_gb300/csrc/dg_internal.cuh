@@ -104,6 +104,9 @@ struct AttnTcParams {
     int cluster_combine;           // 1: the splits CTAs of a query tile form a cluster and merge
                                    // their partial results through distributed shared memory
     int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
+    __nv_bfloat16 *out_hi, *out_lo;// null, or [T, nh*hd] beside out: its bf16 hi / lo split
+                                   // (hi = bf16(o), lo = bf16(o - hi)), written by the schedules
+                                   // whose CTAs write the output themselves
     int static_keys;               // keys [0, static_keys) of every kv group (cache rows) were
                                    // complete before the kernel ahead of this one started: the
                                    // producers may load them before waiting for that kernel

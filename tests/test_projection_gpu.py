@@ -129,3 +129,42 @@ def test_attention_branch_of_a_layer_parity():
     print(f"max {e.max():.3e} mean {e.mean():.3e}")
     assert np.isfinite(e).all()
     assert e.max() <= 5e-3 and e.mean() <= 5e-4
+
+
+@pytest.mark.parametrize("schedule", ["clustered", "one_partition", "stream_k", "nine_partitions"])
+def test_layer_writes_the_o_proj_operands_in_the_attention_kernel(schedule):
+    """Inside dg_attn_forward_layer the attention kernel, where it writes the output itself (one
+    partition, or partitions merged inside a cluster), also writes the bf16 hi / lo split that
+    o_proj reads, with the same arithmetic as the separate split kernel; the other schedules
+    (stream-K, more than 8 partitions through the combine kernel) keep that kernel.  Either way
+    the residual stream must come out bit for bit as when the two steps are called separately."""
+    T, ctx, nh, nkv, hd, H = 130, 700, 8, 4, 256, 512
+    d = make_inputs(T, ctx, nh, nkv, hd, seed=95)
+    g = torch.Generator().manual_seed(96)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float32)
+    x = r(T, H)
+    ln, wq, wk, wv = weights(H, nh, nkv, hd, 97)
+    wo, ln_post = r(H, nh * hd) / (nh * hd) ** 0.5, 1.0 + 0.1 * r(H)
+    cu = lambda t: None if t is None else t.cuda()
+    results = []
+    for fused in (True, False):
+        plan = B.Plan(nh, nkv, hd, ctx, T, EPS, ROPE_THETA)
+        if schedule == "one_partition":
+            plan.set(B.DG_OPT_SPLITS, 1)
+        elif schedule == "stream_k":
+            plan.set(B.DG_OPT_SCHEDULE, B.DG_SCHEDULE_STREAM_K)
+        elif schedule == "nine_partitions":
+            plan.set(B.DG_OPT_SPLITS, 9)
+        plan.proj_prepare(H, cu(ln), cu(wq), cu(wk), cu(wv))
+        plan.oproj_prepare(H, cu(wo), cu(ln_post))
+        xd = cu(x)
+        kc, vc = cu(d["k_cache"]), cu(d["v_cache"])
+        if fused:
+            plan.forward_layer(xd, kc, vc, cu(d["q_norm_w"]), cu(d["k_norm_w"]))
+        else:
+            attn = plan.forward_hidden(xd, kc, vc, cu(d["q_norm_w"]), cu(d["k_norm_w"]))
+            plan.oproj_residual(attn, xd)
+        assert plan.sync_status() == B.DG_OK
+        results.append(xd)
+        plan.close()
+    assert torch.equal(results[0], results[1])
