@@ -14,8 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "dgattn")
 LIB = os.path.join(PKG, "libdgattn.so")
-SOURCES = ["api.cu", "norm_rope.cu", "attn_fp32.cu", "attn_tc.cu", "aux_kernels.cu", "noalloc.cu",
-           "proj_tc.cu"]
+SOURCES = ["api.cu", "norm_rope.cu", "attn_fp32.cu", "attn_tc.cu", "attn_tc_split.cu",
+           "aux_kernels.cu", "noalloc.cu", "proj_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -26,7 +26,8 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-ATTN_KERNEL_SOURCES = ["attn_tc.cu", "sm103_ptx.cuh", "dg_internal.cuh", "api.cu"]
+ATTN_KERNEL_SOURCES = ["attn_tc_kernel.cuh", "attn_tc.cu", "sm103_ptx.cuh", "dg_internal.cuh",
+                       "api.cu"]
 
 
 def attn_kernel_source_id() -> str:

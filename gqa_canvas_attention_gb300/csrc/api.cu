@@ -176,6 +176,7 @@ struct dg_attn_plan {
     int oH;                         // hidden size W_o was prepared for
     int otile;                      // o_proj output columns per CTA
     bool oproj_ready, has_ln_post;
+    bool split_attn;                // the attention variant writing aoh / aol is set up (hd 128, 256)
     __nv_bfloat16 *woh, *wol;       // [oH, nh*hd] W_o, bf16 hi / lo
     __nv_bfloat16 *aoh, *aol;       // [T_pad, nh*hd] the attention output, bf16 hi / lo
     float *ybuf, *part_ss;          // [T, oH] the projection, [T, oH/128] its partial sums
@@ -544,7 +545,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.cluster_combine = !stream_k && cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
         a.static_keys = fresh_cache ? 0 : p->ctx;
-        if (split && p->aoh && !stream_k && (splits == 1 || a.cluster_combine)) {
+        if (split && p->split_attn && p->aoh && !stream_k && (splits == 1 || a.cluster_combine)) {
             a.out_hi = p->aoh;
             a.out_lo = p->aol;
         }
@@ -1290,6 +1291,13 @@ int dg_attn_oproj_prepare(dg_attn_plan *p, int H, const float *wo, const float *
     }
     cudaError_t err = dg::once_per_device(g_proj_attrs, dg::proj_prepare_attrs);
     if (err != cudaSuccess) return cuda_fail(err, "projection kernel attributes");
+    // The layer path's attention variant is set up (and so loaded) here, not with the plan: a
+    // plan that never runs the layer keeps only the default attention kernels on the device.
+    if (p->tc_ok && (p->hd == 128 || p->hd == 256)) {
+        err = dg::attn_tc_split_prepare(p->hd);
+        if (err != cudaSuccess) return cuda_fail(err, "attention kernel attributes");
+        p->split_attn = true;
+    }
     const int K = p->nh * p->hd;
     const int t_pad = ((p->T + dg::kTileM - 1) / dg::kTileM) * dg::kTileM;
     if (H != p->oH) {

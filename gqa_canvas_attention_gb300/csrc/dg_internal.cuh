@@ -104,9 +104,6 @@ struct AttnTcParams {
     int cluster_combine;           // 1: the splits CTAs of a query tile form a cluster and merge
                                    // their partial results through distributed shared memory
     int inject_stall;              // test hook: withhold the first P-ready signal of each CTA
-    __nv_bfloat16 *out_hi, *out_lo;// null, or [T, nh*hd] beside out: its bf16 hi / lo split
-                                   // (hi = bf16(o), lo = bf16(o - hi)), written by the schedules
-                                   // whose CTAs write the output themselves
     int static_keys;               // keys [0, static_keys) of every kv group (cache rows) were
                                    // complete before the kernel ahead of this one started: the
                                    // producers may load them before waiting for that kernel
@@ -115,6 +112,9 @@ struct AttnTcParams {
     // to part_o / part_ml at slot = its rank among the CTAs of that pair
     int sk_ctas, qtiles;
     long long sk_units;
+    __nv_bfloat16 *out_hi, *out_lo;// null, or [T, nh*hd] beside out: its bf16 hi / lo split
+                                   // (hi = bf16(o), lo = bf16(o - hi)), written by the split
+                                   // schedule's CTAs that write output rows (the layer path)
 };
 
 // Stream-K schedule: U key-tile units over C CTAs, CTA c taking [sk_begin(c), sk_begin(c + 1)).
@@ -258,6 +258,11 @@ cudaError_t launch_attn_fp32(const AttnFp32Params &p, int hd, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnTcParams &p, const TcMaps &maps, int hd, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t attn_tc_prepare(int hd);   // one-time function attributes (smem opt-in)
+// The split-schedule variant that also writes o_proj's bf16 hi/lo operands (p.out_hi/out_lo;
+// hd 128 and 256): its own launch with the configuration launch_attn_tc built, and its attributes.
+cudaError_t launch_attn_tc_split(const cudaLaunchConfig_t &cfg, const TcMaps &maps,
+                                 const AttnTcParams &p, int hd);
+cudaError_t attn_tc_split_prepare(int hd);
 // Clusters of `splits` CTAs the GPU can hold at once (0: that cluster launch cannot run).
 int attn_tc_max_clusters(int hd, int splits, int qtiles, int nkv);
 constexpr int kMaxClusterSplits = 8;   // portable cluster size
