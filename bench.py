@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--path", default="tc", choices=["tc", "fp32"])
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--hidden", type=int, default=0,
                     help="run each forward from a residual stream of this width through the "
                          "projection step (input norm + q/k/v projections) instead of from q/k/v")
@@ -571,90 +571,102 @@ def main():
         del src_buf, dst_buf, flush
 
     # ---------------------------------------------------------------- end to end from host memory
-    # Each forward's canvas goes host -> device and its output device -> host through pinned
-    # buffers, every step, the cache once per step.  The copies run on copy streams and the
-    # forwards on the compute stream, four buffers deep and ordered by events, so the transfers of
-    # the next and previous forwards overlap the kernels of forward i (as a serving loop would run them); the
-    # next step's cache is copied on a stream of its own while this step's forwards run.
+    # Every step's inputs go host -> device and every forward's output device -> host through
+    # pinned buffers, inside the timed region.  The transfers are pipelined a step at a time: a
+    # step's canvases and cache (one copy per array) upload on one copy stream while the step
+    # before it computes, and its 48 outputs download on another while the step after it
+    # computes, through two device slots of each.  The compute stream then meets events only at
+    # step boundaries: an event recorded or awaited between two forwards would switch off the
+    # overlap of one forward's attention kernel with the next forward's first stage
+    # (programmatic dependent launch), ~15 us per forward.  The first step's upload and the last
+    # step's download have nothing to overlap with; both are inside the timed region.
     e2e = None
     if args.e2e_steps > 0 and not args.hidden:
-        pin = lambda t: None if t is None else t.cpu().pin_memory()
-        h_kc, h_vc = pin(kc), pin(vc)
-        h_canv = [{k: pin(v) for k, v in c.items()} for c in canv]
-        h_out = [torch.empty((w.T, w.nh * w.hd), dtype=torch.float32).pin_memory()
-                 for _ in range(n_fwd)]
-        # four device buffers of canvas inputs and outputs: the link (pinned copies at ~200 GB/s
-        # one way, ~140 GB/s each way when both directions run) is nearly as busy as the GPU, so
-        # the copies get slack to absorb their jitter
-        NB = 4
-        d_in = [{k: torch.empty_like(v) if v is not None else None for k, v in canv[0].items()}
-                for _ in range(NB)]
-        d_out = [torch.empty_like(out) for _ in range(NB)]
+        keys = [k for k in ("q", "k_canvas", "v_canvas", "q_norm_w", "k_norm_w")
+                if canv[0][k] is not None]
+        h_in = {k: torch.stack([c[k].cpu() for c in canv]).pin_memory() for k in keys}
+        h_kc = kc.cpu().pin_memory() if kc is not None else None
+        h_vc = vc.cpu().pin_memory() if vc is not None else None
+        h_out = torch.empty((n_fwd, w.T, w.nh * w.hd), dtype=torch.float32).pin_memory()
+        d_in = [{k: torch.empty_like(h_in[k], device=dev) for k in keys} for _ in range(2)]
+        d_out = [torch.empty_like(h_out, device=dev) for _ in range(2)]
         d_kc = [torch.empty_like(kc) if kc is not None else None for _ in range(2)]
         d_vc = [torch.empty_like(vc) if vc is not None else None for _ in range(2)]
-        h2d = (0 if kc is None else (kc.numel() + vc.numel()) * 4)
-        h2d += sum(v.numel() * 4 for v in canv[0].values() if v is not None) * n_fwd
-        d2h = out.numel() * 4 * n_fwd
-        s_in, s_out, s_cache = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        h2d = sum(t.numel() * 4 for t in h_in.values())
+        h2d += 0 if kc is None else (kc.numel() + vc.numel()) * 4
+        d2h = h_out.numel() * 4
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()
-        ev_cache, ev_cache_free = [ev(), ev()], [ev(), ev()]
-        ev_in, ev_in_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
-        ev_done, ev_out_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
-        counter = {"step": 0, "fwd": 0}
+        ev_in_ready, ev_done, ev_out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        used = {"done": [False, False], "out": [False, False]}
+        e2e_graphs = []
 
-        def cache_copy(cb):
-            # the cache of a coming step into buffer cb, once that buffer's previous prepare is done
-            with torch.cuda.stream(s_cache):
-                s_cache.wait_event(ev_cache_free[cb])
-                d_kc[cb].copy_(h_kc, non_blocking=True)
-                d_vc[cb].copy_(h_vc, non_blocking=True)
-                ev_cache[cb].record(s_cache)
+        def upload(slot):
+            # a step's inputs into `slot`, once the step that last read it has finished
+            with torch.cuda.stream(s_in):
+                if used["done"][slot]:
+                    s_in.wait_event(ev_done[slot])
+                for k in keys:
+                    d_in[slot][k].copy_(h_in[k], non_blocking=True)
+                if kc is not None:
+                    d_kc[slot].copy_(h_kc, non_blocking=True)
+                    d_vc[slot].copy_(h_vc, non_blocking=True)
+                ev_in_ready[slot].record(s_in)
 
-        def e2e_step():
-            cb = counter["step"] % 2
-            counter["step"] += 1
+        def compute(slot):
+            # one step on the inputs of `slot`: the cache conversion, then the 48 forwards
             if kc is not None:
-                stream.wait_event(ev_cache[cb])
-                plan.cache_prepare(d_kc[cb], d_vc[cb])
-                ev_cache_free[cb].record(stream)
-                cache_copy(cb ^ 1)                  # the next step's cache
-            for i, hc in enumerate(h_canv):
-                b = counter["fwd"] % NB
-                counter["fwd"] += 1
-                with torch.cuda.stream(s_in):
-                    s_in.wait_event(ev_in_free[b])
-                    for k, v in hc.items():
-                        if v is not None:
-                            d_in[b][k].copy_(v, non_blocking=True)
-                    ev_in[b].record(s_in)
-                stream.wait_event(ev_in[b])
-                stream.wait_event(ev_out_free[b])
-                plan.forward(d_in[b]["q"], d_in[b]["k_canvas"], d_in[b]["v_canvas"], None, None,
-                             d_in[b]["q_norm_w"], d_in[b]["k_norm_w"], None, d_out[b])
-                ev_in_free[b].record(stream)
-                ev_done[b].record(stream)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_done[b])
-                    h_out[i].copy_(d_out[b], non_blocking=True)
-                    ev_out_free[b].record(s_out)
+                plan.cache_prepare(d_kc[slot], d_vc[slot])
+            x = d_in[slot]
+            for i in range(n_fwd):
+                plan.forward(x["q"][i], x["k_canvas"][i], x["v_canvas"][i], None, None,
+                             x["q_norm_w"][i] if "q_norm_w" in x else None,
+                             x["k_norm_w"][i] if "k_norm_w" in x else None, None,
+                             d_out[slot][i])
 
-        if kc is not None:
-            cache_copy(0)
-        e2e_step()
+        # each slot's step is captured once into a CUDA graph and replayed, as in the timed
+        # region above (the events stay outside the graphs, at step boundaries): enqueuing the
+        # forwards one by one cost the host ~45 us each, nearly what they take on the device
+        run_compute = []
+        for slot in range(2):
+            if args.no_graph:
+                run_compute.append(lambda slot=slot: compute(slot))
+            else:
+                g_ = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_):
+                    compute(slot)
+                run_compute.append(g_.replay)
+                e2e_graphs.append(g_)
+
+        def e2e_run(n_steps):
+            upload(0)
+            for st in range(n_steps):
+                slot = st % 2
+                if st + 1 < n_steps:
+                    upload(slot ^ 1)                # the next step's inputs, during this step
+                stream.wait_event(ev_in_ready[slot])
+                if used["out"][slot]:
+                    stream.wait_event(ev_out_free[slot])
+                run_compute[slot]()
+                ev_done[slot].record(stream)
+                used["done"][slot] = True
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[slot])
+                    h_out.copy_(d_out[slot], non_blocking=True)
+                    ev_out_free[slot].record(s_out)
+                used["out"][slot] = True
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
+
+        e2e_run(2)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        s_in.wait_event(e0)
-        s_out.wait_event(e0)
         h0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        e2e_run(args.e2e_steps)
         host_ms = (time.perf_counter() - h0) * 1e3 / args.e2e_steps
-        stream.wait_stream(s_in)
-        stream.wait_stream(s_out)
-        stream.wait_stream(s_cache)
         e1.record(stream)
         torch.cuda.synchronize()
         if plan.sync_status() != B.DG_OK:
@@ -663,14 +675,18 @@ def main():
         if rank == 0:
             checked["e2e"] = [check_rows(w, 0, h_out[0], args.path),
                               check_rows(w, n_fwd - 1, h_out[n_fwd - 1], args.path)]
+        del run_compute, e2e_graphs
         ems, e2e_flops = replicas.aggregate(e0.elapsed_time(e1), flops_step * args.e2e_steps,
                                             dev if world > 1 else None)
         e2e = {"value": replicas.throughput(ems, e2e_flops) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ems / args.e2e_steps, "host_enqueue_ms_per_step": host_ms,
-               "overlap": "canvas copies on two streams, four buffers deep against the "
-                          "forwards; the next step's cache copied on a third stream during this "
-                          "step"}
+               "steps": args.e2e_steps,
+               "cuda_graph": not args.no_graph,
+               "overlap": "a step's canvases and cache upload while the step before it "
+                          "computes and its outputs download while the step after it computes "
+                          "(two device slots of each, events at step boundaries only); the "
+                          "first upload and the last download are timed unoverlapped"}
 
     launches_per_step = (1 if w.ctx > 0 else 0) + n_fwd * (plan.get(B.DG_INFO_LAUNCHES)
                                                            + (1 if args.hidden else 0)
