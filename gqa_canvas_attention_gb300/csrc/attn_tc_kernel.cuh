@@ -117,11 +117,6 @@ template <int HD> struct Layout {
 constexpr float kRescaleThreshold = 15.0f;
 constexpr float kHeadroom = 0.0f;
 
-// Rows [r0, r0 + nr) of the in-cluster merge of P partitions: out = sum_p w_p O_p with the
-// per-row weights w (already divided by the merged denominator).  The peers' staged O rows are
-// read through distributed shared memory, whose latency is long: each thread takes U float4
-// columns (of different rows) at once, so U * P loads are in flight per thread.  The CTA's own
-// rows (partition `self`) are read through the local shared-memory path.
 // Four output values as the bf16 hi / lo pair the o_proj GEMM takes (hi = bf16(o),
 // lo = bf16(o - hi)), at element i of the two [T, nh*hd] arrays.
 __device__ __forceinline__ void store_split4(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i,
@@ -138,6 +133,11 @@ __device__ __forceinline__ void store_split4(__nv_bfloat16 *hi, __nv_bfloat16 *l
                                                     *reinterpret_cast<const uint32_t *>(&l23));
 }
 
+// Rows [r0, r0 + nr) of the in-cluster merge of P partitions: out = sum_p w_p O_p with the
+// per-row weights w (already divided by the merged denominator).  The peers' staged O rows are
+// read through distributed shared memory, whose latency is long: each thread takes U float4
+// columns (of different rows) at once, so U * P loads are in flight per thread.  The CTA's own
+// rows (partition `self`) are read through the local shared-memory path.
 template <int P, int HD, int THREADS, int PITCH, bool SPLIT>
 __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int self, int r0, int nr,
                                                    const float *wgt, float *const *dst,
