@@ -1405,6 +1405,7 @@ int dg_attn_forward_layer(dg_attn_plan *p, float *resid, const float *k_cache,
         return DG_ERR_STATE;
     }
     // the attention kernel writes o_proj's bf16 operand split itself where it writes the output
+    // (then attn_buf is left unwritten: nothing after it reads the fp32 rows)
     bool split = false;
     if (int rc = forward_hidden_impl(p, resid, k_cache, v_cache, q_norm_w, k_norm_w, cos_sin,
                                      p->attn_buf, s, &split))

@@ -178,18 +178,20 @@ __device__ __forceinline__ void cluster_merge_rows(uint32_t smem_base, int self,
                 acc.z = fmaf(w, v[u][q].z, acc.z);
                 acc.w = fmaf(w, v[u][q].w, acc.w);
             }
-            *reinterpret_cast<float4 *>(d + 4 * (item % V4)) = acc;
             if constexpr (SPLIT)
                 store_split4(out_hi, out_lo, (size_t)(d - out) + 4 * (item % V4), acc);
+            else
+                *reinterpret_cast<float4 *>(d + 4 * (item % V4)) = acc;
         }
     }
 }
 
 // SK: the stream-K schedule (a CTA may hold two pieces); its bookkeeping is compiled only into
 // that instantiation (it costs the split schedule ~2% at hd = 256 otherwise).  SPLIT (split
-// schedule only): the CTAs that write output rows also write their bf16 hi / lo split into
-// p.out_hi / p.out_lo; an instantiation of its own, since even an untaken branch there cost the
-// kernel 1-2.5%.
+// schedule only): the CTAs that write output rows write their bf16 hi / lo split into
+// p.out_hi / p.out_lo instead of the fp32 rows (the o_proj GEMM reads only the split; an SM
+// sends ~13.5 bytes per cycle, so every byte written counts); an instantiation of its own, since
+// even an untaken branch there cost the kernel 1-2.5%.
 template <int HD, bool SK, bool SPLIT = false>
 __global__ void __launch_bounds__(Layout<HD>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
@@ -827,10 +829,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnTcParams p)
                         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mydst), j));
                     if (d) {
                         const float4 o4 = *reinterpret_cast<const float4 *>(stage + j * 36 + 4 * sub);
-                        *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) = o4;
                         if constexpr (SPLIT)
                             store_split4(p.out_hi, p.out_lo,
                                          (size_t)(d - p.out) + 32 * c + 4 * sub, o4);
+                        else
+                            *reinterpret_cast<float4 *>(d + 32 * c + 4 * sub) = o4;
                     }
                 }
                 __syncwarp();

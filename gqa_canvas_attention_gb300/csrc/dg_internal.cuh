@@ -112,7 +112,7 @@ struct AttnTcParams {
     // to part_o / part_ml at slot = its rank among the CTAs of that pair
     int sk_ctas, qtiles;
     long long sk_units;
-    __nv_bfloat16 *out_hi, *out_lo;// null, or [T, nh*hd] beside out: its bf16 hi / lo split
+    __nv_bfloat16 *out_hi, *out_lo;// null, or [T, nh*hd] in place of out: its bf16 hi / lo split
                                    // (hi = bf16(o), lo = bf16(o - hi)), written by the split
                                    // schedule's CTAs that write output rows (the layer path)
 };
@@ -258,8 +258,9 @@ cudaError_t launch_attn_fp32(const AttnFp32Params &p, int hd, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnTcParams &p, const TcMaps &maps, int hd, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t attn_tc_prepare(int hd);   // one-time function attributes (smem opt-in)
-// The split-schedule variant that also writes o_proj's bf16 hi/lo operands (p.out_hi/out_lo;
-// hd 128 and 256): its own launch with the configuration launch_attn_tc built, and its attributes.
+// The split-schedule variant that writes o_proj's bf16 hi/lo operands (p.out_hi/out_lo) in place
+// of the fp32 rows (hd 128 and 256): its own launch with the configuration launch_attn_tc built,
+// and its attributes.
 cudaError_t launch_attn_tc_split(const cudaLaunchConfig_t &cfg, const TcMaps &maps,
                                  const AttnTcParams &p, int hd);
 cudaError_t attn_tc_split_prepare(int hd);
