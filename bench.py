@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--path", default="tc", choices=["tc", "fp32"])
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--e2e-steps", type=int, default=80)
     ap.add_argument("--hidden", type=int, default=0,
                     help="run each forward from a residual stream of this width through the "
                          "projection step (input norm + q/k/v projections) instead of from q/k/v")
