@@ -19,6 +19,12 @@
 // Roles: warp 0 TMA producer (6-stage ring), warp 1 MMA issuer and TMEM owner, warps 2-9
 // epilogue (two threads per token row = TMEM lane, each taking half of the columns).  Every
 // mbarrier wait is bounded.
+//
+// Every kernel here is launched with programmatic dependent launch: it lets the next kernel of
+// the stream be scheduled at once and waits for the one before it (pdl_wait) after its own set-up
+// and before it touches any data, so launches and set-ups overlap the tail of the kernel ahead.
+// A kernel is launched only once every CTA of the one before it has started, so CTAs scheduled
+// early never keep that one from running.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -42,6 +48,8 @@ __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
     // one CTA per token row: r_t and the bf16 hi/lo split of the row (each thread's loads of the
     // row are issued together)
     __shared__ float red[8];
+    pdl_launch_dependents();
+    pdl_wait();
     const int t = blockIdx.x;
     const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)t * p.H);
     uint2 *xh = reinterpret_cast<uint2 *>(p.xh + (size_t)t * p.H);
@@ -165,32 +173,44 @@ __device__ __forceinline__ void store_q_rows(__nv_bfloat16 *tile_base, int r, in
 // of maps.xh / maps.xl, B rows brow0..brow0+63 and brow1..brow1+63 of maps.wh / maps.wl, in
 // kStepK-wide steps of the contraction through a kProjStages ring.
 
-// TMA producer (one thread): returns false when a wait ran out.
+// TMA producer (one thread): returns false when a wait ran out.  The weights were prepared
+// before the kernel ahead of this one started, so the first stages' W panels are requested
+// before this thread waits for that kernel (pdl_wait), and the activation panels after it.
 __device__ __forceinline__ bool gemm_load_loop(uint8_t *smem, uint64_t *full, uint64_t *empty,
                                                const ProjMaps &maps, int m0, int brow0, int brow1,
                                                int nk, uint64_t limit, int b_rows = 128)
 {
     // brow1 >= 0: two boxes of 64 W rows; brow1 < 0: one box of b_rows rows from brow0
     const uint32_t tx = 2 * kPanelBytes + 2 * (uint32_t)b_rows * kStepK * 2;
-    bool ok = true;
-    int issued[kProjStages] = {};
-    for (int it = 0; it < nk; ++it) {
-        const int s = it % kProjStages;
-        if (it >= kProjStages && !mbar_wait_bounded(&empty[s], ((it / kProjStages) - 1) & 1, limit)) {
-            ok = false;
-            break;
-        }
+    auto load_w = [&](int it) {
+        const int s = it % kProjStages, k0 = it * kStepK;
         uint8_t *st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], tx);
-        const int k0 = it * kStepK;
-        tma_load_3d(st, &maps.xh, &full[s], k0, m0, 0);
-        tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], k0, m0, 0);
         tma_load_3d(st + 2 * kPanelBytes, &maps.wh, &full[s], k0, brow0, 0);
         tma_load_3d(st + 3 * kPanelBytes, &maps.wl, &full[s], k0, brow0, 0);
         if (brow1 >= 0) {
             tma_load_3d(st + 2 * kPanelBytes + kPanelBytes / 2, &maps.wh, &full[s], k0, brow1, 0);
             tma_load_3d(st + 3 * kPanelBytes + kPanelBytes / 2, &maps.wl, &full[s], k0, brow1, 0);
         }
+    };
+    const int pre = nk < kProjStages ? nk : kProjStages;
+    for (int it = 0; it < pre; ++it) load_w(it);
+    pdl_wait();
+    bool ok = true;
+    int issued[kProjStages] = {};
+    for (int it = 0; it < nk; ++it) {
+        const int s = it % kProjStages;
+        if (it >= pre) {
+            if (!mbar_wait_bounded(&empty[s], ((it / kProjStages) - 1) & 1, limit)) {
+                ok = false;
+                break;
+            }
+            load_w(it);
+        }
+        uint8_t *st = smem + s * kStageBytes;
+        const int k0 = it * kStepK;
+        tma_load_3d(st, &maps.xh, &full[s], k0, m0, 0);
+        tma_load_3d(st + kPanelBytes, &maps.xl, &full[s], k0, m0, 0);
         ++issued[s];
     }
     // let every load issued here land before the CTA can exit
@@ -281,6 +301,11 @@ qkv_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tacc = *tmem_slot;
+    // (the producer thread waits inside gemm_load_loop, after its weight requests)
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     // Epilogue: eight warps, two per TMEM lane quarter.  Thread (row r, half h) takes columns
     // 32h..32h+31 of each of the two groups (RoPE partners stay in one thread).
@@ -505,6 +530,11 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tacc = *tmem_slot;
+    // (the producer thread waits inside gemm_load_loop, after its weight requests)
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     if (warp == 0) {
         if (lane == 0 && !gemm_load_loop(smem, full, empty, maps, m0, n0, -1, nk, limit, N))
@@ -567,6 +597,8 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
 // resid = (resid + y (mean y^2 + eps)^-1/2 w) * scale, one CTA per token row.
 __global__ void __launch_bounds__(256) post_norm_kernel(PostNormParams p)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     float ss = 0.f;     // every warp sums the row's partial sums itself
@@ -598,13 +630,14 @@ cudaError_t launch_proj_hd(const ProjParams &p, const ProjMaps &maps, int n_tile
     cfg.blockDim = dim3(kQkvThreads);
     cfg.dynamicSmemBytes = kProjSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = HD == 256 ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = HD == 256 ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = HD == 256 ? 1 : 0;
+    cfg.numAttrs = HD == 256 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, qkv_proj_kernel<HD>, maps, p);
 }
 
@@ -647,28 +680,46 @@ int oproj_tile_n(int H, int T, int num_sms)
     return best;
 }
 
+// A launch configuration with programmatic dependent launch on stream s.
+static cudaLaunchConfig_t pdl_config(dim3 grid, int threads, size_t smem, cudaStream_t s,
+                                     cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0] = pdl_attribute();
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 cudaError_t launch_oproj(const OprojParams &p, const ProjMaps &maps, cudaStream_t s)
 {
-    const dim3 grid(p.H / p.tile_n, (p.T + kTileM - 1) / kTileM);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        pdl_config(dim3(p.H / p.tile_n, (p.T + kTileM - 1) / kTileM), kProjThreads, kProjSmem, s, attr);
     switch (p.tile_n) {
-    case 128: oproj_kernel<128><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
-    case 80: oproj_kernel<80><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
-    case 64: oproj_kernel<64><<<grid, kProjThreads, kProjSmem, s>>>(maps, p); break;
+    case 128: return cudaLaunchKernelEx(&cfg, oproj_kernel<128>, maps, p);
+    case 80: return cudaLaunchKernelEx(&cfg, oproj_kernel<80>, maps, p);
+    case 64: return cudaLaunchKernelEx(&cfg, oproj_kernel<64>, maps, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_post_norm(const PostNormParams &p, cudaStream_t s)
 {
-    post_norm_kernel<<<p.T, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3(p.T), 256, 0, s, attr);
+    return cudaLaunchKernelEx(&cfg, post_norm_kernel, p);
 }
 
 cudaError_t launch_hidden_prep(const ProjPrepParams &p, cudaStream_t s)
 {
-    hidden_prep_kernel<<<p.T, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3(p.T), 256, 0, s, attr);
+    return cudaLaunchKernelEx(&cfg, hidden_prep_kernel, p);
 }
 
 cudaError_t launch_proj_weights(const ProjWeightParams &p, cudaStream_t s)
