@@ -20,11 +20,13 @@
 // epilogue (two threads per token row = TMEM lane, each taking half of the columns).  Every
 // mbarrier wait is bounded.
 //
-// Every kernel here is launched with programmatic dependent launch: it lets the next kernel of
-// the stream be scheduled at once and waits for the one before it (pdl_wait) after its own set-up
-// and before it touches any data, so launches and set-ups overlap the tail of the kernel ahead.
-// A kernel is launched only once every CTA of the one before it has started, so CTAs scheduled
-// early never keep that one from running.
+// Every kernel here is launched with programmatic dependent launch: after its own set-up it waits
+// for the kernel before it (pdl_wait) and only then lets the next kernel of the stream be
+// scheduled, so launches and set-ups overlap the tail of the kernel ahead.  Because no kernel
+// signals before its wait, everything enqueued ahead of a kernel's predecessor has completed
+// by the time the kernel starts: the GEMM producers rely on that when they request the prepared
+// weights before their own wait.  A kernel is launched only once every CTA of the one before it
+// has started, so CTAs scheduled early never keep that one from running.
 #include "dg_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -48,8 +50,8 @@ __global__ void __launch_bounds__(256) hidden_prep_kernel(ProjPrepParams p)
     // one CTA per token row: r_t and the bf16 hi/lo split of the row (each thread's loads of the
     // row are issued together)
     __shared__ float red[8];
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.x;
     const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)t * p.H);
     uint2 *xh = reinterpret_cast<uint2 *>(p.xh + (size_t)t * p.H);
@@ -597,8 +599,8 @@ oproj_kernel(const __grid_constant__ ProjMaps maps, const OprojParams p)
 // resid = (resid + y (mean y^2 + eps)^-1/2 w) * scale, one CTA per token row.
 __global__ void __launch_bounds__(256) post_norm_kernel(PostNormParams p)
 {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     float ss = 0.f;     // every warp sums the row's partial sums itself
