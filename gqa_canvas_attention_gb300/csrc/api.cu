@@ -150,6 +150,11 @@ struct dg_attn_plan {
     // first stage writes the set the previous forward's attention kernel is not reading.
     OperandSet op, alt;
     bool alt_cache;              // alt holds the prepared cache rows too
+    // A cache conversion was enqueued after the last attention kernel.  The attention kernel
+    // loads cache rows before its dependency wait only when they were written before the kernel
+    // ahead of it started, which the first-stage kernel (it signals before it waits) does not
+    // guarantee for a conversion right before it: the next attention kernel waits first.
+    bool cache_fresh;
     unsigned long long attn_launched;   // tensor-core attention kernels enqueued
     float *part_o;
     float2 *part_ml;
@@ -544,7 +549,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         a.splits = splits; a.tiles_per_split = tps; a.n_tiles = nt;
         a.cluster_combine = !stream_k && cluster_combine(p, splits) ? 1 : 0;
         a.inject_stall = p->inject_stall;
-        a.static_keys = fresh_cache ? 0 : p->ctx;
+        a.static_keys = fresh_cache || p->cache_fresh ? 0 : p->ctx;
         if (split && p->split_attn && p->aoh && !stream_k && (splits == 1 || a.cluster_combine)) {
             a.out_hi = p->aoh;
             a.out_lo = p->aol;
@@ -557,6 +562,7 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         err = dg::launch_attn_tc(a, p->op.maps, p->hd, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
         ++p->attn_launched;
+        p->cache_fresh = false;
         if (split) *split = a.out_hi != nullptr;
     } else {
         dg::AttnFp32Params a{};
@@ -637,6 +643,7 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);
         if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
+        p->cache_fresh = true;
         if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
     }
     return DG_OK;
@@ -1002,6 +1009,7 @@ int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void
     }
     cudaError_t err = dg::launch_cache_prep(c, s);
     if (err != cudaSuccess) return cuda_fail(err, "cache conversion launch");
+    p->cache_fresh = true;
     if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
     p->alt_cache = p->path == DG_PATH_TC && p->alt.qh;
     if (p->path == DG_PATH_FP32) {
