@@ -650,14 +650,18 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
 }
 
 // Without a caller's table the first stage reads the plan's cos|sin table, rebuilt on the stream
-// (ahead of the work that reads it) after a change of position.
-int rope_table(dg_attn_plan *p, const float *&cos_sin, cudaStream_t s)
+// (ahead of the work that reads it) after a change of position.  *built: the table was enqueued
+// just now, so a first stage launched next must wait for it before reading anything (with
+// resident inputs it would otherwise read the table before its dependency wait).
+int rope_table(dg_attn_plan *p, const float *&cos_sin, cudaStream_t s, bool *built = nullptr)
 {
+    if (built) *built = false;
     if (cos_sin) return DG_OK;
     if (p->rope_dirty) {
         cudaError_t err = dg::launch_rope_table(p->rope_cs, p->inv_freq, p->T, p->hd, p->pos0, s);
         if (err != cudaSuccess) return cuda_fail(err, "cos/sin table launch");
         p->rope_dirty = false;
+        if (built) *built = true;
     }
     cos_sin = p->rope_cs;
     return DG_OK;
@@ -1058,11 +1062,13 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
     auto run = [&]() -> int {
         bool fused;
         if (int rc = resolve_cache(p, k_cache, v_cache, s, &fused)) return rc;
-        if (int rc = rope_table(p, cos_sin, s)) return rc;
+        bool built;
+        if (int rc = rope_table(p, cos_sin, s, &built)) return rc;
         dg::NormRopeParams n = norm_params(p);
         n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w;
         n.cos_sin = cos_sin;
         n.other_set = other;
+        if (built) n.inputs_resident = 0;
         if (fused) fuse_cache(p, n, k_cache, v_cache);
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
         int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
@@ -1094,10 +1100,12 @@ int dg_attn_norm_rope(dg_attn_plan *p, const float *q, const float *k_canvas,
                                   {{q, qb}, {k_canvas, kb}, {v_canvas, kb}, {q_norm_w, wb},
                                    {k_norm_w, wb}, {cos_sin, 2 * (size_t)p->T * wb}}))
         return rc;
-    if (int rc = rope_table(p, cos_sin, s)) return rc;
+    bool built;
+    if (int rc = rope_table(p, cos_sin, s, &built)) return rc;
     dg::NormRopeParams n = norm_params(p);
     n.q = q; n.k = k_canvas; n.v = v_canvas; n.wq = q_norm_w; n.wk = k_norm_w; n.cos_sin = cos_sin;
     n.q_out = q_hat; n.k_out = k_hat; n.v_out = v_hat;
+    if (built) n.inputs_resident = 0;
     cudaError_t err = dg::launch_norm_rope(n, p->hd, dg::kOutFp32, s);
     if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
     return DG_OK;
