@@ -136,6 +136,8 @@ struct dg_attn_plan {
     int inject_stall;
     int inputs_resident;
     int device, num_sms;
+    int smem_per_sm, smem_reserved;     // shared memory of an SM, reserved per block
+    int attn_ctas;                      // CTAs of the last tensor-core attention launch
     bool tc_ok;
     // clusters of s CTAs (s = 2..8) the tensor-core kernel can hold at once (0: not launchable)
     int max_clusters[dg::kMaxClusterSplits + 1];
@@ -563,6 +565,8 @@ int enqueue_attention(dg_attn_plan *p, const float *k_cache, const float *v_cach
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core attention launch");
         ++p->attn_launched;
         p->cache_fresh = false;
+        p->attn_ctas = a.sk_ctas ? a.sk_ctas
+                                 : ((a.rows + dg::kTileM - 1) / dg::kTileM) * a.nkv * a.splits;
         if (split) *split = a.out_hi != nullptr;
     } else {
         dg::AttnFp32Params a{};
@@ -647,6 +651,24 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
         if ((rc = record_event(p, DG_STAGE_CACHE, s))) return rc;
     }
     return DG_OK;
+}
+
+// A first stage that runs beside the previous forward's attention kernel (resident inputs, the
+// other operand set) asks for shared memory it does not use: just enough that none of its blocks
+// fits on an SM holding an attention CTA, when that kernel's grid leaves SMs idle and a few KB
+// suffice.  Its blocks then run on the idle SMs and leave the attention kernel's SMs alone (on
+// the 48-step hd = 256 workload 0.8 us per forward; where the attention grid covers every SM the
+// stage keeps all of them).
+size_t beside_smem(const dg_attn_plan *p, const dg::NormRopeParams &n)
+{
+    if (p->path != DG_PATH_TC || !n.inputs_resident || !n.other_set || p->attn_ctas <= 0 ||
+        p->attn_ctas >= p->num_sms)
+        return 0;
+    const long long free_bytes = (long long)p->smem_per_sm - (long long)dg::attn_tc_smem_bytes(p->hd) -
+                                 p->smem_reserved;
+    if (free_bytes < p->smem_reserved) return 0;     // no block fits beside an attention CTA
+    const long long need = free_bytes - p->smem_reserved + 128;
+    return need <= 8192 ? (size_t)need : 0;
 }
 
 // Without a caller's table the first stage reads the plan's cos|sin table, rebuilt on the stream
@@ -735,6 +757,8 @@ dg_attn_plan *dg_attn_plan_create(int nh, int nkv, int hd, int ctx, int T, float
     p->wait_limit_ms = 2000;
     p->device = dev;
     p->num_sms = prop.multiProcessorCount;
+    p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
+    p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
 
     const size_t nq = (size_t)T * nh * hd, nk = (size_t)T * nkv * hd;
     p->inv_freq = (float4 *)dalloc(p, sizeof(float4) * (hd / 2), err);
@@ -1073,7 +1097,7 @@ int dg_attn_forward(dg_attn_plan *p, const float *q, const float *k_canvas, cons
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
         int rc = record_event(p, DG_STAGE_NORM_ROPE, s);
         if (rc) return rc;
-        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s, beside_smem(p, n));
         if (err != cudaSuccess) return cuda_fail(err, "norm/rope launch");
         if ((rc = record_event(p, DG_STAGE_NORM_ROPE, s))) return rc;
         return enqueue_attention(p, k_cache, v_cache, out, s, fused);
@@ -1139,7 +1163,7 @@ int dg_attn_attend(dg_attn_plan *p, const float *q_hat, const float *k_hat, cons
         if (fused) fuse_cache(p, n, k_cache, v_cache);
         n.do_norm = 0; n.do_rope = 0;
         const int mode = p->path == DG_PATH_TC ? dg::kOutTc : dg::kOutFp32;
-        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s);
+        cudaError_t err = dg::launch_norm_rope(n, p->hd, mode, s, beside_smem(p, n));
         if (err != cudaSuccess) return cuda_fail(err, "operand layout launch");
         return enqueue_attention(p, k_cache, v_cache, out, s, fused);
     };

@@ -249,7 +249,10 @@ template <class F> cudaError_t once_per_device(std::atomic<unsigned long long> &
 constexpr int kNormCacheUnroll = 4;
 
 // Host launchers (return cudaGetLastError()).
-cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s);
+// smem_bytes: dynamic shared memory each block asks for and does not use (see beside_smem in
+// the plan code), 0 normally.
+cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s,
+                             size_t smem_bytes = 0);
 // cos|sin table [T, 2*hd] of the positions pos0 .. pos0 + T - 1 (layout of a caller's table).
 cudaError_t launch_rope_table(float *cs, const float4 *inv_freq, int T, int hd, long long pos0,
                               cudaStream_t s);

@@ -403,7 +403,7 @@ __global__ void rope_table_kernel(float *cs, const float4 *inv_freq, int T, int 
 }
 
 template <int HD>
-cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
+cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s, size_t smem_bytes)
 {
     const int jobs = p.nh + 2 * p.nkv;
     const int chunks = (jobs + kChunkRows<HD> - 1) / kChunkRows<HD>;
@@ -411,6 +411,7 @@ cudaError_t launch_hd(const NormRopeParams &p, int mode, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((warps + 3) / 4 + p.cache_blocks));
     cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
@@ -433,13 +434,14 @@ cudaError_t launch_rope_table(float *cs, const float4 *inv_freq, int T, int hd, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s)
+cudaError_t launch_norm_rope(const NormRopeParams &p, int hd, int mode, cudaStream_t s,
+                             size_t smem_bytes)
 {
     switch (hd) {
-    case 32: return launch_hd<32>(p, mode, s);
-    case 64: return launch_hd<64>(p, mode, s);
-    case 128: return launch_hd<128>(p, mode, s);
-    case 256: return launch_hd<256>(p, mode, s);
+    case 32: return launch_hd<32>(p, mode, s, smem_bytes);
+    case 64: return launch_hd<64>(p, mode, s, smem_bytes);
+    case 128: return launch_hd<128>(p, mode, s, smem_bytes);
+    case 256: return launch_hd<256>(p, mode, s, smem_bytes);
     default: return cudaErrorInvalidValue;
     }
 }
