@@ -642,7 +642,8 @@ int resolve_cache(dg_attn_plan *p, const float *&k_cache, const float *&v_cache,
             return DG_OK;
         }
         dg::CachePrepParams c{k_cache, v_cache, p->op.kh, p->op.kl, p->op.vh, nullptr, nullptr,
-                              p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32, p->status};
+                              p->nkv, p->ctx, p->S, p->S_pad, p->hd, dg::kCacheF32, p->status,
+                              nullptr, nullptr, nullptr};
         int rc = record_event(p, DG_STAGE_CACHE, s);
         if (rc) return rc;
         cudaError_t err = dg::launch_cache_prep(c, s);

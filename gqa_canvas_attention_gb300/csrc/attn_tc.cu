@@ -70,7 +70,7 @@ TcGeom tc_geometry(int hd)
     case 64: return {Cfg<64>::NK, Cfg<64>::VK, Cfg<64>::QL_TMEM};
     case 128: return {Cfg<128>::NK, Cfg<128>::VK, Cfg<128>::QL_TMEM};
     case 256: return {Cfg<256>::NK, Cfg<256>::VK, Cfg<256>::QL_TMEM};
-    default: return {0, 0};
+    default: return {0, 0, false};
     }
 }
 
