@@ -1011,7 +1011,8 @@ int dg_attn_cache_prepare_typed(dg_attn_plan *p, const void *k_cache, const void
     const int type = dtype == DG_DTYPE_F16 ? dg::kCacheF16
                    : dtype == DG_DTYPE_BF16 ? dg::kCacheBf16 : dg::kCacheF32;
     dg::CachePrepParams c{k_cache, v_cache, p->op.kh, p->op.kl, p->op.vh, nullptr, nullptr,
-                          p->nkv, p->ctx, p->S, p->S_pad, p->hd, type, p->status};
+                          p->nkv, p->ctx, p->S, p->S_pad, p->hd, type, p->status,
+                          nullptr, nullptr, nullptr};
     if (p->path == DG_PATH_FP32) {
         if (dtype == DG_DTYPE_F32) {
             p->prep_k = static_cast<const float *>(k_cache);
