@@ -266,7 +266,9 @@ int dg_attn_oproj_residual(dg_attn_plan *plan, const float *attn_out, float *res
 
 /* The whole attention branch of a decoder layer on the residual stream resid [T, H], in place:
  * input norm and projections (dg_attn_proj_prepare), the block, o_proj, post-attention norm and
- * residual add (dg_attn_oproj_prepare, same H).  The block's output is kept in the plan. */
+ * residual add (dg_attn_oproj_prepare, same H).  The block's output stays inside the plan and
+ * is not returned: as o_proj's bf16 hi/lo operands, written by the attention kernel itself, or
+ * in fp32 first under the schedules that finish in a combine kernel. */
 int dg_attn_forward_layer(dg_attn_plan *plan, float *resid, const float *k_cache,
                           const float *v_cache, const float *q_norm_w, const float *k_norm_w,
                           const float *cos_sin, cudaStream_t stream);
