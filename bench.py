@@ -698,6 +698,10 @@ def main():
     if not args.no_side and not args.hidden and world == 1:
         side = side_workloads(B, dev, args, attn_peak, peaks)
 
+    # the capture is of the default run's kernel (the auto schedule, the instantiation without
+    # the o_proj operand split)
+    traffic = (attn_traffic() if tc and w.name == "denoise48_ctx8k" and not args.hidden
+               and not args.splits else None)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
@@ -710,10 +714,9 @@ def main():
         "canvas_steps_per_s": n_fwd * args.steps * world / (ms / 1e3),
         "roofline": {"bound": attn_bound, "achieved": attn_tflops, "peak": attn_peak,
                      "unit": "TFLOP/s", "frac": attn_tflops / attn_peak,
-                     # the capture is of the default run's kernel (the auto schedule, the
-                     # instantiation without the o_proj operand split)
-                     "traffic": (attn_traffic() if tc and w.name == "denoise48_ctx8k"
-                                 and not args.hidden and not args.splits else None),
+                     "traffic": traffic,
+                     # DRAM rate: the captured bytes per launch over the kernel time above
+                     "dram_gbs": traffic / (kern_us * 1e-6) / 1e9 if traffic else None,
                      "kernel": "attn_tc_kernel" if tc else "attn_fp32_kernel",
                      "peak_source": peak_src,
                      "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"] if tc else None,
